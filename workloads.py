@@ -1,0 +1,200 @@
+"""Seeded synthetic attention inputs (Q, K, V in fp16), shared by the tests and the bench.
+
+This module only draws random numbers and rounds them to fp16. It holds none of the
+attention arithmetic: the oracle (``oracle/``) and the CUDA path each receive the
+arrays it returns and nothing else.
+
+The input families follow the two overflow causes named in the abstract of
+"Online Pseudo-average Shifting Attention (PASA) for Robust Low-precision LLM Inference:
+Algorithms and Numerical Analysis" (arXiv 2503.01873): a large bias of K along the
+sequence dimension (the Qwen2-7B case) and Q/K "resonance", i.e. Q and K channels that
+oscillate in phase or 180 degrees out of phase (the Stable-Video-Diffusion case). The
+real activations are not available, so these distributions stand in for them:
+
+* ``iid``        Q, K, V ~ N(0, 1).
+* ``kbias``      Q, V ~ N(0, 1); K = N(0, 1) + b, one bias vector b ~ N(0, bias_std^2)
+                 per (batch, kv-head), added to every K row.
+* ``kbias_t3``   Q, V ~ N(0, 1); K = b + t_scale * T, b ~ N(0, bias_std^2) per
+                 (batch, kv-head) and channel, T iid Student-t with ``t_dof`` degrees.
+* ``resonance``  Q[t, d] = A sin(w_d t + phi_d) + N(0, noise_std^2),
+                 K[t, d] = A sin(w_d t + phi_d + delta_d) + N(0, noise_std^2),
+                 delta_d in {0, pi}; w_d, phi_d, delta_d drawn per (batch, head); V ~ N(0, 1).
+                 ``freq`` picks w_d: "uniform_pi" (U(0, pi)), "rope" (10000^(-2d/D)),
+                 "slow" (U(0, 0.01)). ``phase_flip`` False keeps every delta_d = 0.
+
+Every value is drawn in float64 from numpy's PCG64 and rounded once to fp16
+(round-to-nearest-even). Arrays are laid out [B, H, S, D], C-contiguous.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    Sq: int
+    Sk: int
+    D: int
+    causal: bool
+    kind: str
+    seed: int
+    params: tuple = ()
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+    def flops(self) -> float:
+        """FlashAttention FLOP convention: 4*B*Hq*Sq*Sk*D, counting only visible pairs when causal."""
+        return 4.0 * self.B * self.Hq * self.visible_pairs() * self.D
+
+    def visible_pairs(self) -> int:
+        if not self.causal:
+            return self.Sq * self.Sk
+        # bottom-right aligned mask: key j visible to query i iff j <= i + Sk - Sq
+        off = self.Sk - self.Sq
+        total = 0
+        for i in range(self.Sq):
+            total += max(0, min(self.Sk, i + off + 1))
+        return total
+
+    def with_shape(self, **kw) -> "Workload":
+        return dataclasses.replace(self, **kw)
+
+
+def _p(**kw):
+    return tuple(sorted(kw.items()))
+
+
+# The five workloads the method is measured on, plus resonance variants.
+WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("iid_b1h1_s128_d64", 1, 1, 1, 128, 128, 64, False, "iid", 1001),
+        Workload("kbias20_b1h28g4_s4096_d128_causal", 1, 28, 4, 4096, 4096, 128, True,
+                 "kbias", 1002, _p(bias_std=20.0)),
+        Workload("resonance_a30_b2h5_s9216_d64", 2, 5, 5, 9216, 9216, 64, False,
+                 "resonance", 1003, _p(A=30.0, noise_std=0.5, freq="uniform_pi", phase_flip=True)),
+        Workload("iid_b4h32g8_s8192_d128_causal", 4, 32, 8, 8192, 8192, 128, True, "iid", 1004),
+        Workload("kbias10_t3_b1h28g4_s32768_d128_causal", 1, 28, 4, 32768, 32768, 128, True,
+                 "kbias_t3", 1005, _p(bias_std=10.0, t_scale=4.0, t_dof=3)),
+        # resonance variants: RoPE-like and slow frequencies
+        Workload("resonance_rope_a30_b2h5_s9216_d64", 2, 5, 5, 9216, 9216, 64, False,
+                 "resonance", 1013, _p(A=30.0, noise_std=0.5, freq="rope", phase_flip=True)),
+        Workload("resonance_slow_a30_b2h5_s9216_d64", 2, 5, 5, 9216, 9216, 64, False,
+                 "resonance", 1023, _p(A=30.0, noise_std=0.5, freq="slow", phase_flip=True)),
+        # overflow demonstration: slow in-phase resonance with A = 48 pushes raw scores past 65504
+        Workload("resonance_hot_a48_b2h5_s9216_d64", 2, 5, 5, 9216, 9216, 64, False,
+                 "resonance", 1033, _p(A=48.0, noise_std=0.5, freq="slow", phase_flip=False)),
+    ]
+}
+
+# The order the five measured workloads are listed in.
+MEASURED = [
+    "iid_b1h1_s128_d64",
+    "kbias20_b1h28g4_s4096_d128_causal",
+    "resonance_a30_b2h5_s9216_d64",
+    "iid_b4h32g8_s8192_d128_causal",
+    "kbias10_t3_b1h28g4_s32768_d128_causal",
+]
+
+
+def _f16(x: np.ndarray) -> np.ndarray:
+    return np.asarray(x, dtype=np.float64).astype(np.float16)
+
+
+def make_inputs(w: Workload, seed: int | None = None):
+    """Return (q, k, v) as fp16 numpy arrays [B, H, S, D] for workload ``w``.
+
+    The same seed always gives the same bytes. Generation is per (batch, head), in the
+    order Q heads, then K heads, then V heads, from one PCG64 stream per tensor.
+    """
+    params = dict(w.params)
+    seed = w.seed if seed is None else seed
+    ss = np.random.SeedSequence(seed)
+    sq, sk, sv, sp = ss.spawn(4)
+    rq = np.random.Generator(np.random.PCG64(sq))
+    rk = np.random.Generator(np.random.PCG64(sk))
+    rv = np.random.Generator(np.random.PCG64(sv))
+    rp = np.random.Generator(np.random.PCG64(sp))  # per-head parameters (bias, frequencies)
+
+    q = np.empty((w.B, w.Hq, w.Sq, w.D), np.float16)
+    k = np.empty((w.B, w.Hkv, w.Sk, w.D), np.float16)
+    v = np.empty((w.B, w.Hkv, w.Sk, w.D), np.float16)
+
+    if w.kind == "resonance":
+        if w.Hq != w.Hkv:
+            raise ValueError("resonance inputs pair each query head with its own key head")
+        A = float(params["A"])
+        ns = float(params["noise_std"])
+        freq = params["freq"]
+        flip = bool(params["phase_flip"])
+        for b in range(w.B):
+            for h in range(w.Hq):
+                if freq == "uniform_pi":
+                    wd = rp.uniform(0.0, math.pi, w.D)
+                elif freq == "rope":
+                    wd = 10000.0 ** (-2.0 * np.arange(w.D) / w.D)
+                elif freq == "slow":
+                    wd = rp.uniform(0.0, 0.01, w.D)
+                else:
+                    raise ValueError(freq)
+                phi = rp.uniform(0.0, 2.0 * math.pi, w.D)
+                delta = np.where(rp.random(w.D) < 0.5, math.pi, 0.0) if flip else np.zeros(w.D)
+                tq = np.arange(w.Sq, dtype=np.float64)[:, None]
+                tk = np.arange(w.Sk, dtype=np.float64)[:, None]
+                q[b, h] = _f16(A * np.sin(wd * tq + phi) + ns * rq.standard_normal((w.Sq, w.D)))
+                k[b, h] = _f16(A * np.sin(wd * tk + phi + delta) + ns * rk.standard_normal((w.Sk, w.D)))
+        for b in range(w.B):
+            for h in range(w.Hkv):
+                v[b, h] = _f16(rv.standard_normal((w.Sk, w.D)))
+        return q, k, v
+
+    for b in range(w.B):
+        for h in range(w.Hq):
+            q[b, h] = _f16(rq.standard_normal((w.Sq, w.D)))
+    for b in range(w.B):
+        for h in range(w.Hkv):
+            if w.kind == "iid":
+                k[b, h] = _f16(rk.standard_normal((w.Sk, w.D)))
+            elif w.kind == "kbias":
+                bias = rp.normal(0.0, float(params["bias_std"]), w.D)
+                k[b, h] = _f16(rk.standard_normal((w.Sk, w.D)) + bias)
+            elif w.kind == "kbias_t3":
+                bias = rp.normal(0.0, float(params["bias_std"]), w.D)
+                t = rk.standard_t(float(params["t_dof"]), (w.Sk, w.D))
+                k[b, h] = _f16(bias + float(params["t_scale"]) * t)
+            else:
+                raise ValueError(w.kind)
+    for b in range(w.B):
+        for h in range(w.Hkv):
+            v[b, h] = _f16(rv.standard_normal((w.Sk, w.D)))
+    return q, k, v
+
+
+def sample_rows(w: Workload, n: int, seed: int = 7, block_rows: int = 128) -> np.ndarray:
+    """Flat row indices ((b*Hq + h)*Sq + i) to compare on at full size.
+
+    Always includes the first and last row of every head, rows on both sides of
+    every ``block_rows`` boundary of the first head, and ``n`` uniformly drawn rows.
+    """
+    rng = np.random.Generator(np.random.PCG64(seed))
+    rows = set()
+    for b in range(w.B):
+        for h in range(w.Hq):
+            base = (b * w.Hq + h) * w.Sq
+            rows.add(base)
+            rows.add(base + w.Sq - 1)
+    for i in range(block_rows, w.Sq, block_rows * max(1, w.Sq // (block_rows * 8))):
+        rows.add(i - 1)
+        rows.add(i)
+    total = w.B * w.Hq * w.Sq
+    rows.update(int(x) for x in rng.integers(0, total, n))
+    return np.array(sorted(rows), dtype=np.int64)
