@@ -1,0 +1,375 @@
+"""Benchmark: PASA attention forward TFLOP/s on GB300, fraction of the tensor-core peak.
+
+One step = the whole hot path on one batch of synthetic input already resident in HBM:
+the pseudo-average shift of K (kshift kernel) followed by the attention kernel, both
+through the C ABI (pasa_kshift, pasa_attn_fwd_shifted). FLOPs follow the FlashAttention
+convention (4 * B * Hq * visible (query, key) pairs * D). The e2e figure goes through
+pasa_attn_fwd with host buffers: pinned host -> device copies of q, k, v, the call, and
+device -> host copies of o and lse, all inside the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--mode M]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on this host's cores
+
+Prints one JSON line (rank 0). Under torchrun (N > 1) every rank runs its own replica of
+the workload on its own GPU (weak scaling: the work is independent per (batch, head), so
+there is no data-path collective); value = all ranks' FLOPs / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as wl  # noqa: E402
+
+DEFAULT_WORKLOAD = "kbias10_t3_b1h28g4_s32768_d128_causal"
+ALSO_WORKLOADS = ["iid_b4h32g8_s8192_d128_causal"]
+MODE_NAMES = {0: "shift_f16acc", 1: "shift_f32acc", 2: "naive_f16acc", 3: "noshift_f32acc"}
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def __enter__(self):
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for _, _, flags in rows for n, f in zip(names, flags) if f.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def visible_pairs_rows(w: wl.Workload, rows: np.ndarray) -> np.ndarray:
+    i = rows % w.Sq
+    if not w.causal:
+        return np.full(len(rows), w.Sk, np.int64)
+    return np.clip(i + w.Sk - w.Sq + 1, 0, w.Sk)
+
+
+def cpu_oracle_sample(w: wl.Workload, q, k, v, budget_s: float, seed: int = 0):
+    """Time the fp64 oracle on random rows of the workload for about `budget_s` seconds."""
+    import oracle
+
+    rng = np.random.default_rng(seed)
+    total_rows = w.B * w.Hq * w.Sq
+    n = 16
+    elapsed, flops, rows_done = 0.0, 0.0, 0
+    while elapsed < budget_s:
+        rows = np.sort(rng.integers(0, total_rows, n)).astype(np.int64)
+        t0 = time.perf_counter()
+        oracle.attention(q, k, v, causal=w.causal, rows=rows)
+        dt = time.perf_counter() - t0
+        elapsed += dt
+        flops += float(4.0 * w.D * visible_pairs_rows(w, rows).sum())
+        rows_done += n
+        n = int(min(max(n * 2, 16), max(16, n * (budget_s - elapsed) / max(dt, 1e-3))))
+        if budget_s - elapsed < 0.2 * dt:
+            break
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    threads = int(os.environ.get("OMP_NUM_THREADS", cores))
+    return {
+        "value": flops / elapsed / 1e12,
+        "unit": "TFLOP/s",
+        "cores": threads,
+        "kind": "oracle",
+        "sample": f"{rows_done} random query rows of {w.name} (fp64 oracle, all visible keys), {elapsed:.1f} s",
+    }
+
+
+def bench_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int, also: bool = False):
+    import torch
+
+    import precision_flashattention_numerics_gb300 as pasa
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    q, k, v = wl.make_inputs(w, seed=w.seed + 7919 * rank)
+    qt, kt, vt = (torch.from_numpy(x).to(dev) for x in (q, k, v))
+    o = torch.empty_like(qt)
+    lse = torch.empty((w.B, w.Hq, w.Sq), device=dev, dtype=torch.float32)
+    nb = (w.Sk + pasa.block_rows() - 1) // pasa.block_rows()
+    shift = args.mode in (0, 1)
+    ks = torch.empty_like(kt) if shift else kt
+    means = torch.empty((w.B, w.Hkv, nb, w.D), device=dev, dtype=torch.float16) if shift else None
+    stream = torch.cuda.current_stream()
+
+    def step():
+        if shift:
+            pasa.kshift(kt, out=ks, means=means)
+        pasa.attn_fwd_shifted(qt, ks, means, vt, causal=w.causal, mode=args.mode, out=o, lse=lse)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    pasa.check_device_error()
+
+    n = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    sampler = ClockSampler(local_rank) if not also else None
+    if sampler:
+        sampler.__enter__()
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(n):
+        ev[i][0].record(stream)
+        if shift:
+            pasa.kshift(kt, out=ks, means=means)
+        ev[i][1].record(stream)
+        pasa.attn_fwd_shifted(qt, ks, means, vt, causal=w.causal, mode=args.mode, out=o, lse=lse)
+        ev[i][2].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    if sampler:
+        sampler.__exit__(None, None, None)
+    pasa.check_device_error()
+    total_ms = t_start.elapsed_time(t_end)
+    total_ms = max_over_ranks(total_ms, world)
+    attn_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(n)]
+    kshift_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(n)] if shift else [0.0] * n
+    flops = w.flops()
+    finite = bool(torch.isfinite(o).all().item())
+    res = {
+        "total_ms": total_ms,
+        "ms_per_step": total_ms / n,
+        "attn_ms": statistics.mean(attn_ms),
+        "kshift_ms": statistics.mean(kshift_ms),
+        "flops": flops,
+        "tflops": flops * n * world / (total_ms * 1e-3) / 1e12,
+        "attn_tflops": flops / (statistics.mean(attn_ms) * 1e-3) / 1e12,
+        "finite": finite,
+        "clocks": sampler.summary() if sampler else None,
+        "host": (q, k, v),
+    }
+    if also:
+        return res
+
+    # end to end through pasa_attn_fwd with host buffers (copies inside the timed region)
+    qh, kh, vh = (torch.from_numpy(x).pin_memory() for x in (q, k, v))
+    oh = torch.empty(qt.shape, dtype=torch.float16).pin_memory()
+    lh = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        qt.copy_(qh, non_blocking=True)
+        kt.copy_(kh, non_blocking=True)
+        vt.copy_(vh, non_blocking=True)
+        pasa.attn_fwd_alloc(qt, kt, vt, causal=w.causal, mode=args.mode, out=o, lse=lse)
+        oh.copy_(o, non_blocking=True)
+        lh.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    n_e2e = max(2, min(n, 5))
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    pasa.check_device_error()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    res["e2e"] = {
+        "value": flops * n_e2e * world / (e2e_ms * 1e-3) / 1e12,
+        "unit": "TFLOP/s",
+        "h2d_bytes_per_step": int(q.nbytes + k.nbytes + v.nbytes),
+        "d2h_bytes_per_step": int(oh.numel() * 2 + lh.numel() * 4),
+        "ms_per_step": e2e_ms / n_e2e,
+    }
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="pasa", choices=["pasa", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--mode", type=int, default=0, choices=[0, 1, 2, 3])
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-also", action="store_true")
+    args = ap.parse_args()
+
+    rank, world, local_rank = dist_env()
+    w = wl.WORKLOADS[args.workload]
+    peaks, peak_src = load_peaks()
+    config = {
+        "workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk, "D": w.D,
+        "causal": w.causal, "inputs": w.kind, "mode": MODE_NAMES[args.mode],
+        "l2": "inputs larger than L2 (129 MB); no flush between steps",
+        "flop_convention": "4*B*Hq*visible_pairs*D",
+    }
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        q, k, v = wl.make_inputs(w)
+        steps = []
+        per_step_budget = max(1.0, min(args.cpu_budget, 60.0) / max(1, args.steps))
+        for s in range(max(0, args.warmup) + args.steps):
+            r = cpu_oracle_sample(w, q, k, v, budget_s=per_step_budget if s >= args.warmup else 0.5, seed=s)
+            if s >= args.warmup:
+                steps.append(r)
+        val = statistics.mean(r["value"] for r in steps)
+        out = {
+            "impl": "reference", "metric": "PASA attn fwd TFLOP/s (fp64 CPU oracle)", "value": val,
+            "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": None, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic", "config": config,
+            "cpu_baseline": {**steps[-1], "value": val},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }
+        print(json.dumps(out))
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    res = bench_gpu(args, w, rank, world, local_rank)
+    also = {}
+    if not args.no_also and world == 1:
+        for name in ALSO_WORKLOADS:
+            if name == w.name:
+                continue
+            wa = wl.WORKLOADS[name]
+            ra = bench_gpu(args, wa, rank, world, local_rank, also=True)
+            also[name] = {"tflops": round(ra["tflops"], 1), "ms_per_step": round(ra["ms_per_step"], 4),
+                          "attn_ms": round(ra["attn_ms"], 4), "kshift_ms": round(ra["kshift_ms"], 4),
+                          "finite": ra["finite"]}
+
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))  # fp16 dense = bf16 dense rate
+    attn_achieved = res["flops"] / (res["attn_ms"] * 1e-3) / 1e12
+    roofline = {
+        "kernel": "attn_fwd_kernel", "bound": "tensor", "achieved": round(attn_achieved, 1), "peak": peak,
+        "unit": "TFLOP/s", "frac": round(attn_achieved / peak, 4), "traffic": None,
+        "peak_source": f"{peak_src} bf16 dense burst (fp16 dense has the same nominal rate)",
+    }
+    kshift_kernel = None
+    if args.mode in (0, 1):
+        kb = 2 * (w.B * w.Hkv * w.Sk * w.D * 2) + w.B * w.Hkv * math.ceil(w.Sk / 112) * w.D * 2
+        gbs = kb / (res["kshift_ms"] * 1e-3) / 1e9
+        hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        kshift_kernel = {"kernel": "kshift_kernel", "bound": "hbm", "achieved": round(gbs, 1), "peak": hbm,
+                         "unit": "GB/s", "frac": round(gbs / hbm, 4), "bytes_per_launch": kb,
+                         "ms": round(res["kshift_ms"], 5)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        q, k, v = res["host"]
+        cpu = cpu_oracle_sample(w, q, k, v, budget_s=args.cpu_budget)
+
+    if rank == 0:
+        out = {
+            "metric": "PASA attn fwd TFLOP/s at 1 GB300 (fraction of dense fp16 tensor peak in roofline)",
+            "value": round(res["tflops"], 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": round(res["ms_per_step"], 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic", "config": config,
+            "roofline": roofline, "kshift": kshift_kernel, "cpu_baseline": cpu, "e2e": res["e2e"],
+            "gpu_launches": args.steps * (2 if args.mode in (0, 1) else 1), "clocks": res["clocks"],
+            "finite_output": res["finite"], "also": also,
+        }
+        print(json.dumps(out))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,136 @@
+/*
+ * pasa.h — C ABI of the PASA attention forward library (libpasa.so, sm_103a / GB300).
+ *
+ * PASA: "Online Pseudo-average Shifting Attention (PASA) for Robust Low-precision LLM
+ * Inference: Algorithms and Numerical Analysis" (arXiv 2503.01873), Abstract. A
+ * FlashAttention forward pass in half precision in which each key block is shifted by its
+ * pseudo-average along the sequence before the fp16 score GEMM ("online pseudo-average
+ * shifting") and the per-row offsets q_i . m_j are added back in fp32 inside the online
+ * softmax ("global recovering"). The result equals plain attention
+ *     O = softmax(scale * Q K^T) V,   LSE_i = ln sum_j exp(scale * q_i . k_j)
+ * up to rounding, while the fp16 scores stay far from the fp16 limit 65504.
+ *
+ * Conventions shared by every entry point:
+ *   - Tensors are device pointers to contiguous row-major arrays, fp16 = IEEE binary16:
+ *       q, o  [B, Hq,  Sq, D]      k, v  [B, Hkv, Sk, D]      lse [B, Hq, Sq] fp32
+ *     Query head h reads key/value head h / (Hq / Hkv) (grouped-query attention).
+ *   - Every device pointer must be 16-byte aligned (TMA), else PASA_ERR_ALIGN.
+ *   - The caller owns all buffers; entry points never free or keep them.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream). Work is enqueued
+ *     asynchronously: a PASA_OK return means "validated and launched", like a CUDA kernel
+ *     launch. Argument errors are detected on the host before anything is enqueued.
+ *   - Device-side failures (a pipeline wait that timed out) are latched in a device error
+ *     word and reported by pasa_check_device_error().
+ *   - Supported: D in {64, 128}; B, Hq, Hkv, Sq, Sk >= 1; Hq % Hkv == 0; a GPU of compute
+ *     capability 10.3 (sm_103a). Anything else returns an error and launches nothing.
+ *   - Causal masking is bottom-right aligned: key j is visible to query i iff
+ *     j <= i + Sk - Sq. A query row with no visible key gets O = 0 and LSE = -inf.
+ */
+#ifndef PASA_H_
+#define PASA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes (return values). */
+#define PASA_OK 0
+#define PASA_ERR_NULLPTR (-1)     /* a required pointer is NULL */
+#define PASA_ERR_SHAPE (-2)       /* a size is <= 0, Hq % Hkv != 0, or a size overflows */
+#define PASA_ERR_UNSUPPORTED (-3) /* D not in {64,128}, unknown mode, or not an sm_103 GPU */
+#define PASA_ERR_ALIGN (-4)       /* a pointer is not 16-byte aligned */
+#define PASA_ERR_CUDA (-5)        /* a CUDA runtime/driver call failed (see pasa_last_cuda_error) */
+#define PASA_ERR_TIMEOUT (-6)     /* a device-side pipeline wait gave up (pasa_check_device_error) */
+#define PASA_ERR_WORKSPACE (-7)   /* workspace NULL or smaller than pasa_attn_fwd_workspace_bytes */
+
+/* Score modes (the `mode` argument). */
+#define PASA_MODE_SHIFT_F16ACC 0   /* PASA: shifted keys, fp16-accumulated scores, fp32 offsets */
+#define PASA_MODE_SHIFT_F32ACC 1   /* PASA shift with fp32-accumulated scores */
+#define PASA_MODE_NAIVE_F16ACC 2   /* no shift, fp16-accumulated scores: shows the fp16 overflow */
+#define PASA_MODE_NOSHIFT_F32ACC 3 /* no shift, fp32-accumulated scores: plain FlashAttention */
+
+/* Rows per key block: the block the pseudo-average is taken over (112). */
+int pasa_block_rows(void);
+
+/*
+ * PASA attention forward (the whole hot path: pseudo-average shift of K, then the fused
+ * attention kernel). Abstract of the PASA paper: "online pseudo-average shifting" and
+ * "global recovering" inside a FlashAttention forward pass.
+ *
+ *   q, k, v   fp16 inputs (layout above); o fp16 output [B, Hq, Sq, D].
+ *   lse       fp32 output [B, Hq, Sq], natural-log sum of exp of the scaled scores; may
+ *             be NULL to skip it.
+ *   causal    0 or 1 (bottom-right aligned mask).
+ *   scale     softmax scale; <= 0 selects 1/sqrt(D).
+ *   mode      PASA_MODE_* above. Modes 0 and 1 need a workspace for the shifted keys and
+ *             block means: this entry point takes it from the CUDA stream-ordered allocator
+ *             (cudaMallocAsync / cudaFreeAsync on `stream`); use pasa_attn_fwd_ws to pass
+ *             your own.
+ * Overflow in mode 2 is not an error: it shows up as inf/NaN in o, which is the point of
+ * that mode.
+ */
+int pasa_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                  int Sq, int Sk, int D, int causal, float scale, int mode, void* stream);
+
+/* Workspace bytes pasa_attn_fwd_ws needs for these sizes and mode (0 for modes 2 and 3). */
+size_t pasa_attn_fwd_workspace_bytes(int B, int Hkv, int Sk, int D, int mode);
+
+/*
+ * Same as pasa_attn_fwd with a caller-owned device workspace of at least
+ * pasa_attn_fwd_workspace_bytes(B, Hkv, Sk, D, mode) bytes, 256-byte aligned. Its
+ * contents on entry do not matter; it must not be used by other work until the stream
+ * has passed this call.
+ */
+int pasa_attn_fwd_ws(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                     int Sq, int Sk, int D, int causal, float scale, int mode, void* workspace,
+                     size_t workspace_bytes, void* stream);
+
+/*
+ * The attention kernel alone, on keys already shifted by pasa_kshift (for modes 0 and 1:
+ * k_shifted and means exactly as pasa_kshift wrote them for the same k) or on raw keys
+ * (modes 2 and 3: pass k as k_shifted; means is ignored and may be NULL). This is the
+ * second half of pasa_attn_fwd; callers that keep shifted keys (a KV cache) skip the shift.
+ * Arguments as in pasa_attn_fwd; means is fp16 [B, Hkv, ceil(Sk / pasa_block_rows()), D].
+ */
+int pasa_attn_fwd_shifted(const void* q, const void* k_shifted, const void* means, const void* v, void* o,
+                          float* lse, int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,
+                          int mode, void* stream);
+
+/*
+ * The pseudo-average shift step alone (PASA Abstract, "online pseudo-average shifting"),
+ * exposed for testing and diagnostics. For every key block j of pasa_block_rows() rows
+ * (the last block may be shorter) and channel d it writes
+ *     means[b, h, j, d]   the block's pseudo-average m_j[d] (fp16)
+ *     k_shifted[b, h, r, d] = fp16_rn(k[b, h, r, d] - m_j[d])
+ * where m_j[d] = g * round_half_even(sum_r round_half_even(k[r,d] / g) / n), g the fp16
+ * spacing at max_r |k[r,d]| and n the block's row count; m_j[d] = 0 when that maximum is
+ * >= 32768 or the block/channel holds inf or NaN.
+ *   k          fp16 [B, H, Sk, D]        k_shifted  fp16 [B, H, Sk, D]
+ *   means      fp16 [B, H, ceil(Sk / pasa_block_rows()), D]
+ */
+int pasa_kshift(const void* k, void* k_shifted, void* means, int B, int H, int Sk, int D, void* stream);
+
+/*
+ * Synchronise `stream` and read the device error word. Returns PASA_OK, PASA_ERR_TIMEOUT
+ * (a pipeline wait gave up; `info`, if not NULL, receives the CTA index << 32 | wait site)
+ * or PASA_ERR_CUDA. Reading the word clears it.
+ */
+int pasa_check_device_error(void* stream, unsigned long long* info);
+
+/* Human-readable text for a status code (static storage). */
+const char* pasa_strerror(int status);
+
+/* The cudaError_t of the most recent failed CUDA call in this thread (0 if none). */
+int pasa_last_cuda_error(void);
+
+/* 1 if `device` can run this library (compute capability 10.3), else 0. */
+int pasa_device_supported(int device);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PASA_H_ */

@@ -1,0 +1,192 @@
+"""PASA attention forward for GB300 (sm_103a): Python binding of libpasa.so.
+
+The binding only marshals arguments: it checks dtypes/devices, allocates outputs and the
+workspace with PyTorch, and calls the C ABI (include/pasa.h) on the current CUDA stream.
+Every step of the computation runs in the library's CUDA kernels. If libpasa.so is missing
+the calls raise; there is no fallback.
+
+Method: "Online Pseudo-average Shifting Attention (PASA) for Robust Low-precision LLM
+Inference" (arXiv 2503.01873), Abstract.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = [
+    "MODE_SHIFT_F16ACC", "MODE_SHIFT_F32ACC", "MODE_NAIVE_F16ACC", "MODE_NOSHIFT_F32ACC",
+    "PasaError", "attn_fwd", "attn_fwd_alloc", "attn_fwd_shifted", "kshift", "workspace_bytes", "check_device_error", "block_rows",
+    "library", "library_path",
+]
+
+MODE_SHIFT_F16ACC = 0
+MODE_SHIFT_F32ACC = 1
+MODE_NAIVE_F16ACC = 2
+MODE_NOSHIFT_F32ACC = 3
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_HERE, "libpasa.so")
+_lock = threading.Lock()
+_lib = None
+
+# exported symbols and their ctypes signatures, mirroring include/pasa.h
+_P, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "pasa_block_rows": ([], _I),
+    "pasa_attn_fwd": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P], _I),
+    "pasa_attn_fwd_workspace_bytes": ([_I, _I, _I, _I, _I], _SZ),
+    "pasa_attn_fwd_ws": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P], _I),
+    "pasa_attn_fwd_shifted": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P], _I),
+    "pasa_kshift": ([_P, _P, _P, _I, _I, _I, _I, _P], _I),
+    "pasa_check_device_error": ([_P, ctypes.POINTER(ctypes.c_ulonglong)], _I),
+    "pasa_strerror": ([_I], ctypes.c_char_p),
+    "pasa_last_cuda_error": ([], _I),
+    "pasa_device_supported": ([_I], _I),
+}
+
+
+class PasaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        lib = library()
+        msg = lib.pasa_strerror(status).decode()
+        if status == -5:
+            msg += f" (cudaError {lib.pasa_last_cuda_error()})"
+        super().__init__(f"{where}: {msg} [status {status}]")
+        self.status = status
+
+
+def library():
+    """Load libpasa.so (built by __graft_entry__.build()); raises if it is not there."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(library_path):
+                raise RuntimeError(f"{library_path} is missing: build it with "
+                                   "`python -c 'import __graft_entry__ as g; g.build()'`")
+            lib = ctypes.CDLL(library_path)
+            for name, (args, res) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = lib
+    return _lib
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _check(x: torch.Tensor, name: str):
+    if not isinstance(x, torch.Tensor) or not x.is_cuda or x.dtype != torch.float16 or not x.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous CUDA fp16 tensor")
+
+
+def block_rows() -> int:
+    return library().pasa_block_rows()
+
+
+def workspace_bytes(B: int, Hkv: int, Sk: int, D: int, mode: int) -> int:
+    return int(library().pasa_attn_fwd_workspace_bytes(B, Hkv, Sk, D, mode))
+
+
+def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, mode: int = MODE_SHIFT_F16ACC,
+             out=None, lse=None, return_lse: bool = True, workspace=None):
+    """O, LSE of softmax(scale * Q K^T) V via libpasa (q [B,Hq,Sq,D], k/v [B,Hkv,Sk,D], fp16).
+
+    Returns (o fp16 [B,Hq,Sq,D], lse fp32 [B,Hq,Sq] or None). ``mode`` is one of the MODE_*
+    constants. The workspace (modes 0/1) is taken from PyTorch's allocator unless given.
+    """
+    lib = library()
+    _check(q, "q"), _check(k, "k"), _check(v, "v")
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
+        raise ValueError("expected q [B,Hq,Sq,D] and k, v [B,Hkv,Sk,D]")
+    B, Hq, Sq, D = q.shape
+    Bk, Hkv, Sk, Dk = k.shape
+    if Bk != B or Dk != D:
+        raise ValueError("q and k disagree on B or D")
+    if out is None:
+        out = torch.empty_like(q)
+    if return_lse and lse is None:
+        lse = torch.empty((B, Hq, Sq), device=q.device, dtype=torch.float32)
+    if not return_lse:
+        lse = None
+    nbytes = int(lib.pasa_attn_fwd_workspace_bytes(B, Hkv, Sk, D, mode))
+    if nbytes and workspace is None:
+        workspace = torch.empty(nbytes, device=q.device, dtype=torch.uint8)
+    rc = lib.pasa_attn_fwd_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Sk, D,
+                              int(bool(causal)), float(scale) if scale is not None else 0.0, int(mode),
+                              _ptr(workspace) if nbytes else None,
+                              workspace.numel() * workspace.element_size() if nbytes else 0, _stream())
+    if rc != 0:
+        raise PasaError(rc, "pasa_attn_fwd_ws")
+    return out, lse
+
+
+def attn_fwd_alloc(q, k, v, causal: bool = False, scale: float | None = None, mode: int = MODE_SHIFT_F16ACC,
+                   out=None, lse=None):
+    """Like attn_fwd, through pasa_attn_fwd (the library takes its own stream-ordered workspace)."""
+    lib = library()
+    _check(q, "q"), _check(k, "k"), _check(v, "v")
+    B, Hq, Sq, D = q.shape
+    _, Hkv, Sk, _ = k.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Sq), device=q.device, dtype=torch.float32)
+    rc = lib.pasa_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Sk, D,
+                           int(bool(causal)), float(scale) if scale is not None else 0.0, int(mode), _stream())
+    if rc != 0:
+        raise PasaError(rc, "pasa_attn_fwd")
+    return out, lse
+
+
+def attn_fwd_shifted(q, k_shifted, means, v, causal: bool = False, scale: float | None = None,
+                     mode: int = MODE_SHIFT_F16ACC, out=None, lse=None):
+    """The attention kernel alone on keys from :func:`kshift` (modes 0/1) or raw keys (2/3)."""
+    lib = library()
+    _check(q, "q"), _check(k_shifted, "k_shifted"), _check(v, "v")
+    if means is not None:
+        _check(means, "means")
+    B, Hq, Sq, D = q.shape
+    _, Hkv, Sk, _ = k_shifted.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Sq), device=q.device, dtype=torch.float32)
+    rc = lib.pasa_attn_fwd_shifted(_ptr(q), _ptr(k_shifted), _ptr(means), _ptr(v), _ptr(out), _ptr(lse), B, Hq,
+                                   Hkv, Sq, Sk, D, int(bool(causal)),
+                                   float(scale) if scale is not None else 0.0, int(mode), _stream())
+    if rc != 0:
+        raise PasaError(rc, "pasa_attn_fwd_shifted")
+    return out, lse
+
+
+def kshift(k, out=None, means=None):
+    """The pseudo-average shift step alone: returns (k_shifted [B,H,Sk,D], means [B,H,nb,D])."""
+    lib = library()
+    _check(k, "k")
+    B, H, Sk, D = k.shape
+    nb = (Sk + lib.pasa_block_rows() - 1) // lib.pasa_block_rows()
+    ks = torch.empty_like(k) if out is None else out
+    if means is None:
+        means = torch.empty((B, H, nb, D), device=k.device, dtype=torch.float16)
+    rc = lib.pasa_kshift(_ptr(k), _ptr(ks), _ptr(means), B, H, Sk, D, _stream())
+    if rc != 0:
+        raise PasaError(rc, "pasa_kshift")
+    return ks, means
+
+
+def check_device_error():
+    """Synchronise the current stream; raise PasaError if a kernel reported a timeout."""
+    info = ctypes.c_ulonglong(0)
+    rc = library().pasa_check_device_error(_stream(), ctypes.byref(info))
+    if rc != 0:
+        err = PasaError(rc, f"device (info {info.value:#x})")
+        raise err

@@ -1,0 +1,187 @@
+// Online pseudo-average shifting of the keys (the first PASA step).
+//
+// "Online Pseudo-average Shifting Attention (PASA) for Robust Low-precision LLM Inference"
+// (arXiv 2503.01873), Abstract: every key block is shifted by a pseudo-average along the
+// sequence so that a large bias of K along the sequence cannot drive the fp16 scores past
+// 65504; the offsets q_i . m_j are added back later ("global recovering") in fp32, which
+// keeps the result equal to plain attention. The abstract does not define the
+// pseudo-average; this library uses the following reading (the oracle implements the same
+// reading independently, in numpy):
+//
+//   for key block j (kBlockRows rows, n valid) and channel d:
+//     M = max_r |K[r,d]|            g = fp16 spacing at M (2^(E-25), or 2^-24 if E = 0)
+//     t_r = rint_even(K[r,d] / g)   m = g * rint_even(sum_r t_r / n)   (exact integers)
+//     m = 0 when M >= 2^15 or the block/channel holds inf or NaN
+//     K'[r,d] = fp16_rn(K[r,d] - m)
+//
+// m lies on the grid of the block maximum, so K - m is exact in fp16 for most elements.
+//
+// Kernel shape: one CTA of 256 threads per (batch*kv-head, key block). Each thread owns one
+// 16-byte unit (8 channels) of up to ceil(kBlockRows / row_groups) rows and keeps them in
+// registers; the per-channel max and integer sums are reduced with warp shuffles and a
+// small shared-memory exchange across the 8 warps; the block is read from HBM once and
+// K' written once (HBM-bound: 2 * rows * D * 2 bytes per block).
+#pragma once
+
+#include <cstdint>
+#include <cuda_fp16.h>
+
+namespace pasa {
+
+constexpr int kBlockRows = 112;      // keys per block: the shift block and the attention key tile
+constexpr int kShiftThreads = 256;
+
+// round-half-even(s / n) for integers, n > 0.
+__device__ __forceinline__ int rne_div(int s, int n) {
+  const int a = s < 0 ? -s : s;
+  int q = a / n;
+  const int r = a - q * n;
+  if (2 * r > n || (2 * r == n && (q & 1))) ++q;
+  return s < 0 ? -q : q;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kShiftThreads)
+kshift_kernel(const __half* __restrict__ k, __half* __restrict__ kshift, __half* __restrict__ means, int Sk,
+              int nb) {
+  constexpr int U = D / 8;                       // 16-byte units per row
+  constexpr int R = kShiftThreads / U;           // row groups
+  constexpr int RPT = (kBlockRows + R - 1) / R;  // rows per thread (upper bound)
+  constexpr int NW = kShiftThreads / 32;
+  static_assert(32 % U == 0 || U % 32 == 0, "unit layout");
+  static_assert(U <= 32, "D <= 256");
+
+  __shared__ uint32_t sh_max[NW][U][4];
+  __shared__ uint32_t sh_nf[NW][U][4];
+  __shared__ int sh_sum[NW][U][8];
+
+  const int j = blockIdx.x;
+  const int bh = blockIdx.y;
+  const int tid = threadIdx.x;
+  const int u = tid % U;
+  const int rg = tid / U;
+  const int warp = tid / 32;
+  const int row0 = j * kBlockRows;
+  const int n = min(kBlockRows, Sk - row0);
+
+  const uint4* src = reinterpret_cast<const uint4*>(k + (static_cast<size_t>(bh) * Sk + row0) * D) + u;
+  uint4* dst = reinterpret_cast<uint4*>(kshift + (static_cast<size_t>(bh) * Sk + row0) * D) + u;
+
+  uint4 x[RPT];
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    const int r = rg + i * R;
+    if (r < n) x[i] = __ldg(src + static_cast<size_t>(r) * U);
+    else x[i] = make_uint4(0, 0, 0, 0);
+  }
+
+  // 1. per-channel max |K| over finite values, and a non-finite flag (16-bit lanes)
+  uint32_t mx[4] = {0, 0, 0, 0}, nf[4] = {0, 0, 0, 0};
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    const uint32_t w[4] = {x[i].x, x[i].y, x[i].z, x[i].w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint32_t a = w[c] & 0x7FFF7FFFu;
+      const uint32_t bad = __vcmpgeu2(a, 0x7C007C00u);  // inf or NaN (rows >= n are zero)
+      nf[c] |= bad;
+      mx[c] = __vmaxu2(mx[c], a & ~bad);
+    }
+  }
+#pragma unroll
+  for (int off = U; off < 32; off *= 2) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      mx[c] = __vmaxu2(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], off));
+      nf[c] |= __shfl_xor_sync(0xffffffffu, nf[c], off);
+    }
+  }
+  if ((tid % 32) < U) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      sh_max[warp][u][c] = mx[c];
+      sh_nf[warp][u][c] = nf[c];
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t m = 0, f = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      m = __vmaxu2(m, sh_max[w][u][c]);
+      f |= sh_nf[w][u][c];
+    }
+    mx[c] = m;
+    nf[c] = f;
+  }
+
+  // 2. grid step per channel and the quantised sum
+  float inv_g[8], g[8];
+  bool guard[8];
+#pragma unroll
+  for (int h = 0; h < 8; ++h) {
+    const uint32_t a = (mx[h / 2] >> (16 * (h & 1))) & 0xFFFFu;
+    const int E = static_cast<int>(a >> 10);
+    const int e = E >= 1 ? E - 25 : -24;            // g = 2^e
+    g[h] = __int_as_float((e + 127) << 23);
+    inv_g[h] = __int_as_float((127 - e) << 23);
+    guard[h] = (E >= 30) || (((nf[h / 2] >> (16 * (h & 1))) & 0xFFFFu) != 0);
+  }
+  int sum[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    const __half* hv = reinterpret_cast<const __half*>(&x[i]);
+#pragma unroll
+    for (int h = 0; h < 8; ++h) {
+      const float f = __half2float(hv[h]);
+      // rows >= n hold zeros; non-finite values only occur in guarded channels
+      const float t = isfinite(f) ? f * inv_g[h] : 0.0f;  // exact: power-of-two scale
+      sum[h] += __float2int_rn(t);
+    }
+  }
+#pragma unroll
+  for (int off = U; off < 32; off *= 2) {
+#pragma unroll
+    for (int h = 0; h < 8; ++h) sum[h] += __shfl_xor_sync(0xffffffffu, sum[h], off);
+  }
+  if ((tid % 32) < U) {
+#pragma unroll
+    for (int h = 0; h < 8; ++h) sh_sum[warp][u][h] = sum[h];
+  }
+  __syncthreads();
+
+  // 3. pseudo-average, then 4. K' = fp16_rn(K - m)
+  float mf[8];
+  __half mh[8];
+#pragma unroll
+  for (int h = 0; h < 8; ++h) {
+    int s = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) s += sh_sum[w][u][h];
+    const int mu = rne_div(s, n);
+    mf[h] = guard[h] ? 0.0f : static_cast<float>(mu) * g[h];  // exact, and exactly an fp16 value
+    mh[h] = __float2half_rn(mf[h]);
+  }
+  if (rg == 0) {
+    uint4 mv;
+    __half* mp = reinterpret_cast<__half*>(&mv);
+#pragma unroll
+    for (int h = 0; h < 8; ++h) mp[h] = mh[h];
+    reinterpret_cast<uint4*>(means + (static_cast<size_t>(bh) * nb + j) * D)[u] = mv;
+  }
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    const int r = rg + i * R;
+    if (r < n) {
+      uint4 o;
+      const __half* hv = reinterpret_cast<const __half*>(&x[i]);
+      __half* op = reinterpret_cast<__half*>(&o);
+#pragma unroll
+      for (int h = 0; h < 8; ++h) op[h] = __float2half_rn(__half2float(hv[h]) - mf[h]);
+      dst[static_cast<size_t>(r) * U] = o;
+    }
+  }
+}
+
+}  // namespace pasa

@@ -1,0 +1,302 @@
+// libpasa.so: the C ABI declared in include/pasa.h. Host-side argument validation, TMA
+// descriptor encoding, workspace layout and kernel dispatch. Compiled as one translation
+// unit for sm_103a.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "../../include/pasa.h"
+#include "attn_fwd.cuh"
+#include "kshift.cuh"
+#include "ptx.cuh"
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e) {
+  t_last_cuda_error = static_cast<int>(e);
+  return PASA_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+// 3-D fp16 view [planes, rows, D] of a contiguous tensor, 128-byte swizzled boxes of
+// 64 x box_rows x 1 elements.
+int make_map(CUtensorMap* m, const void* base, int D, long long rows, long long planes, int box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return cuda_fail(cudaErrorNotSupported);
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(planes)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(rows) * D * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+  return PASA_OK;
+}
+
+int check_device() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return pasa_device_supported(dev) ? PASA_OK : PASA_ERR_UNSUPPORTED;
+}
+
+struct WorkspaceLayout {
+  size_t kshift_off, means_off, total;
+};
+
+WorkspaceLayout workspace_layout(int B, int Hkv, int Sk, int D) {
+  const size_t nb = (static_cast<size_t>(Sk) + pasa::kBlockRows - 1) / pasa::kBlockRows;
+  WorkspaceLayout w;
+  w.kshift_off = 0;
+  w.means_off = align_up(static_cast<size_t>(B) * Hkv * Sk * D * 2, 256);
+  w.total = align_up(w.means_off + static_cast<size_t>(B) * Hkv * nb * D * 2, 256);
+  return w;
+}
+
+template <int D>
+int launch_kshift(const void* k, void* ks, void* means, int B, int H, int Sk, cudaStream_t st) {
+  const int nb = (Sk + pasa::kBlockRows - 1) / pasa::kBlockRows;
+  dim3 grid(nb, B * H);
+  pasa::kshift_kernel<D><<<grid, pasa::kShiftThreads, 0, st>>>(
+      static_cast<const __half*>(k), static_cast<__half*>(ks), static_cast<__half*>(means), Sk, nb);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? PASA_OK : cuda_fail(e);
+}
+
+int kshift_dispatch(const void* k, void* ks, void* means, int B, int H, int Sk, int D, cudaStream_t st) {
+  return D == 64 ? launch_kshift<64>(k, ks, means, B, H, Sk, st) : launch_kshift<128>(k, ks, means, B, H, Sk, st);
+}
+
+template <int D, bool F16ACC, bool SHIFT, bool CAUSAL>
+int launch_attn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mo,
+                const CUtensorMap& mm, const pasa::AttnParams& p, cudaStream_t st) {
+  constexpr int KST = D == 128 ? 3 : 4;
+  constexpr int VST = D == 128 ? 2 : 4;
+  using Smem = pasa::AttnSmem<D, KST, VST>;
+  auto kern = pasa::attn_fwd_kernel<D, F16ACC, SHIFT, CAUSAL, KST, VST>;
+  const int smem = static_cast<int>(sizeof(Smem)) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const long long ctas = static_cast<long long>(p.n_qblk) * p.Hq * p.B;
+  kern<<<static_cast<unsigned>(ctas), pasa::kAttnThreads, smem, st>>>(mq, mk, mv, mo, mm, p);
+  e = cudaGetLastError();
+  return e == cudaSuccess ? PASA_OK : cuda_fail(e);
+}
+
+template <int D>
+int attn_dispatch(int mode, int causal, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                  const CUtensorMap& mo, const CUtensorMap& mm, const pasa::AttnParams& p, cudaStream_t st) {
+#define PASA_CASE(MODE, F16, SH)                                                 \
+  case MODE:                                                                     \
+    return causal ? launch_attn<D, F16, SH, true>(mq, mk, mv, mo, mm, p, st)     \
+                  : launch_attn<D, F16, SH, false>(mq, mk, mv, mo, mm, p, st);
+  switch (mode) {
+    PASA_CASE(PASA_MODE_SHIFT_F16ACC, true, true)
+    PASA_CASE(PASA_MODE_SHIFT_F32ACC, false, true)
+    PASA_CASE(PASA_MODE_NAIVE_F16ACC, true, false)
+    PASA_CASE(PASA_MODE_NOSHIFT_F32ACC, false, false)
+    default:
+      return PASA_ERR_UNSUPPORTED;
+  }
+#undef PASA_CASE
+}
+
+int validate(const void* q, const void* k, const void* v, const void* o, const float* lse, int B, int Hq, int Hkv,
+             int Sq, int Sk, int D, int mode) {
+  if (!q || !k || !v || !o) return PASA_ERR_NULLPTR;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Sk <= 0 || Hq % Hkv != 0) return PASA_ERR_SHAPE;
+  if (D != 64 && D != 128) return PASA_ERR_UNSUPPORTED;
+  if (mode < PASA_MODE_SHIFT_F16ACC || mode > PASA_MODE_NOSHIFT_F32ACC) return PASA_ERR_UNSUPPORTED;
+  // grid size, TMA plane counts and flat LSE indices fit in 32-bit signed integers
+  const long long n_qblk = (static_cast<long long>(Sq) + pasa::kCtaRows - 1) / pasa::kCtaRows;
+  if (n_qblk * Hq * B > 0x7fffffffLL) return PASA_ERR_SHAPE;
+  if (static_cast<long long>(B) * Hq > 0x7fffffffLL || static_cast<long long>(B) * Hkv > 0x7fffffffLL)
+    return PASA_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (lse && !aligned16(lse)))
+    return PASA_ERR_ALIGN;
+  return PASA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pasa_block_rows(void) { return pasa::kBlockRows; }
+
+int pasa_last_cuda_error(void) { return t_last_cuda_error; }
+
+int pasa_device_supported(int device) {
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess) return 0;
+  return (major == 10 && minor == 3) ? 1 : 0;
+}
+
+const char* pasa_strerror(int status) {
+  switch (status) {
+    case PASA_OK: return "ok";
+    case PASA_ERR_NULLPTR: return "a required pointer is NULL";
+    case PASA_ERR_SHAPE: return "invalid sizes (<= 0, Hq % Hkv != 0, or too large)";
+    case PASA_ERR_UNSUPPORTED: return "unsupported head dim, mode or device (needs D in {64,128}, sm_103)";
+    case PASA_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+    case PASA_ERR_CUDA: return "a CUDA call failed";
+    case PASA_ERR_TIMEOUT: return "a device pipeline wait timed out";
+    case PASA_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+  }
+}
+
+size_t pasa_attn_fwd_workspace_bytes(int B, int Hkv, int Sk, int D, int mode) {
+  if (B <= 0 || Hkv <= 0 || Sk <= 0 || D <= 0) return 0;
+  if (mode != PASA_MODE_SHIFT_F16ACC && mode != PASA_MODE_SHIFT_F32ACC) return 0;
+  return workspace_layout(B, Hkv, Sk, D).total;
+}
+
+int pasa_kshift(const void* k, void* k_shifted, void* means, int B, int H, int Sk, int D, void* stream) {
+  if (!k || !k_shifted || !means) return PASA_ERR_NULLPTR;
+  if (B <= 0 || H <= 0 || Sk <= 0) return PASA_ERR_SHAPE;
+  if (D != 64 && D != 128) return PASA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * H > 65535) return PASA_ERR_SHAPE;  // grid.y
+  if (!aligned16(k) || !aligned16(k_shifted) || !aligned16(means)) return PASA_ERR_ALIGN;
+  int rc = check_device();
+  if (rc != PASA_OK) return rc;
+  return kshift_dispatch(k, k_shifted, means, B, H, Sk, D, static_cast<cudaStream_t>(stream));
+}
+
+// Launch the attention kernel on (possibly shifted) keys `kk` and block means `mm`.
+static int attn_launch(const void* q, const void* kk, const void* mm, const void* v, void* o, float* lse, int B,
+                       int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale, int mode, cudaStream_t st) {
+  const bool shift = mode == PASA_MODE_SHIFT_F16ACC || mode == PASA_MODE_SHIFT_F32ACC;
+  if (!(scale > 0.0f) || !std::isfinite(scale)) scale = 1.0f / std::sqrt(static_cast<float>(D));
+  const int nb = (Sk + pasa::kBlockRows - 1) / pasa::kBlockRows;
+  int rc;
+  CUtensorMap mq, mk, mv, mo, mmeans;
+  if ((rc = make_map(&mq, q, D, Sq, static_cast<long long>(B) * Hq, pasa::kTileRows)) != PASA_OK) return rc;
+  if ((rc = make_map(&mk, kk, D, Sk, static_cast<long long>(B) * Hkv, pasa::kBlockRows)) != PASA_OK) return rc;
+  if ((rc = make_map(&mv, v, D, Sk, static_cast<long long>(B) * Hkv, pasa::kBlockRows)) != PASA_OK) return rc;
+  if ((rc = make_map(&mo, o, D, Sq, static_cast<long long>(B) * Hq, pasa::kTileRows)) != PASA_OK) return rc;
+  if (shift) {
+    if ((rc = make_map(&mmeans, mm, D, nb, static_cast<long long>(B) * Hkv, pasa::kChunkBlocks)) != PASA_OK)
+      return rc;
+  } else {
+    mmeans = mk;  // unused by the no-shift kernels
+  }
+  pasa::AttnParams p;
+  p.lse = lse;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Sq = Sq;
+  p.Sk = Sk;
+  p.n_qblk = (Sq + pasa::kCtaRows - 1) / pasa::kCtaRows;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  return D == 64 ? attn_dispatch<64>(mode, causal, mq, mk, mv, mo, mmeans, p, st)
+                 : attn_dispatch<128>(mode, causal, mq, mk, mv, mo, mmeans, p, st);
+}
+
+int pasa_attn_fwd_shifted(const void* q, const void* k_shifted, const void* means, const void* v, void* o,
+                          float* lse, int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,
+                          int mode, void* stream) {
+  int rc = validate(q, k_shifted, v, o, lse, B, Hq, Hkv, Sq, Sk, D, mode);
+  if (rc != PASA_OK) return rc;
+  const bool shift = mode == PASA_MODE_SHIFT_F16ACC || mode == PASA_MODE_SHIFT_F32ACC;
+  if (shift && !means) return PASA_ERR_NULLPTR;
+  if (shift && !aligned16(means)) return PASA_ERR_ALIGN;
+  rc = check_device();
+  if (rc != PASA_OK) return rc;
+  return attn_launch(q, k_shifted, shift ? means : k_shifted, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, mode,
+                     static_cast<cudaStream_t>(stream));
+}
+
+int pasa_attn_fwd_ws(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                     int Sq, int Sk, int D, int causal, float scale, int mode, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  int rc = validate(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, mode);
+  if (rc != PASA_OK) return rc;
+  const bool shift = mode == PASA_MODE_SHIFT_F16ACC || mode == PASA_MODE_SHIFT_F32ACC;
+  const WorkspaceLayout wl = workspace_layout(B, Hkv, Sk, D);
+  if (shift) {
+    if (!workspace || workspace_bytes < wl.total) return PASA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PASA_ERR_ALIGN;
+    if (static_cast<long long>(B) * Hkv > 65535) return PASA_ERR_SHAPE;  // kshift grid.y
+  }
+  rc = check_device();
+  if (rc != PASA_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const void* kk = k;
+  const void* mm = k;
+  if (shift) {
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    void* ks = ws + wl.kshift_off;
+    void* means = ws + wl.means_off;
+    rc = kshift_dispatch(k, ks, means, B, Hkv, Sk, D, st);
+    if (rc != PASA_OK) return rc;
+    kk = ks;
+    mm = means;
+  }
+  return attn_launch(q, kk, mm, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, mode, st);
+}
+
+int pasa_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                  int Sq, int Sk, int D, int causal, float scale, int mode, void* stream) {
+  int rc = validate(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, mode);
+  if (rc != PASA_OK) return rc;
+  const size_t bytes = pasa_attn_fwd_workspace_bytes(B, Hkv, Sk, D, mode);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  void* ws = nullptr;
+  if (bytes > 0) {
+    rc = check_device();
+    if (rc != PASA_OK) return rc;
+    cudaError_t e = cudaMallocAsync(&ws, bytes, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  rc = pasa_attn_fwd_ws(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, mode, ws, bytes, stream);
+  if (ws) {
+    cudaError_t e = cudaFreeAsync(ws, st);
+    if (rc == PASA_OK && e != cudaSuccess) rc = cuda_fail(e);
+  }
+  return rc;
+}
+
+int pasa_check_device_error(void* stream, unsigned long long* info) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  int word = 0;
+  unsigned long long inf = 0;
+  e = cudaMemcpyFromSymbol(&word, pasa::g_device_error, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = cudaMemcpyFromSymbol(&inf, pasa::g_device_error_info, sizeof(inf));
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (word == pasa::kDeviceOk) return PASA_OK;
+  const int zero = 0;
+  const unsigned long long zero64 = 0;
+  cudaMemcpyToSymbol(pasa::g_device_error, &zero, sizeof(int));
+  cudaMemcpyToSymbol(pasa::g_device_error_info, &zero64, sizeof(zero64));
+  if (info) *info = inf;
+  return PASA_ERR_TIMEOUT;
+}
+
+}  // extern "C"

@@ -1,0 +1,108 @@
+"""Host-only checks of the C ABI: the library builds, loads and exports every function
+include/pasa.h declares, and argument errors are reported before any launch.
+
+Every call below is rejected by host-side validation, so none reaches a CUDA launch
+(the pointers passed are never dereferenced).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from precision_flashattention_numerics_gb300 import build
+
+    build.build()
+    import precision_flashattention_numerics_gb300 as pasa
+
+    return pasa.library()
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "pasa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pasa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_function(lib):
+    import precision_flashattention_numerics_gb300 as pasa
+
+    names = header_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in pasa.SIGNATURES, f"binding has no signature for {n}"
+
+
+def test_block_rows_and_strings(lib):
+    assert lib.pasa_block_rows() == 112
+    for code in (0, -1, -2, -3, -4, -5, -6, -7):
+        assert lib.pasa_strerror(code)
+    assert lib.pasa_strerror(12345) == b"unknown status"
+
+
+FAKE = 1 << 20          # 16-byte aligned, never dereferenced
+FAKE_MIS = FAKE + 8     # misaligned
+
+
+def call(lib, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, Hq=2, Hkv=1, Sq=64, Sk=64, D=64,
+         causal=0, scale=0.0, mode=3, ws=None, ws_bytes=0):
+    P = ctypes.c_void_p
+    return lib.pasa_attn_fwd_ws(P(q), P(k), P(v), P(o), P(lse), B, Hq, Hkv, Sq, Sk, D, causal, scale, mode,
+                                P(ws) if ws is not None else None, ws_bytes, None)
+
+
+def test_argument_errors(lib):
+    assert call(lib, q=0) == -1
+    assert call(lib, o=0) == -1
+    assert call(lib, B=0) == -2
+    assert call(lib, Sk=-3) == -2
+    assert call(lib, Hq=3, Hkv=2) == -2
+    assert call(lib, D=96) == -3
+    assert call(lib, D=256) == -3
+    assert call(lib, mode=4) == -3
+    assert call(lib, mode=-1) == -3
+    assert call(lib, k=FAKE_MIS) == -4
+    assert call(lib, lse=FAKE_MIS) == -4
+    # modes with the shift need a workspace of the advertised size
+    assert call(lib, mode=0, ws=None) == -7
+    need = lib.pasa_attn_fwd_workspace_bytes(1, 1, 64, 64, 0)
+    assert call(lib, mode=1, ws=FAKE, ws_bytes=need - 1) == -7
+    assert call(lib, mode=1, ws=FAKE + 16, ws_bytes=need) == -4   # workspace must be 256-byte aligned
+    # grid overflow is a shape error
+    assert call(lib, B=65536, Hq=65536, Hkv=1, Sq=1 << 20) == -2
+
+
+def test_kshift_argument_errors(lib):
+    P = ctypes.c_void_p
+    assert lib.pasa_kshift(None, P(FAKE), P(FAKE), 1, 1, 64, 64, None) == -1
+    assert lib.pasa_kshift(P(FAKE), P(FAKE), P(FAKE), 1, 1, 0, 64, None) == -2
+    assert lib.pasa_kshift(P(FAKE), P(FAKE), P(FAKE), 1, 1, 64, 32, None) == -3
+    assert lib.pasa_kshift(P(FAKE_MIS), P(FAKE), P(FAKE), 1, 1, 64, 64, None) == -4
+
+
+def test_workspace_bytes(lib):
+    # shifted keys [B,Hkv,Sk,D] fp16 + means [B,Hkv,ceil(Sk/112),D] fp16, each 256-aligned
+    def expect(B, H, Sk, D):
+        a = -(-(B * H * Sk * D * 2) // 256) * 256
+        nb = -(-Sk // 112)
+        return -(-(a + B * H * nb * D * 2) // 256) * 256
+
+    for (B, H, Sk, D) in [(1, 4, 4096, 128), (2, 5, 9216, 64), (1, 1, 1, 64), (4, 8, 8192, 128)]:
+        for mode in (0, 1):
+            assert lib.pasa_attn_fwd_workspace_bytes(B, H, Sk, D, mode) == expect(B, H, Sk, D)
+        for mode in (2, 3):
+            assert lib.pasa_attn_fwd_workspace_bytes(B, H, Sk, D, mode) == 0
+
+
+def test_no_device_here_is_reported_not_launched(lib):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert lib.pasa_device_supported(0) == 0

@@ -1,0 +1,229 @@
+"""GPU parity of the attention forward pass against the fp64 oracle.
+
+"Online Pseudo-average Shifting Attention (PASA) for Robust Low-precision LLM Inference"
+(arXiv 2503.01873), Abstract: PASA is mathematically equivalent to plain attention, keeps
+fp16 scores from overflowing (65504) under large sequence-dimension bias and Q/K
+resonance, and is judged by RMSE against high-precision attention. Tolerances (output
+scale): relRMSE <= 2e-3 and relMax <= 1e-2 on unbiased data; no inf/NaN and relRMSE <= 5e-3
+on biased and resonance data. LSE is compared in absolute terms.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from gpu_helpers import gather_rows, rel_errors, to_dev
+
+pytestmark = pytest.mark.gpu
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+MODES = [0, 1, 2, 3]
+MODE_NAMES = {0: "shift_f16acc", 1: "shift_f32acc", 2: "naive_f16acc", 3: "noshift_f32acc"}
+
+
+def pasa():
+    import precision_flashattention_numerics_gb300 as p
+
+    return p
+
+
+def run(q, k, v, causal, mode, scale=None):
+    p = pasa()
+    qt, kt, vt = to_dev(q, k, v)
+    o, lse = p.attn_fwd(qt, kt, vt, causal=causal, scale=scale, mode=mode)
+    p.check_device_error()
+    return o, lse
+
+
+def small_case(B, Hq, Hkv, Sq, Sk, D, kind, seed, **params):
+    w = wl.Workload("small", B, Hq, Hkv, Sq, Sk, D, False, kind, seed, tuple(sorted(params.items())))
+    return wl.make_inputs(w)
+
+
+def lse_tolerance(q, k, causal, mode, D):
+    """LSE bound from the arithmetic: fp32-accumulated scores give ~1e-3; fp16-accumulated
+    scores carry a few units of the fp16 spacing at the largest score magnitude (of the
+    shifted keys for mode 0, the raw keys for mode 2), times the softmax scale."""
+    if mode in (1, 3):
+        return 2e-3
+    from oracle import pseudo_average as pa
+
+    kk = pa.kshift_fast(k)[0] if mode == 0 else k
+    smax = float(oracle.row_max_abs_score(q, kk, causal).max())
+    ulp = 2.0 ** (math.floor(math.log2(max(smax, 1e-30))) - 10)
+    return 2e-3 + 4.0 * ulp / math.sqrt(D)
+
+
+SMALL = [
+    # (B, Hq, Hkv, Sq, Sk, D, causal, kind, params)
+    (1, 2, 1, 300, 300, 64, False, "iid", {}),
+    (1, 2, 1, 300, 300, 64, True, "iid", {}),
+    (2, 4, 2, 520, 520, 128, True, "iid", {}),
+    (1, 4, 2, 520, 520, 128, True, "kbias", {"bias_std": 20.0}),
+    (1, 2, 2, 200, 333, 128, True, "iid", {}),      # Sk > Sq: bottom-right aligned mask
+    (1, 2, 2, 333, 200, 64, True, "iid", {}),       # Sq > Sk: leading rows see no key
+    (1, 1, 1, 64, 50, 64, False, "iid", {}),        # a single partial key block
+    (1, 4, 1, 1, 500, 128, True, "iid", {}),        # one query row
+    (1, 2, 2, 257, 1000, 128, False, "kbias_t3", {"bias_std": 10.0, "t_dof": 3, "t_scale": 4.0}),
+]
+
+
+@pytest.mark.parametrize("mode", MODES, ids=[MODE_NAMES[m] for m in MODES])
+@pytest.mark.parametrize("case", range(len(SMALL)))
+def test_small_parity(case, mode):
+    B, Hq, Hkv, Sq, Sk, D, causal, kind, params = SMALL[case]
+    q, k, v = small_case(B, Hq, Hkv, Sq, Sk, D, kind, 100 + case, **params)
+    o, lse = run(q, k, v, causal, mode)
+    o_ref, lse_ref = oracle.attention(q, k, v, causal=causal)
+    og = o.double().cpu().numpy()
+    lg = lse.double().cpu().numpy()
+    assert np.isfinite(og).all()
+    rmse, rmax = rel_errors(og, o_ref)
+    biased = kind != "iid"
+    if mode == 2 and biased:
+        tol = (5e-2, 2e-1)   # the naive fp16 kernel is only expected to stay finite here
+    elif biased:
+        tol = (5e-3, 5e-2)
+    else:
+        tol = (2e-3, 1e-2)
+    assert rmse <= tol[0] and rmax <= tol[1], (rmse, rmax)
+    fin = np.isfinite(lse_ref)
+    assert np.all(np.isneginf(lg[~fin]))
+    assert np.all(og.reshape(-1, D)[~fin.reshape(-1)] == 0.0)
+    assert np.max(np.abs(lg[fin] - lse_ref[fin])) <= lse_tolerance(q, k, causal, mode, D)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_hand_worked_example(causal):
+    # tests/golden/hand_example.json, zero-padded from D = 2 to D = 64 (same scores)
+    ex = json.load(open(os.path.join(HERE, "golden", "hand_example.json")))
+    def pad(x):
+        a = np.zeros(np.array(x).shape[:-1] + (64,))
+        a[..., :2] = np.array(x)
+        return a.astype(np.float16)
+    q, k, v = pad(ex["q"]), pad(ex["k"]), pad(ex["v"])
+    ref = ex["causal" if causal else "noncausal"]
+    for mode in MODES:
+        o, lse = run(q, k, v, causal, mode, scale=ex["scale"])
+        og = o.double().cpu().numpy()[..., :2]
+        np.testing.assert_allclose(og, np.array(ref["o"]), rtol=0, atol=1e-2 * 14)
+        assert np.all(o.double().cpu().numpy()[..., 2:] == 0)
+        np.testing.assert_allclose(lse.double().cpu().numpy(), np.log(np.array(ref["lse_exp"], float)),
+                                   atol=2e-3)
+
+
+@pytest.mark.parametrize("mode", MODES, ids=[MODE_NAMES[m] for m in MODES])
+def test_invariants(mode):
+    p = pasa()
+    rng = np.random.default_rng(11)
+    B, Hq, Hkv, S, D = 1, 4, 2, 400, 128
+    q = (rng.standard_normal((B, Hq, S, D))).astype(np.float16)
+    k = (rng.standard_normal((B, Hkv, S, D))).astype(np.float16)
+    v = (rng.standard_normal((B, Hkv, S, D))).astype(np.float16)
+    ones = np.ones_like(v)
+    # rows of P sum to one: V = 1 gives O = 1 (fp16 rounding of P only)
+    o, _ = run(q, k, ones, True, mode)
+    assert np.abs(o.double().cpu().numpy() - 1.0).max() <= 2e-3
+    # causal row 0 sees key 0 only: O_0 = V_0 exactly
+    o, _ = run(q, k, v, True, mode)
+    og = o.cpu().numpy()
+    for h in range(Hq):
+        np.testing.assert_array_equal(og[0, h, 0], v[0, h // 2, 0])
+    # a single key: O = V_0 exactly, LSE = scale q . k_0
+    o1, l1 = run(q, k[:, :, :1].copy(), v[:, :, :1].copy(), False, mode)
+    og1 = o1.cpu().numpy()
+    for h in range(Hq):
+        np.testing.assert_array_equal(og1[0, h], np.broadcast_to(v[0, h // 2, 0], (S, D)))
+    lref = (q.astype(np.float64) @ np.repeat(k[:, :, :1], 2, axis=1).astype(np.float64).transpose(0, 1, 3, 2))[..., 0]
+    assert np.abs(l1.double().cpu().numpy() - lref / math.sqrt(D)).max() <= 1e-2
+    # GQA equals MHA with the key/value heads repeated, bit for bit
+    kr = np.ascontiguousarray(np.repeat(k, 2, axis=1))
+    vr = np.ascontiguousarray(np.repeat(v, 2, axis=1))
+    o2, l2 = run(q, kr, vr, True, mode)
+    assert torch.equal(o, o2)
+
+
+def test_f32acc_shift_matches_noshift_on_unbiased_data():
+    rng = np.random.default_rng(12)
+    q = rng.standard_normal((1, 2, 700, 128)).astype(np.float16)
+    k = rng.standard_normal((1, 2, 700, 128)).astype(np.float16)
+    v = rng.standard_normal((1, 2, 700, 128)).astype(np.float16)
+    o1, _ = run(q, k, v, False, 1)
+    o3, _ = run(q, k, v, False, 3)
+    rmse, rmax = rel_errors(o1.double().cpu().numpy(), o3.double().cpu().numpy())
+    assert rmse < 1e-3 and rmax < 1e-2
+
+
+def test_recovered_reference_isolates_accumulation_error():
+    # Using the kernel's own shifted keys and means, the fp64 "shift then recover" reference
+    # matches plain attention closely and the GPU output matches both.
+    p = pasa()
+    q, k, v = small_case(1, 4, 2, 520, 520, 128, "kbias", 5, bias_std=20.0)
+    (kt,) = to_dev(k)
+    ks, means = p.kshift(kt)
+    ks, means = ks.cpu().numpy(), means.cpu().numpy()
+    o_rec, _ = oracle.attention_recovered(q, ks, means, 112, v, causal=True)
+    o_ref, _ = oracle.attention(q, k, v, causal=True)
+    assert rel_errors(o_rec, o_ref)[0] < 1e-3
+    o, _ = run(q, k, v, True, 1)
+    assert rel_errors(o.double().cpu().numpy(), o_rec)[0] < 2e-3
+
+
+# ---------------------------------------------------------------------------------------
+# the measured workloads at full size, compared on sampled rows
+# ---------------------------------------------------------------------------------------
+FULL = wl.MEASURED + ["resonance_rope_a30_b2h5_s9216_d64", "resonance_slow_a30_b2h5_s9216_d64",
+                      "resonance_hot_a48_b2h5_s9216_d64"]
+_inputs_cache = {}
+
+
+def full_inputs(name):
+    if name not in _inputs_cache:
+        _inputs_cache.clear()
+        w = wl.WORKLOADS[name]
+        q, k, v = wl.make_inputs(w)
+        rows = wl.sample_rows(w, 160)
+        o_ref, lse_ref = oracle.attention(q, k, v, causal=w.causal, rows=rows)
+        _inputs_cache[name] = (w, (q, k, v), to_dev(q, k, v), rows, o_ref, lse_ref)
+    return _inputs_cache[name]
+
+
+# (relRMSE, relMax) gates per (workload kind, mode); None = reported, only finiteness checked
+def gate(w, mode):
+    unbiased = w.kind == "iid"
+    if mode == 2:
+        return (2e-3, 1e-2) if unbiased else None
+    if mode == 0 and w.kind == "resonance":
+        return None   # fp16 accumulation of resonance scores (|S'| ~ 1e4, ulp 8): reported only
+    return (2e-3, 1e-2) if unbiased else (5e-3, None)
+
+
+FULL_CASES = [(n, m) for n in FULL for m in MODES]
+
+
+@pytest.mark.parametrize("name,mode", FULL_CASES, ids=[f"{n}-{MODE_NAMES[m]}" for n, m in FULL_CASES])
+def test_full_size_sampled_rows(name, mode):
+    p = pasa()
+    w, host, (qt, kt, vt), rows, o_ref, lse_ref = full_inputs(name)
+    o, lse = p.attn_fwd(qt, kt, vt, causal=w.causal, mode=mode)
+    p.check_device_error()
+    n_bad = int((~torch.isfinite(o)).sum().item())
+    og = gather_rows(o, rows)
+    lg = lse.reshape(-1)[torch.as_tensor(rows, device=o.device)].double().cpu().numpy()
+    rmse, rmax = rel_errors(og, o_ref) if n_bad == 0 else (float("nan"), float("nan"))
+    print(f"\n{name} mode={MODE_NAMES[mode]} nonfinite={n_bad} relRMSE={rmse:.3e} relMax={rmax:.3e} "
+          f"lse_maxerr={np.nanmax(np.abs(lg - lse_ref)):.3e}")
+    if name.startswith("resonance_hot") and mode == 2:
+        assert n_bad > 0, "the naive fp16 kernel is expected to overflow on this input"
+        return
+    assert n_bad == 0
+    g = gate(w, mode)
+    if g is not None:
+        assert rmse <= g[0], rmse
+        if g[1] is not None:
+            assert rmax <= g[1], rmax
