@@ -90,6 +90,9 @@ WORKLOADS = {
                  "resonance", 1013, _p(A=30.0, noise_std=0.5, freq="rope", phase_flip=True)),
         Workload("resonance_slow_a30_b2h5_s9216_d64", 2, 5, 5, 9216, 9216, 64, False,
                  "resonance", 1023, _p(A=30.0, noise_std=0.5, freq="slow", phase_flip=True)),
+        # a quarter of the 8K throughput workload: inputs still larger than L2, small enough
+        # for a many-pass profiler capture
+        Workload("iid_b1h32g8_s8192_d128_causal", 1, 32, 8, 8192, 8192, 128, True, "iid", 1044),
         # overflow demonstration: slow in-phase resonance with A = 48 pushes raw scores past 65504
         Workload("resonance_hot_a48_b2h5_s9216_d64", 2, 5, 5, 9216, 9216, 64, False,
                  "resonance", 1033, _p(A=48.0, noise_std=0.5, freq="slow", phase_flip=False)),
