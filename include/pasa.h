@@ -75,6 +75,27 @@ int pasa_block_rows(void);
 int pasa_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                   int Sq, int Sk, int D, int causal, float scale, int mode, void* stream);
 
+/*
+ * pasa_attn_fwd for callers that cannot allocate device memory. (The paper has no
+ * counterpart: this is a library convenience.) Some callers may not call cudaMalloc at
+ * all, for instance a process whose GPU memory is reserved up front by a framework or
+ * serving allocator, or a latency-bound loop in which an allocation is not allowed. This
+ * entry point allocates nothing: the shifted keys and block means go to one 64 MiB array
+ * compiled into the library, which every GPU that loads the library holds until exit.
+ *   - Arguments and results as in pasa_attn_fwd.
+ *   - Returns PASA_ERR_WORKSPACE, and launches nothing, when the problem needs more than
+ *     64 MiB of scratch, i.e. when pasa_attn_fwd_workspace_bytes(B, Hkv, Sk, D, mode)
+ *     exceeds 67108864 (modes 2 and 3 need none).
+ *   - The first call on a device looks up the array's device address with
+ *     cudaGetSymbolAddress (with that device current); make that first call before any
+ *     stream capture.
+ *   - All calls share the one array. Every call writes the part it reads before reading
+ *     it, so nothing has to start at zero, but calls whose work overlaps on the GPU (other
+ *     streams, other host threads) race on the array: order them, e.g. on one stream.
+ */
+int pasa_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                          int Hkv, int Sq, int Sk, int D, int causal, float scale, int mode, void* stream);
+
 /* Workspace bytes pasa_attn_fwd_ws needs for these sizes and mode (0 for modes 2 and 3). */
 size_t pasa_attn_fwd_workspace_bytes(int B, int Hkv, int Sk, int D, int mode);
 

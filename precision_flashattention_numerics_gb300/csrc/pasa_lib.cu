@@ -300,3 +300,63 @@ int pasa_check_device_error(void* stream, unsigned long long* info) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------------
+// Allocation-free variant of pasa_attn_fwd.
+//
+// Some callers may not call cudaMalloc at all: a process whose device memory is owned by a
+// framework or server allocator that reserves the whole GPU up front, or a latency-bound
+// loop where an allocation (and the synchronisation it can imply) is not allowed. For them
+// the shifted keys and block means live in one file-scope device array instead of a
+// workspace. The array is part of this library's device image, so every GPU that loads
+// the library holds it until the process exits.
+// ---------------------------------------------------------------------------------------
+#include <mutex>
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;  // 64 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device. The host-side name of the
+// array is only a stand-in, so the address is looked up once per device (with that device
+// current) and cached.
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return PASA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e);
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return PASA_OK;
+}
+
+}  // namespace
+
+extern "C" int pasa_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                                     int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale, int mode,
+                                     void* stream) {
+  int rc = validate(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, mode);
+  if (rc != PASA_OK) return rc;
+  const size_t need = pasa_attn_fwd_workspace_bytes(B, Hkv, Sk, D, mode);
+  if (need > kNoAllocScratchBytes) return PASA_ERR_WORKSPACE;
+  rc = check_device();
+  if (rc != PASA_OK) return rc;
+  void* ws = nullptr;
+  if (need > 0) {
+    rc = noalloc_scratch(&ws);
+    if (rc != PASA_OK) return rc;
+  }
+  return pasa_attn_fwd_ws(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, mode, ws,
+                          need > 0 ? kNoAllocScratchBytes : 0, stream);
+}
