@@ -277,10 +277,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     const int i = q0 + t * kTileRows + r;
     const int limit = (i < p.Sq) ? (CAUSAL ? min(p.Sk, max(0, i + p.Sk - p.Sq + 1)) : p.Sk) : 0;
     const float sl2 = p.scale_log2;
+    const int my_nblk = t == 0 ? nblk[0] : nblk[1];  // keeps nblk in registers
     float m_run = -INFINITY, l_run = 0.0f;
     bool ok = true;
 
-    for (int j = 0; j < nblk[t]; ++j) {
+    for (int j = 0; j < my_nblk; ++j) {
       if (!mbar_wait(&s.s_full[t], j & 1, abort_flag, 0x300 + t)) { ok = false; break; }
       tc_fence_after();
       // all loads of this block in flight, one wait, then a register fence so no use of
@@ -303,9 +304,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         for (int c = 0; c < kBlockRows; ++c)
           if (c >= cmax) sv[c] = -INFINITY;
       }
-      float mx = sv[0];
+      // row max: three-input max, four independent chains
+      float mxa = sv[0], mxb = sv[1], mxc = sv[2], mxd = sv[3];
 #pragma unroll
-      for (int c = 1; c < kBlockRows; ++c) mx = fmaxf(mx, sv[c]);
+      for (int c = 4; c + 8 <= kBlockRows; c += 8) {
+        mxa = fmax3(mxa, sv[c], sv[c + 1]);
+        mxb = fmax3(mxb, sv[c + 2], sv[c + 3]);
+        mxc = fmax3(mxc, sv[c + 4], sv[c + 5]);
+        mxd = fmax3(mxd, sv[c + 6], sv[c + 7]);
+      }
+      mxa = fmax3(mxa, sv[kBlockRows - 4], sv[kBlockRows - 3]);
+      mxb = fmax3(mxb, sv[kBlockRows - 2], sv[kBlockRows - 1]);
+      const float mx = fmaxf(fmaxf(mxa, mxb), fmaxf(mxc, mxd));
       const float bm = (mx == -INFINITY) ? -INFINITY : (mx + c_raw) * sl2;
       const float m_new = fmaxf(m_run, bm);
       if (j == 0) {
@@ -331,15 +341,21 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         }
       }
       const float bias = (m_run == -INFINITY) ? 0.0f : c_raw * sl2 - m_run;
-      float rowsum = 0.0f;
+      // p = exp2(S' * scale*log2e + (c * scale*log2e - m)): one packed FMA per pair, MUFU
+      // ex2 per element, packed fp32 row sums in four independent accumulators
+      float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       uint32_t pk[kBlockRows / 2];
 #pragma unroll
       for (int c = 0; c < kBlockRows / 2; ++c) {
-        const float p0 = ex2_approx(fmaf(sv[2 * c], sl2, bias));
-        const float p1 = ex2_approx(fmaf(sv[2 * c + 1], sl2, bias));
-        rowsum += p0 + p1;
+        float x0, x1;
+        ffma2(x0, x1, sv[2 * c], sv[2 * c + 1], sl2, sl2, bias, bias);
+        const float p0 = ex2_approx(x0);
+        const float p1 = ex2_approx(x1);
+        const int a = (c & 3) * 2;
+        fadd2(rs[a], rs[a + 1], rs[a], rs[a + 1], p0, p1);
         pk[c] = pack_half2(p0, p1);
       }
+      const float rowsum = ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
       l_run += rowsum;
 #pragma unroll
       for (int c = 0; c < kBlockRows / 16; ++c) tmem_st_x8(tS + c * 8, pk + c * 8);
@@ -350,7 +366,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     }
 
     // epilogue: O / l -> fp16 -> swizzled staging (the tile's Q buffer) -> TMA store
-    const bool have_o = ok && nblk[t] > 0;
+    const bool have_o = ok && my_nblk > 0;
     if (have_o && !mbar_wait(&s.o_full[t], 0, abort_flag, 0x310 + t)) ok = false;
     // A tile without key blocks reaches here before any MMA: its Q load (into the buffer
     // reused as staging) must have landed before the staging is written.
