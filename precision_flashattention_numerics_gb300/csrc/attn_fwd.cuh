@@ -8,15 +8,16 @@
 // ("global recovering"). The shifted keys and the block means come from kshift_kernel.
 //
 // One CTA owns 256 query rows of one (batch, query head) as two 128-row tiles and walks the
-// key blocks (kBlockRows = 112 keys) of its kv head. Warp roles (320 threads):
+// key blocks (kBlockRows = 112 keys) of its kv head. Warp roles (352 threads):
 //   warps 0-3  softmax + epilogue for tile 0   (thread r <-> query row r <-> TMEM lane r)
 //   warps 4-7  softmax + epilogue for tile 1
 //   warp  8    TMA producer: Q once, then K'_j / V_j rings and 16-block chunks of means
-//   warp  9    TMEM owner and MMA issuer (one thread)
+//   warp  9    TMEM owner and MMA issuer for tile 0 (one thread)
+//   warp 10    MMA issuer for tile 1 (one thread)
 // TMEM (512 columns): S_t at t*128 (112 columns, P_t packed fp16 aliased onto its first
 // 56), C_t at t*128+112 (16 columns: offsets of 16 consecutive key blocks), O_t at 256+t*128.
-// Per key block j the MMA thread issues, for each tile, PV_t(j-1) then QK_t(j), so the tensor
-// core works on one tile while the softmax warps of the other tile run (ping-pong).
+// Per key block j each tile's MMA thread issues PV_t(j-1) then QK_t(j), so the tensor core
+// works on one tile while the softmax warps of the other tile run (ping-pong).
 //
 // Score modes: the QK^T accumulator is fp16 (F16ACC, the PASA regime) or fp32. SHIFT
 // selects shifted keys + offsets (PASA) or raw keys (no shift: the naive fp16 kernel or the
@@ -39,7 +40,7 @@ namespace pasa {
 constexpr int kTileRows = 128;       // query rows per tile (MMA M)
 constexpr int kCtaRows = 256;        // two tiles per CTA
 constexpr int kChunkBlocks = 16;     // key blocks per offsets MMA (its N)
-constexpr int kAttnThreads = 320;
+constexpr int kAttnThreads = 352;
 constexpr float kRescaleLog2 = 8.0f;
 
 struct AttnParams {
@@ -47,6 +48,7 @@ struct AttnParams {
   int B, Hq, Hkv, Sq, Sk;
   int n_qblk;        // ceil(Sq / kCtaRows)
   float scale_log2;  // softmax scale * log2(e)
+  float inv_scale_log2;  // 1 / scale_log2
 };
 
 template <int D, int KST, int VST>
@@ -63,11 +65,12 @@ struct AttnSmem {
   alignas(1024) uint8_t v[VST][kKTile];
   alignas(1024) uint8_t m[2][kMTile];
   uint64_t q_full;
-  uint64_t k_full[KST], k_empty[KST];
+  uint64_t k_full[KST], k_empty[KST];  // empty barriers: one arrival per MMA warp
   uint64_t v_full[VST], v_empty[VST];
   uint64_t m_full[2], m_empty[2];
   uint64_t s_full[2], p_full[2], o_full[2];
-  uint64_t drain;
+  uint64_t drain[2];
+  uint64_t issued[2];  // MMA warp t has issued its batch for block j (phase j)
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -119,16 +122,19 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
 
   if (tid == 0) {
     mbar_init(&s.q_full, 1);
-    for (int i = 0; i < KST; ++i) { mbar_init(&s.k_full[i], 1); mbar_init(&s.k_empty[i], 1); }
-    for (int i = 0; i < VST; ++i) { mbar_init(&s.v_full[i], 1); mbar_init(&s.v_empty[i], 1); }
+    for (int i = 0; i < KST; ++i) { mbar_init(&s.k_full[i], 1); mbar_init(&s.k_empty[i], 2); }
+    for (int i = 0; i < VST; ++i) { mbar_init(&s.v_full[i], 1); mbar_init(&s.v_empty[i], 2); }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.m_full[i], 1);
-      mbar_init(&s.m_empty[i], 1);
+      mbar_init(&s.m_empty[i], 2);
       mbar_init(&s.s_full[i], 1);
       mbar_init(&s.p_full[i], 4);
       mbar_init(&s.o_full[i], 1);
     }
-    mbar_init(&s.drain, 1);
+    mbar_init(&s.drain[0], 1);
+    mbar_init(&s.drain[1], 1);
+    mbar_init(&s.issued[0], 1);
+    mbar_init(&s.issued[1], 1);
     s.abort_flag = 0;
     fence_mbar_init();
   }
@@ -158,10 +164,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         for (int c = 0; c < Smem::kChunks; ++c)
           tma_load_3d(s.q[t] + c * Smem::kQChunk, &mapQ, &s.q_full, c * 64, q0 + t * kTileRows, qz);
       int k_issued = 0, v_issued = 0, m_issued = 0;
-      for (int j = 0; j < nblk_max; ++j) {
+      // Issue order K_0, K_1, V_0, K_2, V_1, ...: each K runs one block ahead of V, so an
+      // MMA warp's wait for K_(j+1) never sits behind V_j. A slot is reused once both MMA
+      // warps have released its previous block.
+      auto load_k = [&](int j) -> bool {
         if (SHIFT && (j % kChunkBlocks) == 0) {
           const int ci = j / kChunkBlocks, slot = ci & 1;
-          if (!mbar_wait(&s.m_empty[slot], ((ci >> 1) & 1) ^ 1, abort_flag, 0x101)) break;
+          if (!mbar_wait(&s.m_empty[slot], ((ci >> 1) & 1) ^ 1, abort_flag, 0x101)) return false;
           mbar_arrive_expect_tx(&s.m_full[slot], Smem::kMTile);
 #pragma unroll
           for (int c = 0; c < Smem::kChunks; ++c)
@@ -169,19 +178,28 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
           m_issued = ci + 1;
         }
         const int ks = j % KST;
-        if (!mbar_wait(&s.k_empty[ks], ((j / KST) & 1) ^ 1, abort_flag, 0x102)) break;
+        if (!mbar_wait(&s.k_empty[ks], ((j / KST) & 1) ^ 1, abort_flag, 0x102)) return false;
         mbar_arrive_expect_tx(&s.k_full[ks], Smem::kKTile);
 #pragma unroll
         for (int c = 0; c < Smem::kChunks; ++c)
           tma_load_3d(s.k[ks] + c * Smem::kKChunk, &mapK, &s.k_full[ks], c * 64, j * kBlockRows, kz);
         k_issued = j + 1;
+        return true;
+      };
+      auto load_v = [&](int j) -> bool {
         const int vs = j % VST;
-        if (!mbar_wait(&s.v_empty[vs], ((j / VST) & 1) ^ 1, abort_flag, 0x103)) break;
+        if (!mbar_wait(&s.v_empty[vs], ((j / VST) & 1) ^ 1, abort_flag, 0x103)) return false;
         mbar_arrive_expect_tx(&s.v_full[vs], Smem::kKTile);
 #pragma unroll
         for (int c = 0; c < Smem::kChunks; ++c)
           tma_load_3d(s.v[vs] + c * Smem::kKChunk, &mapV, &s.v_full[vs], c * 64, j * kBlockRows, kz);
         v_issued = j + 1;
+        return true;
+      };
+      bool pok = nblk_max == 0 || load_k(0);
+      for (int j = 0; pok && j < nblk_max; ++j) {
+        if (j + 1 < nblk_max && !load_k(j + 1)) break;
+        if (!load_v(j)) break;
       }
       if (*abort_flag) {
         // Let every copy this warp issued land before the CTA's shared memory goes away.
@@ -197,72 +215,111 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
       }
     }
     __syncwarp();
-  } else if (warp == 9) {
-    // ------------------------------------------------------------------ MMA issuer
+  } else if (warp == 9 || warp == 10) {
+    // ------------------------------------------------------------------ MMA issuers
+    // Warp 9 issues tile 0's MMAs and warp 10 tile 1's, one thread each, so one tile's waits
+    // (for its softmax, or for a K/V tile) overlap the other tile's MMA issue. Both warps
+    // walk every key block: for a block its tile does not use, a warp still waits for the
+    // block to be loaded and then arrives on the slot's release barrier without a commit.
+    // Each release barrier takes one arrival per warp, and a warp only releases a slot after
+    // seeing its current block loaded, so slots are never released early.
+    // The two warps pass a token so that the tensor core still alternates between the tiles
+    // (tile 0's batch for block j after tile 1's batch for block j-1, tile 1's after tile
+    // 0's for block j): one tile's softmax runs while the other tile's batch executes. A
+    // warp does all its other waits while the other warp's batch is executing.
+    const int t = warp - 9;
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_f16(kTileRows, kBlockRows, !F16ACC, false);
       constexpr uint32_t id_c = idesc_f16(kTileRows, kChunkBlocks, true, false);
       constexpr uint32_t id_o = idesc_f16(kTileRows, D, true, true);
-      const uint32_t q_addr[2] = {smem_u32(s.q[0]), smem_u32(s.q[1])};
-      bool ok = mbar_wait(&s.q_full, 0, abort_flag, 0x201);
+      // Descriptor words: the high word is one constant per layout, the low word of every
+      // operand is its buffer's base word plus a compile-time offset (one add per MMA).
+      constexpr uint32_t hi_kmaj = sdesc_hi_sw128(1024);
+      constexpr uint32_t hi_v = sdesc_hi_sw128(1024);
+      const uint32_t q_lo = sdesc_lo(smem_u32(s.q[t]), 16);
+      const uint32_t k_lo0 = sdesc_lo(smem_u32(s.k[0]), 16);
+      const uint32_t v_lo0 = sdesc_lo(smem_u32(s.v[0]), Smem::kKChunk);
+      const uint32_t m_lo0 = sdesc_lo(smem_u32(s.m[0]), 16);
+      constexpr uint32_t kKStride = sizeof(s.k[0]) >> 4;  // descriptor units per ring slot
+      constexpr uint32_t kVStride = sizeof(s.v[0]) >> 4;
+      constexpr uint32_t kMStride = sizeof(s.m[0]) >> 4;
+      const int my_nblk = t == 0 ? nblk[0] : nblk[1];
+      const uint32_t tS = tmem + t * 128;
+      const uint32_t tO = tmem + 256 + t * 128;
+      // Every descriptor word of a batch is formed before the waits that gate it, so once
+      // the gate opens the thread issues nothing but the MMAs (the softmax warps sharing its
+      // SMSP are at their busiest then).
+      uint32_t qd[D / 16];
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) qd[kk] = q_lo + (((kk / 4) * Smem::kQChunk + (kk % 4) * 32) >> 4);
+      bool ok = mbar_wait(&s.q_full, 0, abort_flag, 0x201 + 0x10 * t);
       tc_fence_after();
       for (int j = 0; ok && j <= nblk_max; ++j) {
-        const bool has_k = j < nblk_max;
-        const int ks = j % KST;
-        const int ci = j / kChunkBlocks;
-        const bool chunk_start = SHIFT && has_k && (j % kChunkBlocks) == 0;
-        if (has_k && !mbar_wait(&s.k_full[ks], (j / KST) & 1, abort_flag, 0x202)) break;
-        if (chunk_start && !mbar_wait(&s.m_full[ci & 1], (ci >> 1) & 1, abort_flag, 0x203)) break;
-        bool v_waited = false;
-        const int vs = (j + VST - 1) % VST;  // slot of block j-1
+        uint32_t vd[kBlockRows / 16], kd[D / 16];
+        {
+          const uint32_t v_lo = v_lo0 + ((j + VST - 1) % VST) * kVStride;
+          const uint32_t k_lo = k_lo0 + (j % KST) * kKStride;
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          const uint32_t tS = tmem + t * 128;
-          const uint32_t tO = tmem + 256 + t * 128;
-          if (j >= 1 && j - 1 < nblk[t]) {
-            if (!v_waited) {
-              if (!mbar_wait(&s.v_full[vs], ((j - 1) / VST) & 1, abort_flag, 0x204)) { ok = false; break; }
-              v_waited = true;
-            }
-            if (!mbar_wait(&s.p_full[t], (j - 1) & 1, abort_flag, 0x205)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t v_addr = smem_u32(s.v[vs]);
+          for (int kk = 0; kk < kBlockRows / 16; ++kk) vd[kk] = v_lo + kk * (2048 >> 4);
 #pragma unroll
-            for (int kk = 0; kk < kBlockRows / 16; ++kk) {
-              const uint64_t vd = sdesc_sw128(v_addr + kk * 2048, Smem::kKChunk, 1024);
-              mma_ts(tO, tS + kk * 8, vd, id_o, (j - 1 > 0 || kk > 0) ? 1u : 0u);
-            }
-            if (j - 1 == nblk[t] - 1) mma_commit(&s.o_full[t]);
-          }
-          if (has_k && j < nblk[t]) {
-            if (chunk_start) {
-              const uint32_t m_addr = smem_u32(s.m[ci & 1]);
+          for (int kk = 0; kk < D / 16; ++kk) kd[kk] = k_lo + (((kk / 4) * Smem::kKChunk + (kk % 4) * 32) >> 4);
+        }
+        if (j < nblk_max) {
+          const int ci = j / kChunkBlocks;
+          if (!mbar_wait(&s.k_full[j % KST], (j / KST) & 1, abort_flag, 0x202 + 0x10 * t)) break;
+          if (SHIFT && (j % kChunkBlocks) == 0 &&
+              !mbar_wait(&s.m_full[ci & 1], (ci >> 1) & 1, abort_flag, 0x203 + 0x10 * t))
+            break;
+        }
+        if (j >= 1 && !mbar_wait(&s.v_full[(j - 1) % VST], ((j - 1) / VST) & 1, abort_flag, 0x204 + 0x10 * t)) break;
+        if (j >= 1 && j - 1 < my_nblk && !mbar_wait(&s.p_full[t], (j - 1) & 1, abort_flag, 0x205 + 0x10 * t)) break;
+        // token: tile 0 waits for tile 1's batch of block j-1, tile 1 for tile 0's of block j
+        if (t == 0 && j >= 1 && !mbar_wait(&s.issued[1], (j - 1) & 1, abort_flag, 0x208)) break;
+        if (t == 1 && !mbar_wait(&s.issued[0], j & 1, abort_flag, 0x218)) break;
+        tc_fence_after();
+        if (j >= 1) {
+          const int vs = (j - 1) % VST;
+          if (j - 1 < my_nblk) {
+            const uint32_t acc0 = j - 1 > 0 ? 1u : 0u;
 #pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                const uint64_t ad = sdesc_sw128(q_addr[t] + (kk / 4) * Smem::kQChunk + (kk % 4) * 32, 16, 1024);
-                const uint64_t md = sdesc_sw128(m_addr + (kk / 4) * Smem::kMChunk + (kk % 4) * 32, 16, 1024);
-                mma_ss(tS + kBlockRows, ad, md, id_c, kk > 0 ? 1u : 0u);
-              }
-            }
-            const uint32_t k_addr = smem_u32(s.k[ks]);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint64_t ad = sdesc_sw128(q_addr[t] + (kk / 4) * Smem::kQChunk + (kk % 4) * 32, 16, 1024);
-              const uint64_t kd = sdesc_sw128(k_addr + (kk / 4) * Smem::kKChunk + (kk % 4) * 32, 16, 1024);
-              mma_ss(tS, ad, kd, id_s, kk > 0 ? 1u : 0u);
-            }
-            mma_commit(&s.s_full[t]);
+            for (int kk = 0; kk < kBlockRows / 16; ++kk)
+              mma_ts_w(tO, tS + kk * 8, vd[kk], hi_v, id_o, kk > 0 ? 1u : acc0);
+            if (j - 1 == my_nblk - 1) mma_commit(&s.o_full[t]);
+            mma_commit(&s.v_empty[vs]);
+          } else {
+            mbar_arrive(&s.v_empty[vs]);
           }
         }
-        if (!ok) break;
-        if (has_k) mma_commit(&s.k_empty[ks]);
-        if (chunk_start) mma_commit(&s.m_empty[ci & 1]);
-        if (v_waited) mma_commit(&s.v_empty[vs]);
+        if (j < nblk_max) {
+          const int ks = j % KST;
+          const int ci = j / kChunkBlocks;
+          const bool chunk_start = SHIFT && (j % kChunkBlocks) == 0;
+          if (j < my_nblk) {
+            if (chunk_start) {
+              const uint32_t m_lo = m_lo0 + (ci & 1) * kMStride;
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off_q = ((kk / 4) * Smem::kQChunk + (kk % 4) * 32) >> 4;
+                const uint32_t off_m = ((kk / 4) * Smem::kMChunk + (kk % 4) * 32) >> 4;
+                mma_ss_w(tS + kBlockRows, q_lo + off_q, hi_kmaj, m_lo + off_m, hi_kmaj, id_c, kk > 0 ? 1u : 0u);
+              }
+            }
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) mma_ss_w(tS, qd[kk], hi_kmaj, kd[kk], hi_kmaj, id_s, kk > 0 ? 1u : 0u);
+            mma_commit(&s.s_full[t]);
+            mma_commit(&s.k_empty[ks]);
+            if (chunk_start) mma_commit(&s.m_empty[ci & 1]);
+          } else {
+            mbar_arrive(&s.k_empty[ks]);
+            if (chunk_start) mbar_arrive(&s.m_empty[ci & 1]);
+          }
+        }
+        mbar_arrive(&s.issued[t]);
       }
       // all MMAs issued by this thread complete before TMEM can be released
-      mma_commit(&s.drain);
+      mma_commit(&s.drain[t]);
       const uint64_t t0 = globaltimer_ns();
-      while (!mbar_try_wait(&s.drain, 0) && globaltimer_ns() - t0 < kWaitTimeoutNs) {
+      while (!mbar_try_wait(&s.drain[t], 0) && globaltimer_ns() - t0 < kWaitTimeoutNs) {
       }
     }
     __syncwarp();
@@ -284,38 +341,70 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     for (int j = 0; j < my_nblk; ++j) {
       if (!mbar_wait(&s.s_full[t], j & 1, abort_flag, 0x300 + t)) { ok = false; break; }
       tc_fence_after();
-      // all loads of this block in flight, one wait, then a register fence so no use of
-      // the loaded registers is scheduled before the wait
-      uint32_t sr[kBlockRows];
-#pragma unroll
-      for (int c = 0; c < kBlockRows / 16; ++c) tmem_ld_x16(tS + c * 16, sr + c * 16);
+      // All loads of this block in flight, one wait, then a register fence so no use of the
+      // loaded registers is scheduled before the wait. fp16 scores (F16ACC) are loaded two per
+      // register; their row max is taken in f16x2 and each score enters fp32 through one
+      // mixed-precision add (no separate conversion). fp32 scores are used as loaded.
+      constexpr int kPairs = kBlockRows / 2;
+      uint32_t hp[F16ACC ? kPairs : 1];
+      float sv[F16ACC ? 1 : kBlockRows];
       uint32_t cw = 0;
-      if (SHIFT) tmem_ld_x1(tC + (j % kChunkBlocks), cw);
-      tmem_ld_wait();
-      reg_fence<kBlockRows>(sr);
-      reg_fence<1>(&cw);
-      float sv[kBlockRows];
-#pragma unroll
-      for (int c = 0; c < kBlockRows; ++c) sv[c] = F16ACC ? half_lo_to_float(sr[c]) : __uint_as_float(sr[c]);
-      const float c_raw = SHIFT ? __uint_as_float(cw) : 0.0f;
       const int cmax = limit - j * kBlockRows;
-      if (cmax < kBlockRows) {
+      float mx;
+      if constexpr (F16ACC) {
+        static_assert(kBlockRows == 112, "load split below");
+        tmem_ld_x16_pack16(tS + 0, hp + 0);
+        tmem_ld_x16_pack16(tS + 32, hp + 16);
+        tmem_ld_x16_pack16(tS + 64, hp + 32);
+        tmem_ld_x8_pack16(tS + 96, hp + 48);
+        if (SHIFT) tmem_ld_x1(tC + (j % kChunkBlocks), cw);
+        tmem_ld_wait();
+        reg_fence<kPairs>(hp);
+        reg_fence<1>(&cw);
+        if (cmax < kBlockRows) {
 #pragma unroll
-        for (int c = 0; c < kBlockRows; ++c)
-          if (c >= cmax) sv[c] = -INFINITY;
-      }
-      // row max: three-input max, four independent chains
-      float mxa = sv[0], mxb = sv[1], mxc = sv[2], mxd = sv[3];
+          for (int c = 0; c < kPairs; ++c) {
+            const uint32_t lo = (2 * c < cmax) ? (hp[c] & 0xFFFFu) : 0xFC00u;        // -inf
+            const uint32_t hi = (2 * c + 1 < cmax) ? (hp[c] & 0xFFFF0000u) : 0xFC000000u;
+            hp[c] = lo | hi;
+          }
+        }
+        // f16x2 max tree: 56 -> 28 -> 14 -> 7 -> 4 -> 2 -> 1
+        uint32_t m28[28], m14[14], m7[7];
 #pragma unroll
-      for (int c = 4; c + 8 <= kBlockRows; c += 8) {
-        mxa = fmax3(mxa, sv[c], sv[c + 1]);
-        mxb = fmax3(mxb, sv[c + 2], sv[c + 3]);
-        mxc = fmax3(mxc, sv[c + 4], sv[c + 5]);
-        mxd = fmax3(mxd, sv[c + 6], sv[c + 7]);
+        for (int c = 0; c < 28; ++c) m28[c] = hmax2(hp[2 * c], hp[2 * c + 1]);
+#pragma unroll
+        for (int c = 0; c < 14; ++c) m14[c] = hmax2(m28[2 * c], m28[2 * c + 1]);
+#pragma unroll
+        for (int c = 0; c < 7; ++c) m7[c] = hmax2(m14[2 * c], m14[2 * c + 1]);
+        const uint32_t m4a = hmax2(m7[0], m7[1]), m4b = hmax2(m7[2], m7[3]), m4c = hmax2(m7[4], m7[5]);
+        const uint32_t m1 = hmax2(hmax2(m4a, m4b), hmax2(m4c, m7[6]));
+        mx = fmaxf(half_lo_to_float(m1), half_lo_to_float(m1 >> 16));
+      } else {
+#pragma unroll
+        for (int c = 0; c < kBlockRows / 16; ++c) tmem_ld_x16(tS + c * 16, reinterpret_cast<uint32_t*>(sv) + c * 16);
+        if (SHIFT) tmem_ld_x1(tC + (j % kChunkBlocks), cw);
+        tmem_ld_wait();
+        reg_fence<kBlockRows>(reinterpret_cast<uint32_t*>(sv));
+        reg_fence<1>(&cw);
+        if (cmax < kBlockRows) {
+#pragma unroll
+          for (int c = 0; c < kBlockRows; ++c)
+            if (c >= cmax) sv[c] = -INFINITY;
+        }
+        // fp32 max tree with three-input max: 112 -> 38 -> 13 -> 5 -> 2 -> 1
+        float m38[38], m13[13];
+#pragma unroll
+        for (int c = 0; c < 37; ++c) m38[c] = fmax3(sv[3 * c], sv[3 * c + 1], sv[3 * c + 2]);
+        m38[37] = sv[111];
+#pragma unroll
+        for (int c = 0; c < 12; ++c) m13[c] = fmax3(m38[3 * c], m38[3 * c + 1], m38[3 * c + 2]);
+        m13[12] = fmaxf(m38[36], m38[37]);
+        const float m5a = fmax3(m13[0], m13[1], m13[2]), m5b = fmax3(m13[3], m13[4], m13[5]);
+        const float m5c = fmax3(m13[6], m13[7], m13[8]), m5d = fmax3(m13[9], m13[10], m13[11]);
+        mx = fmaxf(fmax3(m5a, m5b, m5c), fmaxf(m5d, m13[12]));
       }
-      mxa = fmax3(mxa, sv[kBlockRows - 4], sv[kBlockRows - 3]);
-      mxb = fmax3(mxb, sv[kBlockRows - 2], sv[kBlockRows - 1]);
-      const float mx = fmaxf(fmaxf(mxa, mxb), fmaxf(mxc, mxd));
+      const float c_raw = SHIFT ? __uint_as_float(cw) : 0.0f;
       const float bm = (mx == -INFINITY) ? -INFINITY : (mx + c_raw) * sl2;
       const float m_new = fmaxf(m_run, bm);
       if (j == 0) {
@@ -340,20 +429,36 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
           }
         }
       }
-      const float bias = (m_run == -INFINITY) ? 0.0f : c_raw * sl2 - m_run;
-      // p = exp2(S' * scale*log2e + (c * scale*log2e - m)): one packed FMA per pair, MUFU
-      // ex2 per element, packed fp32 row sums in four independent accumulators
+      // p = exp2((S' + c) * scale*log2e - m): MUFU ex2 per element, packed fp32 arithmetic per
+      // pair, row sums in four independent pair accumulators.
       float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      uint32_t pk[kBlockRows / 2];
+      uint32_t pk[kPairs];
+      if constexpr (F16ACC) {
+        // x = (S' + (c - m / sl2)) * sl2
+        const float b16 = (m_run == -INFINITY) ? 0.0f : c_raw - m_run * p.inv_scale_log2;
 #pragma unroll
-      for (int c = 0; c < kBlockRows / 2; ++c) {
-        float x0, x1;
-        ffma2(x0, x1, sv[2 * c], sv[2 * c + 1], sl2, sl2, bias, bias);
-        const float p0 = ex2_approx(x0);
-        const float p1 = ex2_approx(x1);
-        const int a = (c & 3) * 2;
-        fadd2(rs[a], rs[a + 1], rs[a], rs[a + 1], p0, p1);
-        pk[c] = pack_half2(p0, p1);
+        for (int c = 0; c < kPairs; ++c) {
+          float y0, y1, x0, x1;
+          add_f16x2_f32(y0, y1, hp[c], b16);
+          fmul2(x0, x1, y0, y1, sl2, sl2);
+          const float p0 = ex2_approx(x0);
+          const float p1 = ex2_approx(x1);
+          const int a = (c & 3) * 2;
+          fadd2(rs[a], rs[a + 1], rs[a], rs[a + 1], p0, p1);
+          pk[c] = pack_half2(p0, p1);
+        }
+      } else {
+        const float bias = (m_run == -INFINITY) ? 0.0f : c_raw * sl2 - m_run;
+#pragma unroll
+        for (int c = 0; c < kPairs; ++c) {
+          float x0, x1;
+          ffma2(x0, x1, sv[2 * c], sv[2 * c + 1], sl2, sl2, bias, bias);
+          const float p0 = ex2_approx(x0);
+          const float p1 = ex2_approx(x1);
+          const int a = (c & 3) * 2;
+          fadd2(rs[a], rs[a + 1], rs[a], rs[a + 1], p0, p1);
+          pk[c] = pack_half2(p0, p1);
+        }
       }
       const float rowsum = ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
       l_run += rowsum;

@@ -213,6 +213,7 @@ static int attn_launch(const void* q, const void* kk, const void* mm, const void
   p.Sk = Sk;
   p.n_qblk = (Sq + pasa::kCtaRows - 1) / pasa::kCtaRows;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.inv_scale_log2 = 1.0f / p.scale_log2;
   return D == 64 ? attn_dispatch<64>(mode, causal, mq, mk, mv, mo, mmeans, p, st)
                  : attn_dispatch<128>(mode, causal, mq, mk, mv, mo, mmeans, p, st);
 }
