@@ -172,7 +172,7 @@ def bench_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int, also
     qt, kt, vt = (torch.from_numpy(x).to(dev) for x in (q, k, v))
     o = torch.empty_like(qt)
     lse = torch.empty((w.B, w.Hq, w.Sq), device=dev, dtype=torch.float32)
-    nb = (w.Sk + pasa.block_rows() - 1) // pasa.block_rows()
+    nb = (w.Sk + pasa.block_rows(w.D) - 1) // pasa.block_rows(w.D)
     shift = args.mode in (0, 1)
     ks = torch.empty_like(kt) if shift else kt
     means = torch.empty((w.B, w.Hkv, nb, w.D), device=dev, dtype=torch.float16) if shift else None
@@ -342,7 +342,9 @@ def main():
     }
     kshift_kernel = None
     if args.mode in (0, 1):
-        kb = 2 * (w.B * w.Hkv * w.Sk * w.D * 2) + w.B * w.Hkv * math.ceil(w.Sk / 112) * w.D * 2
+        import precision_flashattention_numerics_gb300 as pasa
+
+        kb = 2 * (w.B * w.Hkv * w.Sk * w.D * 2) + w.B * w.Hkv * math.ceil(w.Sk / pasa.block_rows(w.D)) * w.D * 2
         gbs = kb / (res["kshift_ms"] * 1e-3) / 1e9
         hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
         kshift_kernel = {"kernel": "kshift_kernel", "bound": "hbm", "achieved": round(gbs, 1), "peak": hbm,

@@ -52,8 +52,9 @@ extern "C" {
 #define PASA_MODE_NAIVE_F16ACC 2   /* no shift, fp16-accumulated scores: shows the fp16 overflow */
 #define PASA_MODE_NOSHIFT_F32ACC 3 /* no shift, fp32-accumulated scores: plain FlashAttention */
 
-/* Rows per key block: the block the pseudo-average is taken over (112). */
-int pasa_block_rows(void);
+/* Keys per block for head dim D: the block the pseudo-average is taken over, which is also
+ * the attention kernel's key tile (128 for D = 64 and D = 128; 0 for other D). */
+int pasa_block_rows(int D);
 
 /*
  * PASA attention forward (the whole hot path: pseudo-average shift of K, then the fused
@@ -110,11 +111,29 @@ int pasa_attn_fwd_ws(const void* q, const void* k, const void* v, void* o, float
                      size_t workspace_bytes, void* stream);
 
 /*
+ * pasa_attn_fwd_ws plus an overflow diagnostic. The Abstract traces fp16 overflow (> 65504)
+ * in attention scores to a large sequence-dimension bias of K and to Q/K resonance; this
+ * call reports, for every query row, what the score accumulator actually held:
+ *   stats[b, h, i, 0] = max over visible keys of |accumulated score|: the shifted score
+ *                       S' = q_i . k'_j for modes 0/1, the raw score q_i . k_j for modes
+ *                       2/3; in the fp16-accumulate modes this is the fp16 value (inf if the
+ *                       accumulator overflowed);
+ *   stats[b, h, i, 1] = max over visible keys of |S' + q_i . m_j|, the recovered raw score
+ *                       (modes 0/1; equal to [0] for modes 2/3).
+ * stats is fp32 [B, Hq, Sq, 2], 8-byte aligned; rows with no visible key get 0. o and lse
+ * are written as in pasa_attn_fwd_ws. Runs a separately compiled variant of the attention
+ * kernel that also tracks the per-block minimum score.
+ */
+int pasa_attn_fwd_stats(const void* q, const void* k, const void* v, void* o, float* lse, float* stats, int B,
+                        int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale, int mode, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
+/*
  * The attention kernel alone, on keys already shifted by pasa_kshift (for modes 0 and 1:
  * k_shifted and means exactly as pasa_kshift wrote them for the same k) or on raw keys
  * (modes 2 and 3: pass k as k_shifted; means is ignored and may be NULL). This is the
  * second half of pasa_attn_fwd; callers that keep shifted keys (a KV cache) skip the shift.
- * Arguments as in pasa_attn_fwd; means is fp16 [B, Hkv, ceil(Sk / pasa_block_rows()), D].
+ * Arguments as in pasa_attn_fwd; means is fp16 [B, Hkv, ceil(Sk / pasa_block_rows(D)), D].
  */
 int pasa_attn_fwd_shifted(const void* q, const void* k_shifted, const void* means, const void* v, void* o,
                           float* lse, int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,
@@ -122,7 +141,7 @@ int pasa_attn_fwd_shifted(const void* q, const void* k_shifted, const void* mean
 
 /*
  * The pseudo-average shift step alone (PASA Abstract, "online pseudo-average shifting"),
- * exposed for testing and diagnostics. For every key block j of pasa_block_rows() rows
+ * exposed for testing and diagnostics. For every key block j of pasa_block_rows(D) rows
  * (the last block may be shorter) and channel d it writes
  *     means[b, h, j, d]   the block's pseudo-average m_j[d] (fp16)
  *     k_shifted[b, h, r, d] = fp16_rn(k[b, h, r, d] - m_j[d])
@@ -130,7 +149,7 @@ int pasa_attn_fwd_shifted(const void* q, const void* k_shifted, const void* mean
  * spacing at max_r |k[r,d]| and n the block's row count; m_j[d] = 0 when that maximum is
  * >= 32768 or the block/channel holds inf or NaN.
  *   k          fp16 [B, H, Sk, D]        k_shifted  fp16 [B, H, Sk, D]
- *   means      fp16 [B, H, ceil(Sk / pasa_block_rows()), D]
+ *   means      fp16 [B, H, ceil(Sk / pasa_block_rows(D)), D]
  */
 int pasa_kshift(const void* k, void* k_shifted, void* means, int B, int H, int Sk, int D, void* stream);
 

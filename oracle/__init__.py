@@ -54,6 +54,9 @@ def _load():
             lib.oracle_row_max_abs_score.argtypes = [p, p, p, i64, i64, i64, i64, i64, i64,
                                                      ctypes.c_int, p, i64]
             lib.oracle_row_max_abs_score.restype = ctypes.c_int
+            lib.oracle_row_max_abs_recovered.argtypes = [p, p, p, i64, p, i64, i64, i64, i64, i64, i64,
+                                                         ctypes.c_int, p, i64]
+            lib.oracle_row_max_abs_recovered.restype = ctypes.c_int
             lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
             lib.oracle_half_to_double.restype = ctypes.c_double
             _lib = lib
@@ -127,6 +130,21 @@ def row_max_abs_score(q, k, causal: bool, rows=None) -> np.ndarray:
                                           int(bool(causal)), _ptr(r), n)
     if rc != 0:
         raise ValueError("oracle_row_max_abs_score: bad shape")
+    return out if r is not None else out.reshape(B, Hq, Sq)
+
+
+def row_max_abs_recovered(q, kshift, means, block_rows: int, causal: bool, rows=None) -> np.ndarray:
+    """max_j |q_i . (k'_j + m_(j / block_rows))| (unscaled) over the visible keys of each row, in fp64."""
+    B, Hq, Sq, D = q.shape
+    _, Hkv, Sk, _ = kshift.shape
+    qb, kb, mb = _bits(q), _bits(kshift), _bits(means)
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    n = B * Hq * Sq if r is None else len(r)
+    out = np.empty((n,), np.float64)
+    rc = _load().oracle_row_max_abs_recovered(_ptr(qb), _ptr(kb), _ptr(mb), block_rows, _ptr(out), B, Hq, Hkv,
+                                              Sq, Sk, D, int(bool(causal)), _ptr(r), n)
+    if rc != 0:
+        raise ValueError("oracle_row_max_abs_recovered: bad shape")
     return out if r is not None else out.reshape(B, Hq, Sq)
 
 

@@ -196,3 +196,40 @@ int oracle_row_max_abs_score(const uint16_t *q, const uint16_t *k, double *out,
     }
     return 0;
 }
+
+/*
+ * Largest |q_i . k'_j + q_i . m_(j / block_rows)| over the visible keys of each row, unscaled:
+ * the raw score recovered from shifted keys and block means (the quantity PASA's "global
+ * recovering" adds back, Abstract). Equals oracle_row_max_abs_score on the raw keys when
+ * every shifted key is exactly k - m.
+ */
+int oracle_row_max_abs_recovered(const uint16_t *q, const uint16_t *kshift, const uint16_t *means,
+                                 int64_t block_rows, double *out, int64_t B, int64_t Hq, int64_t Hkv,
+                                 int64_t Sq, int64_t Sk, int64_t D, int causal, const int64_t *rows,
+                                 int64_t n_rows) {
+    if (Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || block_rows <= 0) return -1;
+    init_table();
+    if (!rows) n_rows = B * Hq * Sq;
+    int64_t group = Hq / Hkv;
+    int64_t nb = (Sk + block_rows - 1) / block_rows;
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t r = 0; r < n_rows; ++r) {
+        int64_t g = rows ? rows[r] : r;
+        int64_t i = g % Sq;
+        int64_t h = (g / Sq) % Hq;
+        int64_t b = g / (Sq * Hq);
+        const uint16_t *qrow = q + g * D;
+        const uint16_t *kh = kshift + (b * Hkv + h / group) * Sk * D;
+        const uint16_t *mh = means + (b * Hkv + h / group) * nb * D;
+        int64_t n = visible_keys(i, Sq, Sk, causal);
+        double mx = 0.0;
+        for (int64_t j = 0; j < n; ++j) {
+            double dot = 0.0;
+            for (int64_t d = 0; d < D; ++d)
+                dot += g_h2d[qrow[d]] * (g_h2d[kh[j * D + d]] + g_h2d[mh[(j / block_rows) * D + d]]);
+            if (fabs(dot) > mx) mx = fabs(dot);
+        }
+        out[r] = mx;
+    }
+    return 0;
+}

@@ -31,8 +31,14 @@ from __future__ import annotations
 
 import numpy as np
 
-# Rows per key block. The CUDA path shifts and recovers per block of this many keys.
-BLOCK_ROWS = 112
+
+def block_rows_for(D: int) -> int:
+    """Keys per block for head dim D: 128.
+
+    The Abstract leaves the block length open; the reading here is that the shift block is
+    the attention kernel's key tile, so its length is whatever that tile is for the head dim.
+    """
+    return 128
 
 
 def grid_step(absmax: np.ndarray) -> np.ndarray:
@@ -75,7 +81,7 @@ def block_pseudo_average(kb: np.ndarray) -> np.ndarray:
     return out
 
 
-def kshift(k: np.ndarray, block_rows: int = BLOCK_ROWS):
+def kshift(k: np.ndarray, block_rows: int | None = None):
     """Shift every key block by its pseudo-average.
 
     k: [B, H, Sk, D] fp16. Returns (k_shifted [B, H, Sk, D] fp16,
@@ -83,6 +89,7 @@ def kshift(k: np.ndarray, block_rows: int = BLOCK_ROWS):
     """
     k = np.asarray(k, dtype=np.float16)
     B, H, Sk, D = k.shape
+    block_rows = block_rows_for(D) if block_rows is None else block_rows
     nb = (Sk + block_rows - 1) // block_rows
     means = np.zeros((B, H, nb, D), np.float16)
     ks = np.empty_like(k)
@@ -96,10 +103,11 @@ def kshift(k: np.ndarray, block_rows: int = BLOCK_ROWS):
     return ks, means
 
 
-def kshift_fast(k: np.ndarray, block_rows: int = BLOCK_ROWS):
+def kshift_fast(k: np.ndarray, block_rows: int | None = None):
     """Same result as :func:`kshift`, vectorised over all blocks (for large inputs)."""
     k = np.asarray(k, dtype=np.float16)
     B, H, Sk, D = k.shape
+    block_rows = block_rows_for(D) if block_rows is None else block_rows
     nb = (Sk + block_rows - 1) // block_rows
     pad = nb * block_rows - Sk
     x = k.astype(np.float64)

@@ -18,7 +18,7 @@ import torch
 
 __all__ = [
     "MODE_SHIFT_F16ACC", "MODE_SHIFT_F32ACC", "MODE_NAIVE_F16ACC", "MODE_NOSHIFT_F32ACC",
-    "PasaError", "attn_fwd", "attn_fwd_alloc", "attn_fwd_shifted", "kshift", "workspace_bytes", "check_device_error", "block_rows",
+    "PasaError", "attn_fwd", "attn_fwd_alloc", "attn_fwd_shifted", "attn_fwd_stats", "kshift", "workspace_bytes", "check_device_error", "block_rows",
     "library", "library_path",
 ]
 
@@ -35,11 +35,12 @@ _lib = None
 # exported symbols and their ctypes signatures, mirroring include/pasa.h
 _P, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 SIGNATURES = {
-    "pasa_block_rows": ([], _I),
+    "pasa_block_rows": ([_I], _I),
     "pasa_attn_fwd": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P], _I),
     "pasa_attn_fwd_noalloc": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P], _I),
     "pasa_attn_fwd_workspace_bytes": ([_I, _I, _I, _I, _I], _SZ),
     "pasa_attn_fwd_ws": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P], _I),
+    "pasa_attn_fwd_stats": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P], _I),
     "pasa_attn_fwd_shifted": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P], _I),
     "pasa_kshift": ([_P, _P, _P, _I, _I, _I, _I, _P], _I),
     "pasa_check_device_error": ([_P, ctypes.POINTER(ctypes.c_ulonglong)], _I),
@@ -89,8 +90,9 @@ def _check(x: torch.Tensor, name: str):
         raise TypeError(f"{name} must be a contiguous CUDA fp16 tensor")
 
 
-def block_rows() -> int:
-    return library().pasa_block_rows()
+def block_rows(D: int) -> int:
+    """Keys per pseudo-average block (and attention key tile) for head dim D."""
+    return library().pasa_block_rows(D)
 
 
 def workspace_bytes(B: int, Hkv: int, Sk: int, D: int, mode: int) -> int:
@@ -148,6 +150,29 @@ def attn_fwd_alloc(q, k, v, causal: bool = False, scale: float | None = None, mo
     return out, lse
 
 
+def attn_fwd_stats(q, k, v, causal: bool = False, scale: float | None = None, mode: int = MODE_SHIFT_F16ACC):
+    """attn_fwd plus per-row score magnitudes: returns (o, lse, stats [B,Hq,Sq,2] fp32).
+
+    stats[..., 0] = max |score held by the accumulator| (S' for modes 0/1, S for 2/3),
+    stats[..., 1] = max |S' + q.m| (the recovered raw score; = [..., 0] for modes 2/3).
+    """
+    lib = library()
+    _check(q, "q"), _check(k, "k"), _check(v, "v")
+    B, Hq, Sq, D = q.shape
+    _, Hkv, Sk, _ = k.shape
+    out = torch.empty_like(q)
+    lse = torch.empty((B, Hq, Sq), device=q.device, dtype=torch.float32)
+    stats = torch.empty((B, Hq, Sq, 2), device=q.device, dtype=torch.float32)
+    nbytes = int(lib.pasa_attn_fwd_workspace_bytes(B, Hkv, Sk, D, mode))
+    ws = torch.empty(max(nbytes, 1), device=q.device, dtype=torch.uint8)
+    rc = lib.pasa_attn_fwd_stats(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(stats), B, Hq, Hkv, Sq, Sk,
+                                 D, int(bool(causal)), float(scale) if scale is not None else 0.0, int(mode),
+                                 _ptr(ws) if nbytes else None, nbytes, _stream())
+    if rc != 0:
+        raise PasaError(rc, "pasa_attn_fwd_stats")
+    return out, lse, stats
+
+
 def attn_fwd_shifted(q, k_shifted, means, v, causal: bool = False, scale: float | None = None,
                      mode: int = MODE_SHIFT_F16ACC, out=None, lse=None):
     """The attention kernel alone on keys from :func:`kshift` (modes 0/1) or raw keys (2/3)."""
@@ -174,7 +199,8 @@ def kshift(k, out=None, means=None):
     lib = library()
     _check(k, "k")
     B, H, Sk, D = k.shape
-    nb = (Sk + lib.pasa_block_rows() - 1) // lib.pasa_block_rows()
+    bn = lib.pasa_block_rows(D)
+    nb = (Sk + bn - 1) // bn
     ks = torch.empty_like(k) if out is None else out
     if means is None:
         means = torch.empty((B, H, nb, D), device=k.device, dtype=torch.float16)

@@ -8,7 +8,7 @@
 // pseudo-average; this library uses the following reading (the oracle implements the same
 // reading independently, in numpy):
 //
-//   for key block j (kBlockRows rows, n valid) and channel d:
+//   for key block j (block_rows_for(D) rows, n valid) and channel d:
 //     M = max_r |K[r,d]|            g = fp16 spacing at M (2^(E-25), or 2^-24 if E = 0)
 //     t_r = rint_even(K[r,d] / g)   m = g * rint_even(sum_r t_r / n)   (exact integers)
 //     m = 0 when M >= 2^15 or the block/channel holds inf or NaN
@@ -17,7 +17,7 @@
 // m lies on the grid of the block maximum, so K - m is exact in fp16 for most elements.
 //
 // Kernel shape: one CTA of 256 threads per (batch*kv-head, key block). Each thread owns one
-// 16-byte unit (8 channels) of up to ceil(kBlockRows / row_groups) rows and keeps them in
+// 16-byte unit (8 channels) of up to ceil(block rows / row groups) rows and keeps them in
 // registers; the per-channel max and integer sums are reduced with warp shuffles and a
 // small shared-memory exchange across the 8 warps; the block is read from HBM once and
 // K' written once (HBM-bound: 2 * rows * D * 2 bytes per block).
@@ -28,7 +28,9 @@
 
 namespace pasa {
 
-constexpr int kBlockRows = 112;      // keys per block: the shift block and the attention key tile
+// Keys per block: the block the pseudo-average is taken over, which is also the attention
+// kernel's key tile (the N of its score MMA). 128 for both supported head dims.
+__host__ __device__ constexpr int block_rows_for(int D) { return D == 128 || D == 64 ? 128 : 0; }
 constexpr int kShiftThreads = 256;
 
 // round-half-even(s / n) for integers, n > 0.
@@ -40,13 +42,13 @@ __device__ __forceinline__ int rne_div(int s, int n) {
   return s < 0 ? -q : q;
 }
 
-template <int D>
+template <int D, int BN>
 __global__ void __launch_bounds__(kShiftThreads)
 kshift_kernel(const __half* __restrict__ k, __half* __restrict__ kshift, __half* __restrict__ means, int Sk,
               int nb) {
   constexpr int U = D / 8;                       // 16-byte units per row
   constexpr int R = kShiftThreads / U;           // row groups
-  constexpr int RPT = (kBlockRows + R - 1) / R;  // rows per thread (upper bound)
+  constexpr int RPT = (BN + R - 1) / R;          // rows per thread (upper bound)
   constexpr int NW = kShiftThreads / 32;
   static_assert(32 % U == 0 || U % 32 == 0, "unit layout");
   static_assert(U <= 32, "D <= 256");
@@ -61,8 +63,8 @@ kshift_kernel(const __half* __restrict__ k, __half* __restrict__ kshift, __half*
   const int u = tid % U;
   const int rg = tid / U;
   const int warp = tid / 32;
-  const int row0 = j * kBlockRows;
-  const int n = min(kBlockRows, Sk - row0);
+  const int row0 = j * BN;
+  const int n = min(BN, Sk - row0);
 
   const uint4* src = reinterpret_cast<const uint4*>(k + (static_cast<size_t>(bh) * Sk + row0) * D) + u;
   uint4* dst = reinterpret_cast<uint4*>(kshift + (static_cast<size_t>(bh) * Sk + row0) * D) + u;

@@ -68,7 +68,8 @@ struct WorkspaceLayout {
 };
 
 WorkspaceLayout workspace_layout(int B, int Hkv, int Sk, int D) {
-  const size_t nb = (static_cast<size_t>(Sk) + pasa::kBlockRows - 1) / pasa::kBlockRows;
+  const int bn = pasa::block_rows_for(D);
+  const size_t nb = (static_cast<size_t>(Sk) + bn - 1) / bn;
   WorkspaceLayout w;
   w.kshift_off = 0;
   w.means_off = align_up(static_cast<size_t>(B) * Hkv * Sk * D * 2, 256);
@@ -78,9 +79,10 @@ WorkspaceLayout workspace_layout(int B, int Hkv, int Sk, int D) {
 
 template <int D>
 int launch_kshift(const void* k, void* ks, void* means, int B, int H, int Sk, cudaStream_t st) {
-  const int nb = (Sk + pasa::kBlockRows - 1) / pasa::kBlockRows;
+  constexpr int BN = pasa::block_rows_for(D);
+  const int nb = (Sk + BN - 1) / BN;
   dim3 grid(nb, B * H);
-  pasa::kshift_kernel<D><<<grid, pasa::kShiftThreads, 0, st>>>(
+  pasa::kshift_kernel<D, BN><<<grid, pasa::kShiftThreads, 0, st>>>(
       static_cast<const __half*>(k), static_cast<__half*>(ks), static_cast<__half*>(means), Sk, nb);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? PASA_OK : cuda_fail(e);
@@ -90,13 +92,14 @@ int kshift_dispatch(const void* k, void* ks, void* means, int B, int H, int Sk, 
   return D == 64 ? launch_kshift<64>(k, ks, means, B, H, Sk, st) : launch_kshift<128>(k, ks, means, B, H, Sk, st);
 }
 
-template <int D, bool F16ACC, bool SHIFT, bool CAUSAL>
+template <int D, bool F16ACC, bool SHIFT, bool CAUSAL, bool STATS>
 int launch_attn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mo,
                 const CUtensorMap& mm, const pasa::AttnParams& p, cudaStream_t st) {
-  constexpr int KST = D == 128 ? 3 : 4;
+  constexpr int BN = pasa::block_rows_for(D);
+  constexpr int KST = D == 128 ? 3 : 4;  // K ring slots (D = 128: 200 KB of shared memory)
   constexpr int VST = D == 128 ? 2 : 4;
-  using Smem = pasa::AttnSmem<D, KST, VST>;
-  auto kern = pasa::attn_fwd_kernel<D, F16ACC, SHIFT, CAUSAL, KST, VST>;
+  using Smem = pasa::AttnSmem<D, BN, KST, VST>;
+  auto kern = pasa::attn_fwd_kernel<D, BN, F16ACC, SHIFT, CAUSAL, KST, VST, STATS>;
   const int smem = static_cast<int>(sizeof(Smem)) + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -106,13 +109,13 @@ int launch_attn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap&
   return e == cudaSuccess ? PASA_OK : cuda_fail(e);
 }
 
-template <int D>
+template <int D, bool STATS>
 int attn_dispatch(int mode, int causal, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                   const CUtensorMap& mo, const CUtensorMap& mm, const pasa::AttnParams& p, cudaStream_t st) {
-#define PASA_CASE(MODE, F16, SH)                                                 \
-  case MODE:                                                                     \
-    return causal ? launch_attn<D, F16, SH, true>(mq, mk, mv, mo, mm, p, st)     \
-                  : launch_attn<D, F16, SH, false>(mq, mk, mv, mo, mm, p, st);
+#define PASA_CASE(MODE, F16, SH)                                                        \
+  case MODE:                                                                            \
+    return causal ? launch_attn<D, F16, SH, true, STATS>(mq, mk, mv, mo, mm, p, st)     \
+                  : launch_attn<D, F16, SH, false, STATS>(mq, mk, mv, mo, mm, p, st);
   switch (mode) {
     PASA_CASE(PASA_MODE_SHIFT_F16ACC, true, true)
     PASA_CASE(PASA_MODE_SHIFT_F32ACC, false, true)
@@ -131,7 +134,7 @@ int validate(const void* q, const void* k, const void* v, const void* o, const f
   if (D != 64 && D != 128) return PASA_ERR_UNSUPPORTED;
   if (mode < PASA_MODE_SHIFT_F16ACC || mode > PASA_MODE_NOSHIFT_F32ACC) return PASA_ERR_UNSUPPORTED;
   // grid size, TMA plane counts and flat LSE indices fit in 32-bit signed integers
-  const long long n_qblk = (static_cast<long long>(Sq) + pasa::kCtaRows - 1) / pasa::kCtaRows;
+  const long long n_qblk = (static_cast<long long>(Sq) + pasa::kTileRows - 1) / pasa::kTileRows;
   if (n_qblk * Hq * B > 0x7fffffffLL) return PASA_ERR_SHAPE;
   if (static_cast<long long>(B) * Hq > 0x7fffffffLL || static_cast<long long>(B) * Hkv > 0x7fffffffLL)
     return PASA_ERR_SHAPE;
@@ -144,7 +147,7 @@ int validate(const void* q, const void* k, const void* v, const void* o, const f
 
 extern "C" {
 
-int pasa_block_rows(void) { return pasa::kBlockRows; }
+int pasa_block_rows(int D) { return pasa::block_rows_for(D); }
 
 int pasa_last_cuda_error(void) { return t_last_cuda_error; }
 
@@ -170,7 +173,7 @@ const char* pasa_strerror(int status) {
 }
 
 size_t pasa_attn_fwd_workspace_bytes(int B, int Hkv, int Sk, int D, int mode) {
-  if (B <= 0 || Hkv <= 0 || Sk <= 0 || D <= 0) return 0;
+  if (B <= 0 || Hkv <= 0 || Sk <= 0 || pasa::block_rows_for(D) == 0) return 0;
   if (mode != PASA_MODE_SHIFT_F16ACC && mode != PASA_MODE_SHIFT_F32ACC) return 0;
   return workspace_layout(B, Hkv, Sk, D).total;
 }
@@ -188,15 +191,17 @@ int pasa_kshift(const void* k, void* k_shifted, void* means, int B, int H, int S
 
 // Launch the attention kernel on (possibly shifted) keys `kk` and block means `mm`.
 static int attn_launch(const void* q, const void* kk, const void* mm, const void* v, void* o, float* lse, int B,
-                       int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale, int mode, cudaStream_t st) {
+                       int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale, int mode, cudaStream_t st,
+                       float* stats = nullptr) {
   const bool shift = mode == PASA_MODE_SHIFT_F16ACC || mode == PASA_MODE_SHIFT_F32ACC;
   if (!(scale > 0.0f) || !std::isfinite(scale)) scale = 1.0f / std::sqrt(static_cast<float>(D));
-  const int nb = (Sk + pasa::kBlockRows - 1) / pasa::kBlockRows;
+  const int bn = pasa::block_rows_for(D);
+  const int nb = (Sk + bn - 1) / bn;
   int rc;
   CUtensorMap mq, mk, mv, mo, mmeans;
   if ((rc = make_map(&mq, q, D, Sq, static_cast<long long>(B) * Hq, pasa::kTileRows)) != PASA_OK) return rc;
-  if ((rc = make_map(&mk, kk, D, Sk, static_cast<long long>(B) * Hkv, pasa::kBlockRows)) != PASA_OK) return rc;
-  if ((rc = make_map(&mv, v, D, Sk, static_cast<long long>(B) * Hkv, pasa::kBlockRows)) != PASA_OK) return rc;
+  if ((rc = make_map(&mk, kk, D, Sk, static_cast<long long>(B) * Hkv, bn)) != PASA_OK) return rc;
+  if ((rc = make_map(&mv, v, D, Sk, static_cast<long long>(B) * Hkv, bn)) != PASA_OK) return rc;
   if ((rc = make_map(&mo, o, D, Sq, static_cast<long long>(B) * Hq, pasa::kTileRows)) != PASA_OK) return rc;
   if (shift) {
     if ((rc = make_map(&mmeans, mm, D, nb, static_cast<long long>(B) * Hkv, pasa::kChunkBlocks)) != PASA_OK)
@@ -211,11 +216,15 @@ static int attn_launch(const void* q, const void* kk, const void* mm, const void
   p.Hkv = Hkv;
   p.Sq = Sq;
   p.Sk = Sk;
-  p.n_qblk = (Sq + pasa::kCtaRows - 1) / pasa::kCtaRows;
+  p.n_qblk = (Sq + pasa::kTileRows - 1) / pasa::kTileRows;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.inv_scale_log2 = 1.0f / p.scale_log2;
-  return D == 64 ? attn_dispatch<64>(mode, causal, mq, mk, mv, mo, mmeans, p, st)
-                 : attn_dispatch<128>(mode, causal, mq, mk, mv, mo, mmeans, p, st);
+  p.stats = stats;
+  if (stats)
+    return D == 64 ? attn_dispatch<64, true>(mode, causal, mq, mk, mv, mo, mmeans, p, st)
+                   : attn_dispatch<128, true>(mode, causal, mq, mk, mv, mo, mmeans, p, st);
+  return D == 64 ? attn_dispatch<64, false>(mode, causal, mq, mk, mv, mo, mmeans, p, st)
+                 : attn_dispatch<128, false>(mode, causal, mq, mk, mv, mo, mmeans, p, st);
 }
 
 int pasa_attn_fwd_shifted(const void* q, const void* k_shifted, const void* means, const void* v, void* o,
@@ -259,6 +268,35 @@ int pasa_attn_fwd_ws(const void* q, const void* k, const void* v, void* o, float
     mm = means;
   }
   return attn_launch(q, kk, mm, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, mode, st);
+}
+
+int pasa_attn_fwd_stats(const void* q, const void* k, const void* v, void* o, float* lse, float* stats, int B,
+                        int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale, int mode, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  int rc = validate(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, mode);
+  if (rc != PASA_OK) return rc;
+  if (!stats) return PASA_ERR_NULLPTR;
+  if ((reinterpret_cast<uintptr_t>(stats) & 7u) != 0) return PASA_ERR_ALIGN;
+  const bool shift = mode == PASA_MODE_SHIFT_F16ACC || mode == PASA_MODE_SHIFT_F32ACC;
+  const WorkspaceLayout wl = workspace_layout(B, Hkv, Sk, D);
+  if (shift) {
+    if (!workspace || workspace_bytes < wl.total) return PASA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PASA_ERR_ALIGN;
+    if (static_cast<long long>(B) * Hkv > 65535) return PASA_ERR_SHAPE;
+  }
+  rc = check_device();
+  if (rc != PASA_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const void* kk = k;
+  const void* mm = k;
+  if (shift) {
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    rc = kshift_dispatch(k, ws + wl.kshift_off, ws + wl.means_off, B, Hkv, Sk, D, st);
+    if (rc != PASA_OK) return rc;
+    kk = ws + wl.kshift_off;
+    mm = ws + wl.means_off;
+  }
+  return attn_launch(q, kk, mm, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, mode, st, stats);
 }
 
 int pasa_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,

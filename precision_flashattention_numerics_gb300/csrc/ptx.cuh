@@ -370,6 +370,18 @@ __device__ __forceinline__ void add_f16x2_f32(float& d0, float& d1, uint32_t h2,
       : "r"(h2), "f"(c));
 }
 
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t hmin2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("min.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
 __device__ __forceinline__ uint32_t hmax2(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("max.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));

@@ -40,7 +40,10 @@ def test_exports_every_declared_function(lib):
 
 
 def test_block_rows_and_strings(lib):
-    assert lib.pasa_block_rows() == 112
+    # the key tile (and shift block): 128 keys for both supported head dims
+    assert lib.pasa_block_rows(64) == 128
+    assert lib.pasa_block_rows(128) == 128
+    assert lib.pasa_block_rows(96) == 0
     for code in (0, -1, -2, -3, -4, -5, -6, -7):
         assert lib.pasa_strerror(code)
     assert lib.pasa_strerror(12345) == b"unknown status"
@@ -87,10 +90,10 @@ def test_kshift_argument_errors(lib):
 
 
 def test_workspace_bytes(lib):
-    # shifted keys [B,Hkv,Sk,D] fp16 + means [B,Hkv,ceil(Sk/112),D] fp16, each 256-aligned
+    # shifted keys [B,Hkv,Sk,D] fp16 + means [B,Hkv,ceil(Sk/128),D] fp16, each 256-aligned
     def expect(B, H, Sk, D):
         a = -(-(B * H * Sk * D * 2) // 256) * 256
-        nb = -(-Sk // 112)
+        nb = -(-Sk // 128)
         return -(-(a + B * H * nb * D * 2) // 256) * 256
 
     for (B, H, Sk, D) in [(1, 4, 4096, 128), (2, 5, 9216, 64), (1, 1, 1, 64), (4, 8, 8192, 128)]:

@@ -62,7 +62,7 @@ def lse_tolerance(q, k, causal, mode, D):
     ks = None
     if mode in (0, 1):
         ks, means = pa.kshift_fast(k)
-        rows = np.repeat(means.astype(np.float64), pa.BLOCK_ROWS, axis=2)[:, :, :k.shape[2]]
+        rows = np.repeat(means.astype(np.float64), pa.block_rows_for(k.shape[3]), axis=2)[:, :, :k.shape[2]]
         err = ks.astype(np.float64) - (k.astype(np.float64) - rows)
         err = np.repeat(err, g, axis=1)
         tol += scale * float(np.abs(qd @ err.transpose(0, 1, 3, 2)).max())
@@ -182,7 +182,7 @@ def test_recovered_reference_isolates_accumulation_error():
     (kt,) = to_dev(k)
     ks, means = p.kshift(kt)
     ks, means = ks.cpu().numpy(), means.cpu().numpy()
-    o_rec, _ = oracle.attention_recovered(q, ks, means, 112, v, causal=True)
+    o_rec, _ = oracle.attention_recovered(q, ks, means, p.block_rows(128), v, causal=True)
     o_ref, _ = oracle.attention(q, k, v, causal=True)
     assert rel_errors(o_rec, o_ref)[0] < 1e-3
     o, _ = run(q, k, v, True, 1)

@@ -31,8 +31,10 @@ def f16(x):
 @pytest.mark.parametrize("B,H,Sk,D,kind", [
     (1, 2, 300, 64, "iid"),
     (1, 1, 1, 64, "iid"),
-    (1, 1, 112, 128, "iid"),
-    (1, 1, 113, 128, "iid"),
+    (1, 1, 128, 128, "iid"),    # exactly one block (128 keys)
+    (1, 1, 129, 128, "iid"),    # one key past it
+    (1, 1, 128, 64, "iid"),
+    (1, 1, 129, 64, "iid"),
     (1, 4, 4096, 128, "kbias"),
     (2, 3, 1000, 128, "kbias_t3"),
     (2, 5, 9216, 64, "resonance"),

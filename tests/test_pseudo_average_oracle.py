@@ -94,7 +94,7 @@ def test_shift_is_mostly_exact_and_removes_bias():
     # the point of rounding the mean to the grid: K - m is exact in fp16 for most elements
     rng = np.random.default_rng(2)
     k = f16(rng.standard_normal((1, 2, 448, 64)) + rng.normal(0, 20, (1, 2, 1, 64)))
-    ks, means = pa.kshift_fast(k)
+    ks, means = pa.kshift_fast(k, block_rows=112)
     exact = ks.astype(np.float64) == k.astype(np.float64) - np.repeat(means.astype(np.float64), 112, axis=2)
     assert exact.mean() > 0.85
     assert np.abs(ks.astype(np.float64)).max() < 8.0       # bias of ~20 per channel removed
@@ -105,7 +105,7 @@ def test_shifted_value_is_correctly_rounded():
     # K' = fp16(K - m) with one rounding: compare against the two fp16 neighbours
     rng = np.random.default_rng(3)
     k = f16(rng.standard_normal((1, 1, 224, 32)) * rng.uniform(0.01, 100, 32))
-    ks, means = pa.kshift_fast(k)
+    ks, means = pa.kshift_fast(k, block_rows=112)
     exact = k.astype(np.float64) - np.repeat(means.astype(np.float64), 112, axis=2)
     got = ks.astype(np.float64)
     lo = np.nextafter(ks, np.float16(-np.inf)).astype(np.float64)
@@ -131,3 +131,17 @@ def test_shift_then_recover_equals_plain_attention(oracle_mod, causal):
     # and without the offsets the result is wrong: the recovery step is load-bearing
     o2, _ = oracle_mod.attention(q, ks, v, causal=causal, scale=0.05)
     assert np.abs(o2 - o0).max() > 1e-3
+
+
+def test_recovered_score_magnitude_equals_raw_when_shift_is_exact(oracle_mod):
+    # q . (k' + m) = q . k when k' = k - m exactly (coarse-grid data); the shifted magnitude
+    # itself is much smaller because the per-channel bias is gone
+    rng = np.random.default_rng(6)
+    q = f16(rng.integers(-3, 4, (1, 4, 30, 16)))
+    k = f16(rng.integers(-20, 21, (1, 2, 230, 16)) + rng.integers(-200, 200, (1, 2, 1, 16)))
+    ks, means = pa.kshift(k, block_rows=112)
+    for causal in (False, True):
+        raw = oracle_mod.row_max_abs_score(q, k, causal)
+        rec = oracle_mod.row_max_abs_recovered(q, ks, means, 112, causal)
+        np.testing.assert_array_equal(rec, raw)
+        assert np.median(raw / np.maximum(oracle_mod.row_max_abs_score(q, ks, causal), 1)) > 2
