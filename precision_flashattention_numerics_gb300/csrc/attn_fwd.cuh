@@ -423,10 +423,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             hp[c] = ((2 * c < cmax) ? (hp[c] & 0xFFFFu) : 0xFC00u) |
                     ((2 * c + 1 < cmax) ? (hp[c] & 0xFFFF0000u) : 0xFC000000u);  // -inf when masked
         }
-        uint32_t tmp[kPairs];
+        uint32_t tmp[8];
 #pragma unroll
-        for (int c = 0; c < kPairs; ++c) tmp[c] = hp[c];
-        const uint32_t m1 = tree_h2<kPairs, true>(tmp);
+        for (int k = 0; k < 8; ++k) tmp[k] = hp[k];
+#pragma unroll
+        for (int c = 8; c < kPairs; ++c) tmp[c & 7] = hmax2(tmp[c & 7], hp[c]);
+        const uint32_t m1 = tree_h2<8, true>(tmp);
         mx = fmaxf(half_lo_to_float(m1), half_lo_to_float(m1 >> 16));
       } else {
         if (cmax < BN) {
