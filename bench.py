@@ -17,6 +17,7 @@ there is no data-path collective); value = all ranks' FLOPs / the slowest rank's
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -37,6 +38,29 @@ DEFAULT_WORKLOAD = "kbias10_t3_b1h28g4_s32768_d128_causal"
 ALSO_WORKLOADS = ["iid_b4h32g8_s8192_d128_causal"]
 MODE_NAMES = {0: "shift_f16acc", 1: "shift_f32acc", 2: "naive_f16acc", 3: "noshift_f32acc"}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one attention-kernel launch,
+# from an ncu capture of a quarter of the 32K workload (7 of 28 query heads, 1 of 4 kv heads:
+# 75.65 MB read + 24.80 MB written) scaled x4 to a full launch; the traffic is per head, so it
+# grows in proportion. Summary and command: profiles/attn_fwd_kbias10_t3_b1h7g1_s32768_full.md.
+# Reported only while the kernel source is the one the counters were taken on.
+TRAFFIC_WORKLOAD = "kbias10_t3_b1h28g4_s32768_d128_causal"
+TRAFFIC_MODE = 0
+TRAFFIC_BYTES = 4 * (75.649792e6 + 24.798720e6)
+TRAFFIC_KERNEL_SHA = "f0216f659691a9ac"
+
+
+def measured_traffic(w, mode):
+    src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "precision_flashattention_numerics_gb300",
+                       "csrc", "attn_fwd.cuh")
+    try:
+        with open(src, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        return None
+    if w.name != TRAFFIC_WORKLOAD or mode != TRAFFIC_MODE or sha != TRAFFIC_KERNEL_SHA:
+        return None
+    return round(TRAFFIC_BYTES)
 
 
 def load_peaks():
@@ -334,10 +358,11 @@ def main():
                           "finite": ra["finite"]}
 
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))  # fp16 dense = bf16 dense rate
+    traffic = measured_traffic(w, args.mode)
     attn_achieved = res["flops"] / (res["attn_ms"] * 1e-3) / 1e12
     roofline = {
         "kernel": "attn_fwd_kernel", "bound": "tensor", "achieved": round(attn_achieved, 1), "peak": peak,
-        "unit": "TFLOP/s", "frac": round(attn_achieved / peak, 4), "traffic": None,
+        "unit": "TFLOP/s", "frac": round(attn_achieved / peak, 4), "traffic": traffic,
         "peak_source": f"{peak_src} bf16 dense burst (fp16 dense has the same nominal rate)",
     }
     kshift_kernel = None
