@@ -36,7 +36,8 @@ import workloads as wl  # noqa: E402
 
 DEFAULT_WORKLOAD = "kbias10_t3_b1h28g4_s32768_d128_causal"
 ALSO_WORKLOADS = ["iid_b4h32g8_s8192_d128_causal"]
-MODE_NAMES = {0: "shift_f16acc", 1: "shift_f32acc", 2: "naive_f16acc", 3: "noshift_f32acc"}
+MODE_NAMES = {0: "shift_f16acc", 1: "shift_f32acc", 2: "naive_f16acc", 3: "noshift_f32acc", 4: "shift_f16all"}
+SHIFT_MODES = (0, 1, 4)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one attention-kernel launch,
@@ -197,7 +198,7 @@ def bench_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int, also
     o = torch.empty_like(qt)
     lse = torch.empty((w.B, w.Hq, w.Sq), device=dev, dtype=torch.float32)
     nb = (w.Sk + pasa.block_rows(w.D) - 1) // pasa.block_rows(w.D)
-    shift = args.mode in (0, 1)
+    shift = args.mode in SHIFT_MODES
     ks = torch.empty_like(kt) if shift else kt
     means = torch.empty((w.B, w.Hkv, nb, w.D), device=dev, dtype=torch.float16) if shift else None
     stream = torch.cuda.current_stream()
@@ -300,7 +301,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="pasa", choices=["pasa", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.WORKLOADS))
-    ap.add_argument("--mode", type=int, default=0, choices=[0, 1, 2, 3])
+    ap.add_argument("--mode", type=int, default=0, choices=[0, 1, 2, 3, 4])
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-also", action="store_true")
@@ -366,7 +367,7 @@ def main():
         "peak_source": f"{peak_src} bf16 dense burst (fp16 dense has the same nominal rate)",
     }
     kshift_kernel = None
-    if args.mode in (0, 1):
+    if args.mode in SHIFT_MODES:
         import precision_flashattention_numerics_gb300 as pasa
 
         kb = 2 * (w.B * w.Hkv * w.Sk * w.D * 2) + w.B * w.Hkv * math.ceil(w.Sk / pasa.block_rows(w.D)) * w.D * 2
@@ -388,7 +389,7 @@ def main():
             "warmup": max(3, args.warmup), "ms_per_step": round(res["ms_per_step"], 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic", "config": config,
             "roofline": roofline, "kshift": kshift_kernel, "cpu_baseline": cpu, "e2e": res["e2e"],
-            "gpu_launches": args.steps * (2 if args.mode in (0, 1) else 1), "clocks": res["clocks"],
+            "gpu_launches": args.steps * (2 if args.mode in SHIFT_MODES else 1), "clocks": res["clocks"],
             "finite_output": res["finite"], "also": also,
         }
         print(json.dumps(out))

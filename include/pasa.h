@@ -51,6 +51,11 @@ extern "C" {
 #define PASA_MODE_SHIFT_F32ACC 1   /* PASA shift with fp32-accumulated scores */
 #define PASA_MODE_NAIVE_F16ACC 2   /* no shift, fp16-accumulated scores: shows the fp16 overflow */
 #define PASA_MODE_NOSHIFT_F32ACC 3 /* no shift, fp32-accumulated scores: plain FlashAttention */
+/* PASA with half precision throughout the loop ("Online Pseudo-average Shifting Attention
+ * (PASA) for Robust Low-precision LLM Inference", Abstract: half-precision computation
+ * throughout FlashAttention): mode 0, plus an fp16 PV accumulator and an fp16 running row
+ * sum. The running max, the offsets and the final division stay fp32. */
+#define PASA_MODE_SHIFT_F16ALL 4
 
 /* Keys per block for head dim D: the block the pseudo-average is taken over, which is also
  * the attention kernel's key tile (128 for D = 64 and D = 128; 0 for other D). */
@@ -66,7 +71,7 @@ int pasa_block_rows(int D);
  *             be NULL to skip it.
  *   causal    0 or 1 (bottom-right aligned mask).
  *   scale     softmax scale; <= 0 selects 1/sqrt(D).
- *   mode      PASA_MODE_* above. Modes 0 and 1 need a workspace for the shifted keys and
+ *   mode      PASA_MODE_* above. Modes 0, 1 and 4 need a workspace for the shifted keys and
  *             block means: this entry point takes it from the CUDA stream-ordered allocator
  *             (cudaMallocAsync / cudaFreeAsync on `stream`); use pasa_attn_fwd_ws to pass
  *             your own.
@@ -115,11 +120,11 @@ int pasa_attn_fwd_ws(const void* q, const void* k, const void* v, void* o, float
  * in attention scores to a large sequence-dimension bias of K and to Q/K resonance; this
  * call reports, for every query row, what the score accumulator actually held:
  *   stats[b, h, i, 0] = max over visible keys of |accumulated score|: the shifted score
- *                       S' = q_i . k'_j for modes 0/1, the raw score q_i . k_j for modes
+ *                       S' = q_i . k'_j for modes 0/1/4, the raw score q_i . k_j for modes
  *                       2/3; in the fp16-accumulate modes this is the fp16 value (inf if the
  *                       accumulator overflowed);
  *   stats[b, h, i, 1] = max over visible keys of |S' + q_i . m_j|, the recovered raw score
- *                       (modes 0/1; equal to [0] for modes 2/3).
+ *                       (modes 0/1/4; equal to [0] for modes 2/3).
  * stats is fp32 [B, Hq, Sq, 2], 8-byte aligned; rows with no visible key get 0. o and lse
  * are written as in pasa_attn_fwd_ws. Runs a separately compiled variant of the attention
  * kernel that also tracks the per-block minimum score.
@@ -129,7 +134,7 @@ int pasa_attn_fwd_stats(const void* q, const void* k, const void* v, void* o, fl
                         size_t workspace_bytes, void* stream);
 
 /*
- * The attention kernel alone, on keys already shifted by pasa_kshift (for modes 0 and 1:
+ * The attention kernel alone, on keys already shifted by pasa_kshift (for modes 0, 1 and 4:
  * k_shifted and means exactly as pasa_kshift wrote them for the same k) or on raw keys
  * (modes 2 and 3: pass k as k_shifted; means is ignored and may be NULL). This is the
  * second half of pasa_attn_fwd; callers that keep shifted keys (a KV cache) skip the shift.

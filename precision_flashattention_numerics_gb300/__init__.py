@@ -17,7 +17,7 @@ import threading
 import torch
 
 __all__ = [
-    "MODE_SHIFT_F16ACC", "MODE_SHIFT_F32ACC", "MODE_NAIVE_F16ACC", "MODE_NOSHIFT_F32ACC",
+    "MODE_SHIFT_F16ACC", "MODE_SHIFT_F32ACC", "MODE_NAIVE_F16ACC", "MODE_NOSHIFT_F32ACC", "MODE_SHIFT_F16ALL",
     "PasaError", "attn_fwd", "attn_fwd_alloc", "attn_fwd_shifted", "attn_fwd_stats", "kshift", "workspace_bytes", "check_device_error", "block_rows",
     "library", "library_path",
 ]
@@ -26,6 +26,7 @@ MODE_SHIFT_F16ACC = 0
 MODE_SHIFT_F32ACC = 1
 MODE_NAIVE_F16ACC = 2
 MODE_NOSHIFT_F32ACC = 3
+MODE_SHIFT_F16ALL = 4   # mode 0 with an fp16 PV accumulator and an fp16 running row sum
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_HERE, "libpasa.so")
@@ -104,7 +105,7 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, mode: in
     """O, LSE of softmax(scale * Q K^T) V via libpasa (q [B,Hq,Sq,D], k/v [B,Hkv,Sk,D], fp16).
 
     Returns (o fp16 [B,Hq,Sq,D], lse fp32 [B,Hq,Sq] or None). ``mode`` is one of the MODE_*
-    constants. The workspace (modes 0/1) is taken from PyTorch's allocator unless given.
+    constants. The workspace (modes 0/1/4) is taken from PyTorch's allocator unless given.
     """
     lib = library()
     _check(q, "q"), _check(k, "k"), _check(v, "v")
@@ -153,7 +154,7 @@ def attn_fwd_alloc(q, k, v, causal: bool = False, scale: float | None = None, mo
 def attn_fwd_stats(q, k, v, causal: bool = False, scale: float | None = None, mode: int = MODE_SHIFT_F16ACC):
     """attn_fwd plus per-row score magnitudes: returns (o, lse, stats [B,Hq,Sq,2] fp32).
 
-    stats[..., 0] = max |score held by the accumulator| (S' for modes 0/1, S for 2/3),
+    stats[..., 0] = max |score held by the accumulator| (S' for modes 0/1/4, S for 2/3),
     stats[..., 1] = max |S' + q.m| (the recovered raw score; = [..., 0] for modes 2/3).
     """
     lib = library()
@@ -175,7 +176,7 @@ def attn_fwd_stats(q, k, v, causal: bool = False, scale: float | None = None, mo
 
 def attn_fwd_shifted(q, k_shifted, means, v, causal: bool = False, scale: float | None = None,
                      mode: int = MODE_SHIFT_F16ACC, out=None, lse=None):
-    """The attention kernel alone on keys from :func:`kshift` (modes 0/1) or raw keys (2/3)."""
+    """The attention kernel alone on keys from :func:`kshift` (modes 0/1/4) or raw keys (2/3)."""
     lib = library()
     _check(q, "q"), _check(k_shifted, "k_shifted"), _check(v, "v")
     if means is not None:

@@ -29,7 +29,11 @@
 //
 // Score modes: the QK^T accumulator is fp16 (F16ACC, the PASA regime) or fp32. SHIFT
 // selects shifted keys + offsets (PASA) or raw keys (no shift: the naive fp16 kernel or the
-// plain fp32-accumulate FlashAttention). P is rounded to fp16 and PV accumulates in fp32.
+// plain fp32-accumulate FlashAttention). P is rounded to fp16 and PV accumulates in fp32,
+// except with F16PV (half precision throughout the FlashAttention loop, Abstract): the PV
+// accumulator O is fp16 in TMEM (tcgen05 F16 D format, rescaled in f16x2 arithmetic) and
+// the running row sum is fp16 (each block's probabilities summed in f16x2, then added in
+// fp16). The running max, the offsets and the final division stay fp32.
 //
 // STATS (diagnostic build): per query row, the largest |score| the score accumulator held
 // (S' with the shift, S without; fp16 values in the fp16-accumulate modes, inf if one
@@ -152,11 +156,13 @@ __device__ __forceinline__ void tmem_ld_scores_f16(uint32_t taddr, uint32_t* hp)
   if constexpr (BN % 32 != 0) tmem_ld_x8_pack16(taddr + (BN / 32) * 32, hp + (BN / 32) * 16);
 }
 
-template <int D, int BN, bool F16ACC, bool SHIFT, bool CAUSAL, int KST, int VST, bool STATS = false>
+template <int D, int BN, bool F16ACC, bool SHIFT, bool CAUSAL, int KST, int VST, bool STATS = false,
+          bool F16PV = false>
 __global__ void __launch_bounds__(kAttnThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                 const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapO,
                 const __grid_constant__ CUtensorMap mapM, const AttnParams p) {
+  static_assert(!F16PV || F16ACC, "fp16 PV accumulation is a variant of the fp16-score mode");
   using Smem = AttnSmem<D, BN, KST, VST>;
   using TM = TmemMap<D, BN>;
   extern __shared__ uint8_t smem_raw[];
@@ -335,7 +341,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     // ------------------------------------------------------------------ PV issuer
     // PV(j) once the softmax has written P of block j and V_j has landed.
     if (lane == 0) {
-      constexpr uint32_t id_o = idesc_f16(kTileRows, D, true, true);
+      constexpr uint32_t id_o = idesc_f16(kTileRows, D, !F16PV, true);
       constexpr uint32_t hi_v = sdesc_hi_sw128(1024);
       const uint32_t v_lo0 = sdesc_lo(smem_u32(s.v[0]), Smem::kKChunk);
       constexpr uint32_t kVStride = sizeof(s.v[0]) >> 4;
@@ -464,13 +470,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         rescale = __any_sync(0xffffffffu, need);
         if (need) {
           alpha = ex2_approx(m_run - m_new);
-          l_run *= alpha;
+          if constexpr (F16PV) l_run = __half2float(__hmul(__float2half_rn(l_run), __float2half_rn(alpha)));
+          else l_run *= alpha;
           m_run = m_new;
         }
       }
       // p = exp2((S' + c) * scale*log2e - m): MUFU ex2 per element, packed fp32 arithmetic per
       // pair, row sums in four independent pair accumulators.
       float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      uint32_t hs[4] = {0u, 0u, 0u, 0u};  // F16PV: fp16 row-sum accumulators (f16x2)
       uint32_t pk[kPairs];
       if constexpr (F16ACC) {
         // x = (S' + (c - m / sl2)) * sl2
@@ -482,9 +490,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
           fmul2(x0, x1, y0, y1, sl2, sl2);
           const float p0 = ex2_approx(x0);
           const float p1 = ex2_approx(x1);
-          const int a = (c & 3) * 2;
-          fadd2(rs[a], rs[a + 1], rs[a], rs[a + 1], p0, p1);
           pk[c] = pack_half2(p0, p1);
+          if constexpr (F16PV) {
+            hs[c & 3] = hadd2(hs[c & 3], pk[c]);
+          } else {
+            const int a = (c & 3) * 2;
+            fadd2(rs[a], rs[a + 1], rs[a], rs[a + 1], p0, p1);
+          }
         }
       } else {
         const float bias = (m_run == -INFINITY) ? 0.0f : c_raw * sl2 - m_run;
@@ -499,22 +511,42 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
           pk[c] = pack_half2(p0, p1);
         }
       }
-      const float rowsum = ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
-      l_run += rowsum;
+      if constexpr (F16PV) {
+        const uint32_t h = hadd2(hadd2(hs[0], hs[1]), hadd2(hs[2], hs[3]));
+        const __half rsum = __hadd(__ushort_as_half(static_cast<unsigned short>(h & 0xFFFFu)),
+                                   __ushort_as_half(static_cast<unsigned short>(h >> 16)));
+        l_run = __half2float(__hadd(__float2half_rn(l_run), rsum));
+      } else {
+        const float rowsum = ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
+        l_run += rowsum;
+      }
       // PV(j-1) has to be done before O is rescaled or P rewritten; the exponentials above
       // overlap it.
       if (j >= 1 && !mbar_wait(&s.p_free, (j - 1) & 1, abort_flag, 0x320)) { ok = false; break; }
       tc_fence_after();
       if (rescale) {
         uint32_t w[16];
+        if constexpr (F16PV) {
+          const uint32_t a2 = pack_half2(alpha, alpha);
 #pragma unroll
-        for (int c = 0; c < D / 16; ++c) {
-          tmem_ld_x16(tO + c * 16, w);
-          tmem_ld_wait();
-          reg_fence<16>(w);
+          for (int c = 0; c < D / 32; ++c) {
+            tmem_ld_x16_pack16(tO + c * 32, w);
+            tmem_ld_wait();
+            reg_fence<16>(w);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(__uint_as_float(w[e]) * alpha);
-          tmem_st_x16(tO + c * 16, w);
+            for (int e = 0; e < 16; ++e) w[e] = hmul2(w[e], a2);
+            tmem_st_x16_unpack16(tO + c * 32, w);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < D / 16; ++c) {
+            tmem_ld_x16(tO + c * 16, w);
+            tmem_ld_wait();
+            reg_fence<16>(w);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(__uint_as_float(w[e]) * alpha);
+            tmem_st_x16(tO + c * 16, w);
+          }
         }
       }
 #pragma unroll
@@ -534,27 +566,57 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     tc_fence_after();
     const float inv_l = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
     uint8_t* stage = s.q;
-#pragma unroll
-    for (int c = 0; c < D / 16; ++c) {
-      uint32_t w[16];
-      if (have_o && ok) {
-        tmem_ld_x16(tO + c * 16, w);
-        tmem_ld_wait();
-        reg_fence<16>(w);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 16; ++e) w[e] = 0u;
-      }
-      uint32_t h[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e)
-        h[e] = pack_half2(__uint_as_float(w[2 * e]) * inv_l, __uint_as_float(w[2 * e + 1]) * inv_l);
-      const int col = c * 16;
+    // 16 output columns starting at col, as 8 packed fp16 pairs, into the swizzled staging
+    auto stage16 = [&](int col, const uint32_t* h) {
       const int chunk = col / 64;
       const int u0 = (col % 64) / 8;
       uint8_t* rowp = stage + chunk * Smem::kQChunk + r * 128;
       *reinterpret_cast<uint4*>(rowp + ((u0 ^ (r & 7)) * 16)) = make_uint4(h[0], h[1], h[2], h[3]);
       *reinterpret_cast<uint4*>(rowp + (((u0 + 1) ^ (r & 7)) * 16)) = make_uint4(h[4], h[5], h[6], h[7]);
+    };
+    if constexpr (F16PV) {
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t w[16];
+        if (have_o && ok) {
+          tmem_ld_x16_pack16(tO + c * 32, w);
+          tmem_ld_wait();
+          reg_fence<16>(w);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) w[e] = 0u;
+        }
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t h[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const uint32_t v2 = w[half * 8 + e];
+            const float lo = __half2float(__ushort_as_half(static_cast<unsigned short>(v2 & 0xFFFFu)));
+            const float hi = __half2float(__ushort_as_half(static_cast<unsigned short>(v2 >> 16)));
+            h[e] = pack_half2(lo * inv_l, hi * inv_l);
+          }
+          stage16(c * 32 + half * 16, h);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < D / 16; ++c) {
+        uint32_t w[16];
+        if (have_o && ok) {
+          tmem_ld_x16(tO + c * 16, w);
+          tmem_ld_wait();
+          reg_fence<16>(w);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) w[e] = 0u;
+        }
+        uint32_t h[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          h[e] = pack_half2(__uint_as_float(w[2 * e]) * inv_l, __uint_as_float(w[2 * e + 1]) * inv_l);
+        stage16(c * 16, h);
+      }
     }
     fence_proxy_async_smem();
     named_bar_sync(1, 128);

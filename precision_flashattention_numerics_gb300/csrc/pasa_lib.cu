@@ -92,14 +92,14 @@ int kshift_dispatch(const void* k, void* ks, void* means, int B, int H, int Sk, 
   return D == 64 ? launch_kshift<64>(k, ks, means, B, H, Sk, st) : launch_kshift<128>(k, ks, means, B, H, Sk, st);
 }
 
-template <int D, bool F16ACC, bool SHIFT, bool CAUSAL, bool STATS>
+template <int D, bool F16ACC, bool SHIFT, bool CAUSAL, bool STATS, bool F16PV = false>
 int launch_attn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mo,
                 const CUtensorMap& mm, const pasa::AttnParams& p, cudaStream_t st) {
   constexpr int BN = pasa::block_rows_for(D);
   constexpr int KST = D == 128 ? 3 : 4;  // K ring slots (D = 128: 200 KB of shared memory)
   constexpr int VST = D == 128 ? 2 : 4;
   using Smem = pasa::AttnSmem<D, BN, KST, VST>;
-  auto kern = pasa::attn_fwd_kernel<D, BN, F16ACC, SHIFT, CAUSAL, KST, VST, STATS>;
+  auto kern = pasa::attn_fwd_kernel<D, BN, F16ACC, SHIFT, CAUSAL, KST, VST, STATS, F16PV>;
   const int smem = static_cast<int>(sizeof(Smem)) + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -121,10 +121,18 @@ int attn_dispatch(int mode, int causal, const CUtensorMap& mq, const CUtensorMap
     PASA_CASE(PASA_MODE_SHIFT_F32ACC, false, true)
     PASA_CASE(PASA_MODE_NAIVE_F16ACC, true, false)
     PASA_CASE(PASA_MODE_NOSHIFT_F32ACC, false, false)
+    case PASA_MODE_SHIFT_F16ALL:
+      return causal ? launch_attn<D, true, true, true, STATS, true>(mq, mk, mv, mo, mm, p, st)
+                    : launch_attn<D, true, true, false, STATS, true>(mq, mk, mv, mo, mm, p, st);
     default:
       return PASA_ERR_UNSUPPORTED;
   }
 #undef PASA_CASE
+}
+
+// Modes that shift the keys (and so need the pseudo-average workspace).
+bool shift_mode(int mode) {
+  return mode == PASA_MODE_SHIFT_F16ACC || mode == PASA_MODE_SHIFT_F32ACC || mode == PASA_MODE_SHIFT_F16ALL;
 }
 
 int validate(const void* q, const void* k, const void* v, const void* o, const float* lse, int B, int Hq, int Hkv,
@@ -132,7 +140,7 @@ int validate(const void* q, const void* k, const void* v, const void* o, const f
   if (!q || !k || !v || !o) return PASA_ERR_NULLPTR;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Sk <= 0 || Hq % Hkv != 0) return PASA_ERR_SHAPE;
   if (D != 64 && D != 128) return PASA_ERR_UNSUPPORTED;
-  if (mode < PASA_MODE_SHIFT_F16ACC || mode > PASA_MODE_NOSHIFT_F32ACC) return PASA_ERR_UNSUPPORTED;
+  if (mode < PASA_MODE_SHIFT_F16ACC || mode > PASA_MODE_SHIFT_F16ALL) return PASA_ERR_UNSUPPORTED;
   // grid size, TMA plane counts and flat LSE indices fit in 32-bit signed integers
   const long long n_qblk = (static_cast<long long>(Sq) + pasa::kTileRows - 1) / pasa::kTileRows;
   if (n_qblk * Hq * B > 0x7fffffffLL) return PASA_ERR_SHAPE;
@@ -174,7 +182,7 @@ const char* pasa_strerror(int status) {
 
 size_t pasa_attn_fwd_workspace_bytes(int B, int Hkv, int Sk, int D, int mode) {
   if (B <= 0 || Hkv <= 0 || Sk <= 0 || pasa::block_rows_for(D) == 0) return 0;
-  if (mode != PASA_MODE_SHIFT_F16ACC && mode != PASA_MODE_SHIFT_F32ACC) return 0;
+  if (!shift_mode(mode)) return 0;
   return workspace_layout(B, Hkv, Sk, D).total;
 }
 
@@ -193,7 +201,7 @@ int pasa_kshift(const void* k, void* k_shifted, void* means, int B, int H, int S
 static int attn_launch(const void* q, const void* kk, const void* mm, const void* v, void* o, float* lse, int B,
                        int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale, int mode, cudaStream_t st,
                        float* stats = nullptr) {
-  const bool shift = mode == PASA_MODE_SHIFT_F16ACC || mode == PASA_MODE_SHIFT_F32ACC;
+  const bool shift = shift_mode(mode);
   if (!(scale > 0.0f) || !std::isfinite(scale)) scale = 1.0f / std::sqrt(static_cast<float>(D));
   const int bn = pasa::block_rows_for(D);
   const int nb = (Sk + bn - 1) / bn;
@@ -232,7 +240,7 @@ int pasa_attn_fwd_shifted(const void* q, const void* k_shifted, const void* mean
                           int mode, void* stream) {
   int rc = validate(q, k_shifted, v, o, lse, B, Hq, Hkv, Sq, Sk, D, mode);
   if (rc != PASA_OK) return rc;
-  const bool shift = mode == PASA_MODE_SHIFT_F16ACC || mode == PASA_MODE_SHIFT_F32ACC;
+  const bool shift = shift_mode(mode);
   if (shift && !means) return PASA_ERR_NULLPTR;
   if (shift && !aligned16(means)) return PASA_ERR_ALIGN;
   rc = check_device();
@@ -246,7 +254,7 @@ int pasa_attn_fwd_ws(const void* q, const void* k, const void* v, void* o, float
                      size_t workspace_bytes, void* stream) {
   int rc = validate(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, mode);
   if (rc != PASA_OK) return rc;
-  const bool shift = mode == PASA_MODE_SHIFT_F16ACC || mode == PASA_MODE_SHIFT_F32ACC;
+  const bool shift = shift_mode(mode);
   const WorkspaceLayout wl = workspace_layout(B, Hkv, Sk, D);
   if (shift) {
     if (!workspace || workspace_bytes < wl.total) return PASA_ERR_WORKSPACE;
@@ -277,7 +285,7 @@ int pasa_attn_fwd_stats(const void* q, const void* k, const void* v, void* o, fl
   if (rc != PASA_OK) return rc;
   if (!stats) return PASA_ERR_NULLPTR;
   if ((reinterpret_cast<uintptr_t>(stats) & 7u) != 0) return PASA_ERR_ALIGN;
-  const bool shift = mode == PASA_MODE_SHIFT_F16ACC || mode == PASA_MODE_SHIFT_F32ACC;
+  const bool shift = shift_mode(mode);
   const WorkspaceLayout wl = workspace_layout(B, Hkv, Sk, D);
   if (shift) {
     if (!workspace || workspace_bytes < wl.total) return PASA_ERR_WORKSPACE;

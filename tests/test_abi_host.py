@@ -68,8 +68,9 @@ def test_argument_errors(lib):
     assert call(lib, Hq=3, Hkv=2) == -2
     assert call(lib, D=96) == -3
     assert call(lib, D=256) == -3
-    assert call(lib, mode=4) == -3
+    assert call(lib, mode=5) == -3
     assert call(lib, mode=-1) == -3
+    assert call(lib, mode=4, ws=None) == -7          # mode 4 shifts the keys: it needs the workspace
     assert call(lib, k=FAKE_MIS) == -4
     assert call(lib, lse=FAKE_MIS) == -4
     # modes with the shift need a workspace of the advertised size
@@ -97,7 +98,7 @@ def test_workspace_bytes(lib):
         return -(-(a + B * H * nb * D * 2) // 256) * 256
 
     for (B, H, Sk, D) in [(1, 4, 4096, 128), (2, 5, 9216, 64), (1, 1, 1, 64), (4, 8, 8192, 128)]:
-        for mode in (0, 1):
+        for mode in (0, 1, 4):
             assert lib.pasa_attn_fwd_workspace_bytes(B, H, Sk, D, mode) == expect(B, H, Sk, D)
         for mode in (2, 3):
             assert lib.pasa_attn_fwd_workspace_bytes(B, H, Sk, D, mode) == 0
