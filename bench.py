@@ -42,13 +42,13 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one attention-kernel launch,
 # from an ncu capture of a quarter of the 32K workload (7 of 28 query heads, 1 of 4 kv heads:
-# 75.65 MB read + 24.80 MB written) scaled x4 to a full launch; the traffic is per head, so it
+# 75.79 MB read + 24.62 MB written) scaled x4 to a full launch; the traffic is per head, so it
 # grows in proportion. Summary and command: profiles/attn_fwd_kbias10_t3_b1h7g1_s32768_full.md.
 # Reported only while the kernel source is the one the counters were taken on.
 TRAFFIC_WORKLOAD = "kbias10_t3_b1h28g4_s32768_d128_causal"
 TRAFFIC_MODE = 0
-TRAFFIC_BYTES = 4 * (75.649792e6 + 24.798720e6)
-TRAFFIC_KERNEL_SHA = "f0216f659691a9ac"
+TRAFFIC_BYTES = 4 * (75.793920e6 + 24.617216e6)
+TRAFFIC_KERNEL_SHA = "fe4170540f6e40a7"
 
 
 def measured_traffic(w, mode):

@@ -125,13 +125,19 @@ int pasa_attn_fwd_ws(const void* q, const void* k, const void* v, void* o, float
  *                       accumulator overflowed);
  *   stats[b, h, i, 1] = max over visible keys of |S' + q_i . m_j|, the recovered raw score
  *                       (modes 0/1/4; equal to [0] for modes 2/3).
- * stats is fp32 [B, Hq, Sq, 2], 8-byte aligned; rows with no visible key get 0. o and lse
- * are written as in pasa_attn_fwd_ws. Runs a separately compiled variant of the attention
- * kernel that also tracks the per-block minimum score.
+ * stats is fp32 [B, Hq, Sq, 2], 8-byte aligned; rows with no visible key get 0.
+ * block_stats, if not NULL, is fp32 [B, Hq, ceil(Sk / pasa_block_rows(D)), 2], 8-byte
+ * aligned, and gets the same two magnitudes per key block, as the max over all query rows
+ * that see the block (0 for a block no row sees). Their ratio tells the Abstract's two
+ * causes apart: a sequence-dimension bias of K is removed by the shift ([0] << [1] in the
+ * PASA modes), Q/K resonance within a block is not ([0] close to [1]). The call zeroes
+ * block_stats on the stream before the kernel. o and lse are written as in
+ * pasa_attn_fwd_ws. Runs a separately compiled variant of the attention kernel that also
+ * tracks the per-block minimum score.
  */
-int pasa_attn_fwd_stats(const void* q, const void* k, const void* v, void* o, float* lse, float* stats, int B,
-                        int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale, int mode, void* workspace,
-                        size_t workspace_bytes, void* stream);
+int pasa_attn_fwd_stats(const void* q, const void* k, const void* v, void* o, float* lse, float* stats,
+                        float* block_stats, int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,
+                        int mode, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * The attention kernel alone, on keys already shifted by pasa_kshift (for modes 0, 1 and 4:

@@ -4,8 +4,9 @@ TEST INFRASTRUCTURE ONLY. Only ``tests/``, ``__graft_entry__.smoke()`` and the C
 leg of ``bench.py`` may import this package. The product path (the CUDA library and its
 Python binding) never touches it, and it shares no code with them.
 
-* :func:`attention` / :func:`attention_recovered` / :func:`row_max_abs_score` wrap the plain
-  C implementation in ``attention_ref.c`` (compiled with gcc by :func:`build`).
+* :func:`attention` / :func:`attention_recovered` / :func:`row_max_abs_score` /
+  :func:`row_max_abs_recovered` / :func:`block_max_abs_score` wrap the plain C
+  implementation in ``attention_ref.c`` (compiled with gcc by :func:`build`).
 * ``pseudo_average`` holds the numpy reference for the key-block pseudo-average and the
   shifted keys.
 """
@@ -57,6 +58,8 @@ def _load():
             lib.oracle_row_max_abs_recovered.argtypes = [p, p, p, i64, p, i64, i64, i64, i64, i64, i64,
                                                          ctypes.c_int, p, i64]
             lib.oracle_row_max_abs_recovered.restype = ctypes.c_int
+            lib.oracle_block_max_abs_score.argtypes = [p, p, p, i64, p, i64, i64, i64, i64, i64, i64, ctypes.c_int]
+            lib.oracle_block_max_abs_score.restype = ctypes.c_int
             lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
             lib.oracle_half_to_double.restype = ctypes.c_double
             _lib = lib
@@ -146,6 +149,22 @@ def row_max_abs_recovered(q, kshift, means, block_rows: int, causal: bool, rows=
     if rc != 0:
         raise ValueError("oracle_row_max_abs_recovered: bad shape")
     return out if r is not None else out.reshape(B, Hq, Sq)
+
+
+def block_max_abs_score(q, k, block_rows: int, causal: bool, means=None) -> np.ndarray:
+    """Per key block, max |q_i . k_j| (or |q_i . (k_j + m_block)| with means) over the rows
+    that see the block's keys, in fp64: [B, Hq, ceil(Sk / block_rows)]."""
+    B, Hq, Sq, D = q.shape
+    _, Hkv, Sk, _ = k.shape
+    nb = -(-Sk // block_rows)
+    qb, kb = _bits(q), _bits(k)
+    mb = None if means is None else _bits(means)
+    out = np.empty((B, Hq, nb), np.float64)
+    rc = _load().oracle_block_max_abs_score(_ptr(qb), _ptr(kb), _ptr(mb), block_rows, _ptr(out), B, Hq, Hkv, Sq,
+                                            Sk, D, int(bool(causal)))
+    if rc != 0:
+        raise ValueError("oracle_block_max_abs_score: bad shape")
+    return out
 
 
 def half_to_double(bits: int) -> float:

@@ -233,3 +233,41 @@ int oracle_row_max_abs_recovered(const uint16_t *q, const uint16_t *kshift, cons
     }
     return 0;
 }
+
+/*
+ * Per key block, the largest |q_i . k_j| over every query row i and every key j of the
+ * block that i sees (causal or not), unscaled: out [B, Hq, ceil(Sk / block_rows)]. A block
+ * no row sees gives 0. With k = the shifted keys this is the magnitude the fp16 score
+ * accumulator holds for that block; with means != NULL the score is q_i . (k'_j + m_(j /
+ * block_rows)), the recovered raw score (Abstract: "global recovering").
+ */
+int oracle_block_max_abs_score(const uint16_t *q, const uint16_t *k, const uint16_t *means,
+                               int64_t block_rows, double *out, int64_t B, int64_t Hq, int64_t Hkv,
+                               int64_t Sq, int64_t Sk, int64_t D, int causal) {
+    if (Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || block_rows <= 0) return -1;
+    init_table();
+    int64_t group = Hq / Hkv;
+    int64_t nb = (Sk + block_rows - 1) / block_rows;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t bh = 0; bh < B * Hq; ++bh) {
+        int64_t b = bh / Hq, h = bh % Hq;
+        const uint16_t *kh = k + (b * Hkv + h / group) * Sk * D;
+        const uint16_t *mh = means ? means + (b * Hkv + h / group) * nb * D : NULL;
+        double *o = out + bh * nb;
+        for (int64_t jb = 0; jb < nb; ++jb) o[jb] = 0.0;
+        for (int64_t i = 0; i < Sq; ++i) {
+            const uint16_t *qrow = q + (bh * Sq + i) * D;
+            int64_t n = visible_keys(i, Sq, Sk, causal);
+            for (int64_t j = 0; j < n; ++j) {
+                double dot = 0.0;
+                for (int64_t d = 0; d < D; ++d) {
+                    double kv = g_h2d[kh[j * D + d]];
+                    if (mh) kv += g_h2d[mh[(j / block_rows) * D + d]];
+                    dot += g_h2d[qrow[d]] * kv;
+                }
+                if (fabs(dot) > o[j / block_rows]) o[j / block_rows] = fabs(dot);
+            }
+        }
+    }
+    return 0;
+}

@@ -41,7 +41,7 @@ SIGNATURES = {
     "pasa_attn_fwd_noalloc": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P], _I),
     "pasa_attn_fwd_workspace_bytes": ([_I, _I, _I, _I, _I], _SZ),
     "pasa_attn_fwd_ws": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P], _I),
-    "pasa_attn_fwd_stats": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P], _I),
+    "pasa_attn_fwd_stats": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P], _I),
     "pasa_attn_fwd_shifted": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P], _I),
     "pasa_kshift": ([_P, _P, _P, _I, _I, _I, _I, _P], _I),
     "pasa_check_device_error": ([_P, ctypes.POINTER(ctypes.c_ulonglong)], _I),
@@ -151,11 +151,13 @@ def attn_fwd_alloc(q, k, v, causal: bool = False, scale: float | None = None, mo
     return out, lse
 
 
-def attn_fwd_stats(q, k, v, causal: bool = False, scale: float | None = None, mode: int = MODE_SHIFT_F16ACC):
-    """attn_fwd plus per-row score magnitudes: returns (o, lse, stats [B,Hq,Sq,2] fp32).
+def attn_fwd_stats(q, k, v, causal: bool = False, scale: float | None = None, mode: int = MODE_SHIFT_F16ACC,
+                   block_stats: bool = False):
+    """attn_fwd plus score magnitudes: returns (o, lse, stats [B,Hq,Sq,2] fp32), and with
+    block_stats=True also the per-key-block maxima [B,Hq,ceil(Sk/128),2] fp32.
 
-    stats[..., 0] = max |score held by the accumulator| (S' for modes 0/1/4, S for 2/3),
-    stats[..., 1] = max |S' + q.m| (the recovered raw score; = [..., 0] for modes 2/3).
+    [..., 0] = max |score held by the accumulator| (S' for modes 0/1/4, S for 2/3),
+    [..., 1] = max |S' + q.m| (the recovered raw score; = [..., 0] for modes 2/3).
     """
     lib = library()
     _check(q, "q"), _check(k, "k"), _check(v, "v")
@@ -164,13 +166,18 @@ def attn_fwd_stats(q, k, v, causal: bool = False, scale: float | None = None, mo
     out = torch.empty_like(q)
     lse = torch.empty((B, Hq, Sq), device=q.device, dtype=torch.float32)
     stats = torch.empty((B, Hq, Sq, 2), device=q.device, dtype=torch.float32)
+    nbt = -(-Sk // lib.pasa_block_rows(D))
+    bstats = torch.empty((B, Hq, nbt, 2), device=q.device, dtype=torch.float32) if block_stats else None
     nbytes = int(lib.pasa_attn_fwd_workspace_bytes(B, Hkv, Sk, D, mode))
     ws = torch.empty(max(nbytes, 1), device=q.device, dtype=torch.uint8)
-    rc = lib.pasa_attn_fwd_stats(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(stats), B, Hq, Hkv, Sq, Sk,
+    rc = lib.pasa_attn_fwd_stats(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(stats),
+                                 _ptr(bstats) if bstats is not None else None, B, Hq, Hkv, Sq, Sk,
                                  D, int(bool(causal)), float(scale) if scale is not None else 0.0, int(mode),
                                  _ptr(ws) if nbytes else None, nbytes, _stream())
     if rc != 0:
         raise PasaError(rc, "pasa_attn_fwd_stats")
+    if bstats is not None:
+        return out, lse, stats, bstats
     return out, lse, stats
 
 

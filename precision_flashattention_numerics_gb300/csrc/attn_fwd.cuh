@@ -39,6 +39,9 @@
 // (S' with the shift, S without; fp16 values in the fp16-accumulate modes, inf if one
 // overflowed) and the largest |S' + c| (the recovered raw score; equal to the first without
 // the shift). A block's min and max of S' give both, since c is constant per row and block.
+// The same two magnitudes are also reduced over the query rows of each key block (a warp
+// max, then one atomicMax per warp on the fp32 bits, which order like the values since
+// both are >= 0) into per-(head, block) maxima.
 //
 // Online softmax in log2 units: x = (S' + c) * scale * log2(e). The running max is only
 // moved when a block raises it by more than kRescaleLog2 (so P <= 2^kRescaleLog2 in fp16);
@@ -65,7 +68,9 @@ struct AttnParams {
   int n_qblk;            // ceil(Sq / kTileRows)
   float scale_log2;      // softmax scale * log2(e)
   float inv_scale_log2;  // 1 / scale_log2
-  float* stats;          // STATS kernels: [B, Hq, Sq, 2] fp32 score magnitudes
+  float* stats;          // STATS kernels: [B, Hq, Sq, 2] fp32 score magnitudes per row
+  unsigned* bstats;      // STATS kernels, or nullptr: [B, Hq, nbt, 2] per key block, fp32 bits
+  int nbt;               // key blocks per head, ceil(Sk / BN)
 };
 
 // TMEM column map (see the header comment).
@@ -453,9 +458,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         }
       }
       if constexpr (STATS) {
-        if (cmax > 0) {
-          st_acc = fmaxf(st_acc, fmaxf(fabsf(mx), fabsf(mn)));
-          st_rec = fmaxf(st_rec, fmaxf(fabsf(mx + c_raw), fabsf(mn + c_raw)));
+        const float a_acc = cmax > 0 ? fmaxf(fabsf(mx), fabsf(mn)) : 0.0f;
+        const float a_rec = cmax > 0 ? fmaxf(fabsf(mx + c_raw), fabsf(mn + c_raw)) : 0.0f;
+        st_acc = fmaxf(st_acc, a_acc);
+        st_rec = fmaxf(st_rec, a_rec);
+        if (p.bstats != nullptr) {
+          const unsigned u_acc = __reduce_max_sync(0xffffffffu, __float_as_uint(a_acc));
+          const unsigned u_rec = __reduce_max_sync(0xffffffffu, __float_as_uint(a_rec));
+          if (lane == 0) {
+            unsigned* bs = p.bstats + ((static_cast<size_t>(b) * p.Hq + hq) * p.nbt + j) * 2;
+            atomicMax(bs, u_acc);
+            atomicMax(bs + 1, u_rec);
+          }
         }
       }
       const float bm = (mx == -INFINITY) ? -INFINITY : (mx + c_raw) * sl2;

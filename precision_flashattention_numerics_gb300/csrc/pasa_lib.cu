@@ -200,7 +200,7 @@ int pasa_kshift(const void* k, void* k_shifted, void* means, int B, int H, int S
 // Launch the attention kernel on (possibly shifted) keys `kk` and block means `mm`.
 static int attn_launch(const void* q, const void* kk, const void* mm, const void* v, void* o, float* lse, int B,
                        int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale, int mode, cudaStream_t st,
-                       float* stats = nullptr) {
+                       float* stats = nullptr, float* block_stats = nullptr) {
   const bool shift = shift_mode(mode);
   if (!(scale > 0.0f) || !std::isfinite(scale)) scale = 1.0f / std::sqrt(static_cast<float>(D));
   const int bn = pasa::block_rows_for(D);
@@ -228,6 +228,12 @@ static int attn_launch(const void* q, const void* kk, const void* mm, const void
   p.scale_log2 = scale * 1.4426950408889634f;
   p.inv_scale_log2 = 1.0f / p.scale_log2;
   p.stats = stats;
+  p.bstats = reinterpret_cast<unsigned*>(block_stats);
+  p.nbt = nb;
+  if (block_stats) {
+    const cudaError_t e = cudaMemsetAsync(block_stats, 0, static_cast<size_t>(B) * Hq * nb * 2 * sizeof(float), st);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
   if (stats)
     return D == 64 ? attn_dispatch<64, true>(mode, causal, mq, mk, mv, mo, mmeans, p, st)
                    : attn_dispatch<128, true>(mode, causal, mq, mk, mv, mo, mmeans, p, st);
@@ -278,13 +284,14 @@ int pasa_attn_fwd_ws(const void* q, const void* k, const void* v, void* o, float
   return attn_launch(q, kk, mm, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, mode, st);
 }
 
-int pasa_attn_fwd_stats(const void* q, const void* k, const void* v, void* o, float* lse, float* stats, int B,
-                        int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale, int mode, void* workspace,
-                        size_t workspace_bytes, void* stream) {
+int pasa_attn_fwd_stats(const void* q, const void* k, const void* v, void* o, float* lse, float* stats,
+                        float* block_stats, int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,
+                        int mode, void* workspace, size_t workspace_bytes, void* stream) {
   int rc = validate(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, mode);
   if (rc != PASA_OK) return rc;
   if (!stats) return PASA_ERR_NULLPTR;
   if ((reinterpret_cast<uintptr_t>(stats) & 7u) != 0) return PASA_ERR_ALIGN;
+  if (block_stats && (reinterpret_cast<uintptr_t>(block_stats) & 7u) != 0) return PASA_ERR_ALIGN;
   const bool shift = shift_mode(mode);
   const WorkspaceLayout wl = workspace_layout(B, Hkv, Sk, D);
   if (shift) {
@@ -304,7 +311,7 @@ int pasa_attn_fwd_stats(const void* q, const void* k, const void* v, void* o, fl
     kk = ws + wl.kshift_off;
     mm = ws + wl.means_off;
   }
-  return attn_launch(q, kk, mm, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, mode, st, stats);
+  return attn_launch(q, kk, mm, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, mode, st, stats, block_stats);
 }
 
 int pasa_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,

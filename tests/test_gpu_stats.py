@@ -96,3 +96,67 @@ def test_stats_show_the_overflow_and_its_absence():
     assert np.all(np.abs(got0[:, 0] - shifted) <= 4 * fp16_spacing(shifted))
     # and the recovered raw magnitude is the one the naive kernel could not hold
     assert np.all(np.abs(got0[:, 1] - raw) <= 1e-2 * raw + 64.0)
+
+
+def block_abs_dot_bound(q, k, causal, bn=128):
+    """Per key block, the max over visible (i, j) of sum_d |q_id k_jd| (bounds every partial
+    sum an fp16 accumulator holds for that block): [B, Hq, ceil(Sk / bn)]."""
+    g = q.shape[1] // k.shape[1]
+    a = np.abs(q.astype(np.float64)) @ np.repeat(np.abs(k.astype(np.float64)), g, axis=1).transpose(0, 1, 3, 2)
+    Sq, Sk = q.shape[2], k.shape[2]
+    if causal:
+        mask = np.arange(Sk)[None, :] <= np.arange(Sq)[:, None] + (Sk - Sq)
+        a = np.where(mask, a, 0.0)
+    nb = -(-Sk // bn)
+    return np.stack([a[..., j * bn:(j + 1) * bn].max(axis=(2, 3)) for j in range(nb)], axis=-1)
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2, 3, 4])
+def test_block_stats_small_ragged(mode):
+    import precision_flashattention_numerics_gb300 as pasa
+
+    w = wl.Workload("bst", 1, 4, 2, 333, 333, 128, True, "kbias", 322, (("bias_std", 20.0),))
+    q, k, v = wl.make_inputs(w)
+    qt, kt, vt = to_dev(q, k, v)
+    o, lse, st, bst = pasa.attn_fwd_stats(qt, kt, vt, causal=True, mode=mode, block_stats=True)
+    pasa.check_device_error()
+    bst = bst.double().cpu().numpy()
+    st = st.double().cpu().numpy()
+    ks, means = pa.kshift_fast(k)
+    shifted = mode in (0, 1, 4)
+    acc_ref = oracle.block_max_abs_score(q, ks if shifted else k, 128, True)
+    rec_ref = oracle.block_max_abs_score(q, ks, 128, True, means=means) if shifted else acc_ref
+    assert bst.shape == acc_ref.shape + (2,)
+    # the per-block and per-row maxima are reductions of the same numbers
+    np.testing.assert_array_equal(bst[..., 0].max(-1), st[..., 0].max(-1))
+    np.testing.assert_array_equal(bst[..., 1].max(-1), st[..., 1].max(-1))
+    if mode in (1, 3):
+        np.testing.assert_allclose(bst[..., 0], acc_ref, rtol=2e-6, atol=1e-3)
+        np.testing.assert_allclose(bst[..., 1], rec_ref, rtol=2e-6, atol=1e-3)
+    else:
+        tol = (q.shape[-1] // 16) * fp16_spacing(block_abs_dot_bound(q, ks if shifted else k, True))
+        assert np.all(np.abs(bst[..., 0] - acc_ref) <= tol)
+        assert np.all(np.abs(bst[..., 1] - rec_ref) <= tol + 4 * fp16_spacing(rec_ref))
+
+
+def test_block_stats_tell_bias_from_resonance():
+    # The two causes of fp16 overflow (Abstract): a sequence-dimension bias of K, which the
+    # shift removes (shifted max << raw max per block), and Q/K resonance varying within a
+    # block, which it does not (shifted max close to raw max).
+    import precision_flashattention_numerics_gb300 as pasa
+
+    cases = {
+        "bias": wl.Workload("b", 1, 4, 2, 1024, 1024, 128, True, "kbias", 331, (("bias_std", 20.0),)),
+        "resonance": wl.Workload("r", 1, 2, 2, 2048, 2048, 64, False, "resonance", 332,
+                                 (("A", 30.0), ("freq", "uniform_pi"), ("noise_std", 0.5), ("phase_flip", True))),
+    }
+    ratio = {}
+    for name, w in cases.items():
+        q, k, v = wl.make_inputs(w)
+        qt, kt, vt = to_dev(q, k, v)
+        _, _, _, bst = pasa.attn_fwd_stats(qt, kt, vt, causal=w.causal, mode=1, block_stats=True)
+        pasa.check_device_error()
+        bst = bst.double().cpu().numpy()
+        ratio[name] = np.median(bst[..., 0] / bst[..., 1])
+    assert ratio["bias"] < 0.2, ratio
+    assert ratio["resonance"] > 0.6, ratio

@@ -211,3 +211,34 @@ def test_row_max_abs_score_brute_force(oracle_mod):
         if causal:
             s = np.where(np.tril(np.ones((9, 9), bool)), s, 0.0)
         np.testing.assert_allclose(got, s.max(-1), rtol=1e-15)
+
+
+def test_block_max_abs_score_brute_force(oracle_mod):
+    # per key block, max |q_i . k_j| over the (i, j) pairs the mask allows, by a dense numpy
+    # product on a tiny causal GQA case with a ragged last block (Sk = 10, blocks of 4)
+    rng = np.random.default_rng(41)
+    q = rng.standard_normal((2, 4, 7, 8)).astype(np.float16)
+    k = rng.standard_normal((2, 2, 10, 8)).astype(np.float16)
+    for causal in (False, True):
+        got = oracle_mod.block_max_abs_score(q, k, 4, causal)
+        s = np.abs(q.astype(np.float64) @ np.repeat(k, 2, axis=1).astype(np.float64).transpose(0, 1, 3, 2))
+        if causal:
+            i = np.arange(7)[:, None]
+            j = np.arange(10)[None, :]
+            s = np.where(j <= i + 10 - 7, s, 0.0)
+        want = np.stack([s[..., 0:4].max(axis=(2, 3)), s[..., 4:8].max(axis=(2, 3)), s[..., 8:10].max(axis=(2, 3))], -1)
+        np.testing.assert_array_equal(got, want)
+        # the largest block value of a head is the largest row value of the head
+        np.testing.assert_array_equal(got.max(-1), oracle_mod.row_max_abs_score(q, k, causal).max(-1))
+
+
+def test_block_max_abs_score_recovered_equals_raw_when_shift_is_exact(oracle_mod):
+    from oracle import pseudo_average as pa
+
+    rng = np.random.default_rng(42)
+    q = rng.integers(-3, 4, (1, 2, 30, 16)).astype(np.float16)
+    k = (rng.integers(-20, 21, (1, 1, 300, 16)) + rng.integers(-200, 200, (1, 1, 1, 16))).astype(np.float16)
+    ks, means = pa.kshift(k, block_rows=128)
+    raw = oracle_mod.block_max_abs_score(q, k, 128, False)
+    np.testing.assert_array_equal(oracle_mod.block_max_abs_score(q, ks, 128, False, means=means), raw)
+    assert (oracle_mod.block_max_abs_score(q, ks, 128, False) < 0.5 * raw).all()   # the bias is gone
