@@ -36,8 +36,10 @@ import workloads as wl  # noqa: E402
 
 DEFAULT_WORKLOAD = "kbias10_t3_b1h28g4_s32768_d128_causal"
 ALSO_WORKLOADS = ["iid_b4h32g8_s8192_d128_causal"]
-MODE_NAMES = {0: "shift_f16acc", 1: "shift_f32acc", 2: "naive_f16acc", 3: "noshift_f32acc", 4: "shift_f16all"}
-SHIFT_MODES = (0, 1, 4)
+MODE_NAMES = {0: "shift_f16acc", 1: "shift_f32acc", 2: "naive_f16acc", 3: "noshift_f32acc", 4: "shift_f16all",
+              5: "shift_fp8", 6: "naive_fp8"}
+SHIFT_MODES = (0, 1, 4)     # a pseudo-average shift kernel (fp16 K') runs before the attention kernel
+FP8_MODES = (5, 6)          # an e4m3 key-preparation kernel runs before it
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one attention-kernel launch,
@@ -199,14 +201,28 @@ def bench_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int, also
     lse = torch.empty((w.B, w.Hq, w.Sq), device=dev, dtype=torch.float32)
     nb = (w.Sk + pasa.block_rows(w.D) - 1) // pasa.block_rows(w.D)
     shift = args.mode in SHIFT_MODES
+    fp8 = args.mode in FP8_MODES
     ks = torch.empty_like(kt) if shift else kt
     means = torch.empty((w.B, w.Hkv, nb, w.D), device=dev, dtype=torch.float16) if shift else None
     stream = torch.cuda.current_stream()
+    prep = {}
 
-    def step():
+    def prep_keys():
         if shift:
             pasa.kshift(kt, out=ks, means=means)
-        pasa.attn_fwd_shifted(qt, ks, means, vt, causal=w.causal, mode=args.mode, out=o, lse=lse)
+        elif fp8:
+            prep["k8"], prep["means"], prep["kscale"] = pasa.kprep_fp8(kt, mode=args.mode)
+
+    def attention():
+        if fp8:
+            pasa.attn_fwd_fp8(qt, prep["k8"], prep["means"], prep["kscale"], vt, causal=w.causal, mode=args.mode,
+                              out=o, lse=lse)
+        else:
+            pasa.attn_fwd_shifted(qt, ks, means, vt, causal=w.causal, mode=args.mode, out=o, lse=lse)
+
+    def step():
+        prep_keys()
+        attention()
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -225,10 +241,9 @@ def bench_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int, also
     t_start.record(stream)
     for i in range(n):
         ev[i][0].record(stream)
-        if shift:
-            pasa.kshift(kt, out=ks, means=means)
+        prep_keys()
         ev[i][1].record(stream)
-        pasa.attn_fwd_shifted(qt, ks, means, vt, causal=w.causal, mode=args.mode, out=o, lse=lse)
+        attention()
         ev[i][2].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
@@ -239,7 +254,7 @@ def bench_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int, also
     total_ms = t_start.elapsed_time(t_end)
     total_ms = max_over_ranks(total_ms, world)
     attn_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(n)]
-    kshift_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(n)] if shift else [0.0] * n
+    kshift_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(n)] if (shift or fp8) else [0.0] * n
     flops = w.flops()
     finite = bool(torch.isfinite(o).all().item())
     res = {
@@ -301,7 +316,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="pasa", choices=["pasa", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.WORKLOADS))
-    ap.add_argument("--mode", type=int, default=0, choices=[0, 1, 2, 3, 4])
+    ap.add_argument("--mode", type=int, default=0, choices=[0, 1, 2, 3, 4, 5, 6])
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-also", action="store_true")
@@ -359,18 +374,29 @@ def main():
                           "finite": ra["finite"]}
 
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))  # fp16 dense = bf16 dense rate
+    peak_note = f"{peak_src} bf16 dense burst (fp16 dense has the same nominal rate)"
+    if args.mode in FP8_MODES:
+        # half the FLOPs (QK) at the e4m3 rate, nominally 2x the 16-bit one, half (PV) at fp16:
+        # the time at peak is 3/4 of the all-fp16 time
+        peak = peak * 4.0 / 3.0
+        peak_note = (f"{peak_src} bf16 dense burst x 4/3: QK at the e4m3 rate (nominally 2x the 16-bit rate), "
+                     "PV at the fp16 rate")
     traffic = measured_traffic(w, args.mode)
     attn_achieved = res["flops"] / (res["attn_ms"] * 1e-3) / 1e12
     roofline = {
         "kernel": "attn_fwd_kernel", "bound": "tensor", "achieved": round(attn_achieved, 1), "peak": peak,
         "unit": "TFLOP/s", "frac": round(attn_achieved / peak, 4), "traffic": traffic,
-        "peak_source": f"{peak_src} bf16 dense burst (fp16 dense has the same nominal rate)",
+        "peak_source": peak_note,
     }
     kshift_kernel = None
-    if args.mode in SHIFT_MODES:
+    if args.mode in SHIFT_MODES or args.mode in FP8_MODES:
         import precision_flashattention_numerics_gb300 as pasa
 
-        kb = 2 * (w.B * w.Hkv * w.Sk * w.D * 2) + w.B * w.Hkv * math.ceil(w.Sk / pasa.block_rows(w.D)) * w.D * 2
+        nbk = math.ceil(w.Sk / pasa.block_rows(w.D))
+        if args.mode in FP8_MODES:   # K read, e4m3 codes, block scales (and means in mode 5) written
+            kb = w.B * w.Hkv * (w.Sk * w.D * 3 + nbk * 4 + (nbk * w.D * 2 if args.mode == 5 else 0))
+        else:
+            kb = 2 * (w.B * w.Hkv * w.Sk * w.D * 2) + w.B * w.Hkv * nbk * w.D * 2
         gbs = kb / (res["kshift_ms"] * 1e-3) / 1e9
         hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
         kshift_kernel = {"kernel": "kshift_kernel", "bound": "hbm", "achieved": round(gbs, 1), "peak": hbm,
@@ -387,9 +413,10 @@ def main():
             "metric": "PASA attn fwd TFLOP/s at 1 GB300 (fraction of dense fp16 tensor peak in roofline)",
             "value": round(res["tflops"], 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": max(3, args.warmup), "ms_per_step": round(res["ms_per_step"], 5), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic", "config": config,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3+f16" if args.mode in FP8_MODES else "f16",
+            "data": "synthetic", "config": config,
             "roofline": roofline, "kshift": kshift_kernel, "cpu_baseline": cpu, "e2e": res["e2e"],
-            "gpu_launches": args.steps * (2 if args.mode in SHIFT_MODES else 1), "clocks": res["clocks"],
+            "gpu_launches": args.steps * (2 if (args.mode in SHIFT_MODES or args.mode in FP8_MODES) else 1), "clocks": res["clocks"],
             "finite_output": res["finite"], "also": also,
         }
         print(json.dumps(out))

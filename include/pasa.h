@@ -56,6 +56,14 @@ extern "C" {
  * throughout FlashAttention): mode 0, plus an fp16 PV accumulator and an fp16 running row
  * sum. The running max, the offsets and the final division stay fp32. */
 #define PASA_MODE_SHIFT_F16ALL 4
+/* FP8 scores (D = 128 only). Each query row of Q and each 128-key block of keys is quantised
+ * to e4m3 (largest value 448) with one fp32 scale (row or block absolute maximum / 448);
+ * the score GEMM takes e4m3 operands and accumulates in fp32; the rest is mode 1. Mode 5
+ * quantises the shifted keys K' (PASA, offsets carried as in mode 1), mode 6 the raw keys
+ * (no shift, the naive 8-bit kernel). Not available in pasa_attn_fwd_shifted or
+ * pasa_attn_fwd_stats. */
+#define PASA_MODE_SHIFT_FP8 5
+#define PASA_MODE_NAIVE_FP8 6
 
 /* Keys per block for head dim D: the block the pseudo-average is taken over, which is also
  * the attention kernel's key tile (128 for D = 64 and D = 128; 0 for other D). */
@@ -71,7 +79,7 @@ int pasa_block_rows(int D);
  *             be NULL to skip it.
  *   causal    0 or 1 (bottom-right aligned mask).
  *   scale     softmax scale; <= 0 selects 1/sqrt(D).
- *   mode      PASA_MODE_* above. Modes 0, 1 and 4 need a workspace for the shifted keys and
+ *   mode      PASA_MODE_* above. Modes 0, 1, 4, 5 and 6 need a workspace for the shifted keys and
  *             block means: this entry point takes it from the CUDA stream-ordered allocator
  *             (cudaMallocAsync / cudaFreeAsync on `stream`); use pasa_attn_fwd_ws to pass
  *             your own.
@@ -102,7 +110,8 @@ int pasa_attn_fwd(const void* q, const void* k, const void* v, void* o, float* l
 int pasa_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
                           int Hkv, int Sq, int Sk, int D, int causal, float scale, int mode, void* stream);
 
-/* Workspace bytes pasa_attn_fwd_ws needs for these sizes and mode (0 for modes 2 and 3). */
+/* Workspace bytes pasa_attn_fwd_ws needs for these sizes and mode (0 for modes 2 and 3, and
+ * for the FP8 modes with D != 128). */
 size_t pasa_attn_fwd_workspace_bytes(int B, int Hkv, int Sk, int D, int mode);
 
 /*
@@ -163,6 +172,37 @@ int pasa_attn_fwd_shifted(const void* q, const void* k_shifted, const void* mean
  *   means      fp16 [B, H, ceil(Sk / pasa_block_rows(D)), D]
  */
 int pasa_kshift(const void* k, void* k_shifted, void* means, int B, int H, int Sk, int D, void* stream);
+
+/*
+ * Key preparation of the FP8 score modes (D = 128): per key block j of 128 rows, with
+ * a = max |x| over the block (all channels) of x = K' (mode 5, PASA_MODE_SHIFT_FP8: the
+ * shifted keys exactly as pasa_kshift rounds them to fp16) or x = K (mode 6,
+ * PASA_MODE_NAIVE_FP8), it writes
+ *     kscale[b, h, j]      = fp32(a / 448)        (1 when a = 0)
+ *     k8[b, h, r, d]       = e4m3 code of fp32(x[r, d] * fp32(448 / a)), round to nearest
+ *                            even, saturating at 448 (one byte, the OCP e4m3 encoding)
+ *     means[b, h, j, d]    = the pseudo-average m_j[d] as in pasa_kshift (mode 5 only; may
+ *                            be NULL in mode 6)
+ * 448 is the largest finite e4m3 value: the Abstract's overflow concern at 8 bits, where
+ * a sequence-dimension bias of K spends the 3-bit mantissa on the bias instead of the part
+ * of K that varies. Layouts: k fp16 [B, H, Sk, D]; k8 bytes [B, H, Sk, D]; kscale fp32
+ * [B, H, ceil(Sk / 128)]; means fp16 [B, H, ceil(Sk / 128), D]; all 16-byte aligned. The
+ * results can be kept as an FP8 key cache for pasa_attn_fwd_fp8. Returns
+ * PASA_ERR_UNSUPPORTED for other modes or D != 128.
+ */
+int pasa_kprep_fp8(const void* k, void* k8, void* means, float* kscale, int B, int H, int Sk, int D, int mode,
+                   void* stream);
+
+/*
+ * The attention kernel of the FP8 modes alone, on keys from pasa_kprep_fp8 (same mode).
+ * Q is quantised inside the kernel, per query row r: sq = fp32(a / 448) with a = max |q_r|,
+ * codes e4m3(fp32(q * fp32(448 / a))); the score GEMM multiplies e4m3 codes and accumulates
+ * in fp32, and the scores are sq * kscale_j * (codes product) (+ q . m_j in mode 5). Other
+ * arguments and errors as pasa_attn_fwd_shifted; means may be NULL in mode 6.
+ */
+int pasa_attn_fwd_fp8(const void* q, const void* k8, const void* means, const float* kscale, const void* v, void* o,
+                      float* lse, int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale, int mode,
+                      void* stream);
 
 /*
  * Synchronise `stream` and read the device error word. Returns PASA_OK, PASA_ERR_TIMEOUT

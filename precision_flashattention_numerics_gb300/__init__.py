@@ -17,7 +17,7 @@ import threading
 import torch
 
 __all__ = [
-    "MODE_SHIFT_F16ACC", "MODE_SHIFT_F32ACC", "MODE_NAIVE_F16ACC", "MODE_NOSHIFT_F32ACC", "MODE_SHIFT_F16ALL",
+    "MODE_SHIFT_F16ACC", "MODE_SHIFT_F32ACC", "MODE_NAIVE_F16ACC", "MODE_NOSHIFT_F32ACC", "MODE_SHIFT_F16ALL", "MODE_SHIFT_FP8", "MODE_NAIVE_FP8", "kprep_fp8", "attn_fwd_fp8",
     "PasaError", "attn_fwd", "attn_fwd_alloc", "attn_fwd_shifted", "attn_fwd_stats", "kshift", "workspace_bytes", "check_device_error", "block_rows",
     "library", "library_path",
 ]
@@ -27,6 +27,8 @@ MODE_SHIFT_F32ACC = 1
 MODE_NAIVE_F16ACC = 2
 MODE_NOSHIFT_F32ACC = 3
 MODE_SHIFT_F16ALL = 4   # mode 0 with an fp16 PV accumulator and an fp16 running row sum
+MODE_SHIFT_FP8 = 5      # e4m3 Q and shifted keys, fp32 score accumulation (D = 128)
+MODE_NAIVE_FP8 = 6      # e4m3 Q and raw keys, no shift (D = 128)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_HERE, "libpasa.so")
@@ -44,6 +46,8 @@ SIGNATURES = {
     "pasa_attn_fwd_stats": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P], _I),
     "pasa_attn_fwd_shifted": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P], _I),
     "pasa_kshift": ([_P, _P, _P, _I, _I, _I, _I, _P], _I),
+    "pasa_kprep_fp8": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _P], _I),
+    "pasa_attn_fwd_fp8": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P], _I),
     "pasa_check_device_error": ([_P, ctypes.POINTER(ctypes.c_ulonglong)], _I),
     "pasa_strerror": ([_I], ctypes.c_char_p),
     "pasa_last_cuda_error": ([], _I),
@@ -216,6 +220,40 @@ def kshift(k, out=None, means=None):
     if rc != 0:
         raise PasaError(rc, "pasa_kshift")
     return ks, means
+
+
+def kprep_fp8(k, mode: int = MODE_SHIFT_FP8):
+    """FP8 key preparation (D = 128): returns (k8 [B,H,Sk,D] uint8 e4m3 codes, means
+    [B,H,nb,D] fp16 or None in mode 6, kscale [B,H,nb] fp32)."""
+    lib = library()
+    _check(k, "k")
+    B, H, Sk, D = k.shape
+    nb = -(-Sk // 128)
+    k8 = torch.empty((B, H, Sk, D), device=k.device, dtype=torch.uint8)
+    means = torch.empty((B, H, nb, D), device=k.device, dtype=torch.float16) if mode == MODE_SHIFT_FP8 else None
+    kscale = torch.empty((B, H, nb), device=k.device, dtype=torch.float32)
+    rc = lib.pasa_kprep_fp8(_ptr(k), _ptr(k8), _ptr(means) if means is not None else None, _ptr(kscale), B, H, Sk,
+                            D, int(mode), _stream())
+    if rc != 0:
+        raise PasaError(rc, "pasa_kprep_fp8")
+    return k8, means, kscale
+
+
+def attn_fwd_fp8(q, k8, means, kscale, v, causal: bool = False, scale: float | None = None,
+                 mode: int = MODE_SHIFT_FP8, out=None, lse=None):
+    """The FP8 attention kernel alone on keys from :func:`kprep_fp8`: returns (o, lse)."""
+    lib = library()
+    _check(q, "q"), _check(v, "v")
+    B, Hq, Sq, D = q.shape
+    _, Hkv, Sk, _ = v.shape
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, Hq, Sq), device=q.device, dtype=torch.float32) if lse is None else lse
+    rc = lib.pasa_attn_fwd_fp8(_ptr(q), _ptr(k8), _ptr(means) if means is not None else None, _ptr(kscale), _ptr(v),
+                               _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Sk, D, int(bool(causal)),
+                               float(scale) if scale is not None else 0.0, int(mode), _stream())
+    if rc != 0:
+        raise PasaError(rc, "pasa_attn_fwd_fp8")
+    return out, lse
 
 
 def check_device_error():

@@ -71,6 +71,7 @@ struct AttnParams {
   float* stats;          // STATS kernels: [B, Hq, Sq, 2] fp32 score magnitudes per row
   unsigned* bstats;      // STATS kernels, or nullptr: [B, Hq, nbt, 2] per key block, fp32 bits
   int nbt;               // key blocks per head, ceil(Sk / BN)
+  const float* kscale;   // FP8 kernels: [B, Hkv, nbt] fp32 e4m3 scale of each key block
 };
 
 // TMEM column map (see the header comment).
@@ -86,20 +87,26 @@ struct TmemMap {
   static_assert(D == 64 || D == 128, "head dim");
 };
 
-template <int D, int BN, int KST, int VST>
+template <int D, int BN, int KST, int VST, bool FP8 = false>
 struct AttnSmem {
-  static constexpr int kChunks = D / 64;                 // 128-byte swizzle atoms along D
+  static constexpr int kChunks = D / 64;                 // 128-byte swizzle atoms along D (fp16)
+  static constexpr int kKB = FP8 ? 1 : 2;                // bytes per key element
+  static constexpr int kKChunks = D * kKB / 128;         // 128-byte swizzle atoms of a key row
   static constexpr int kQTile = kTileRows * D * 2;
-  static constexpr int kKTile = BN * D * 2;
+  static constexpr int kKTile = BN * D * kKB;
+  static constexpr int kVTile = BN * D * 2;              // V stays fp16 in every mode
   static constexpr int kMTile = kChunkBlocks * D * 2;
   static constexpr int kQChunk = kTileRows * 128;
-  static constexpr int kKChunk = BN * 128;
+  static constexpr int kKChunk = BN * 128;                 // bytes of one 128-byte-wide atom column
+  static constexpr int kVChunk = BN * 128;
   static constexpr int kMChunk = kChunkBlocks * 128;
   alignas(1024) uint8_t q[kQTile];   // also the O staging buffer
+  alignas(1024) uint8_t q8[FP8 ? kTileRows * D : 16];  // FP8: e4m3 codes of Q (one 128-byte atom per row)
   alignas(1024) uint8_t k[KST][kKTile];
-  alignas(1024) uint8_t v[VST][kKTile];
+  alignas(1024) uint8_t v[VST][kVTile];
   alignas(1024) uint8_t m[2][kMTile];
   uint64_t q_full;
+  uint64_t q8_full;     // FP8: the softmax warps have written the e4m3 Q tile (4 warps)
   uint64_t k_full[KST], k_empty[KST];
   uint64_t v_full[VST], v_empty[VST];
   uint64_t m_full[2], m_empty[2];
@@ -162,13 +169,15 @@ __device__ __forceinline__ void tmem_ld_scores_f16(uint32_t taddr, uint32_t* hp)
 }
 
 template <int D, int BN, bool F16ACC, bool SHIFT, bool CAUSAL, int KST, int VST, bool STATS = false,
-          bool F16PV = false>
+          bool F16PV = false, bool FP8 = false>
 __global__ void __launch_bounds__(kAttnThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                 const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapO,
                 const __grid_constant__ CUtensorMap mapM, const AttnParams p) {
   static_assert(!F16PV || F16ACC, "fp16 PV accumulation is a variant of the fp16-score mode");
-  using Smem = AttnSmem<D, BN, KST, VST>;
+  static_assert(!FP8 || (D == 128 && !F16ACC && !STATS && !F16PV), "FP8 scores: D = 128, fp32 accumulation");
+  using Smem = AttnSmem<D, BN, KST, VST, FP8>;
+  static_assert(sizeof(Smem) + 1024 <= 227 * 1024, "shared memory per CTA");
   using TM = TmemMap<D, BN>;
   extern __shared__ uint8_t smem_raw[];
   Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -196,6 +205,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
 
   if (tid == 0) {
     mbar_init(&s.q_full, 1);
+    mbar_init(&s.q8_full, 4);
     for (int i = 0; i < KST; ++i) { mbar_init(&s.k_full[i], 1); mbar_init(&s.k_empty[i], 1); }
     for (int i = 0; i < VST; ++i) { mbar_init(&s.v_full[i], 1); mbar_init(&s.v_empty[i], 1); }
     for (int i = 0; i < 2; ++i) {
@@ -252,18 +262,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         if (!mbar_wait(&s.k_empty[ks], ((j / KST) & 1) ^ 1, abort_flag, 0x102)) return false;
         mbar_arrive_expect_tx(&s.k_full[ks], Smem::kKTile);
 #pragma unroll
-        for (int c = 0; c < Smem::kChunks; ++c)
-          tma_load_3d(s.k[ks] + c * Smem::kKChunk, &mapK, &s.k_full[ks], c * 64, j * BN, kz);
+        for (int c = 0; c < Smem::kKChunks; ++c)
+          tma_load_3d(s.k[ks] + c * Smem::kKChunk, &mapK, &s.k_full[ks], c * (128 / Smem::kKB), j * BN, kz);
         k_issued = j + 1;
         return true;
       };
       auto load_v = [&](int j) -> bool {
         const int vs = j % VST;
         if (!mbar_wait(&s.v_empty[vs], ((j / VST) & 1) ^ 1, abort_flag, 0x103)) return false;
-        mbar_arrive_expect_tx(&s.v_full[vs], Smem::kKTile);
+        mbar_arrive_expect_tx(&s.v_full[vs], Smem::kVTile);
 #pragma unroll
         for (int c = 0; c < Smem::kChunks; ++c)
-          tma_load_3d(s.v[vs] + c * Smem::kKChunk, &mapV, &s.v_full[vs], c * 64, j * BN, kz);
+          tma_load_3d(s.v[vs] + c * Smem::kVChunk, &mapV, &s.v_full[vs], c * 64, j * BN, kz);
         v_issued = j + 1;
         return true;
       };
@@ -305,7 +315,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
       uint32_t qd[D / 16];
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) qd[kk] = q_lo + (((kk / 4) * Smem::kQChunk + (kk % 4) * 32) >> 4);
-      bool ok = mbar_wait(&s.q_full, 0, abort_flag, 0x201);
+      // FP8: e4m3 Q (written by the softmax warps), K = 32 per MMA, 32 bytes along the row
+      constexpr uint32_t id_s8 = idesc_e4m3(kTileRows, BN);
+      const uint32_t q8_lo = sdesc_lo(smem_u32(s.q8), 16);
+      bool ok = mbar_wait(FP8 ? &s.q8_full : &s.q_full, 0, abort_flag, 0x201);
       for (int j = 0; ok && j < nblk; ++j) {
         const int ks = j % KST;
         const int ci = j / kChunkBlocks;
@@ -315,6 +328,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         const uint32_t k_lo = k_lo0 + ks * kKStride;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) kd[kk] = k_lo + (((kk / 4) * Smem::kKChunk + (kk % 4) * 32) >> 4);
+        // (FP8: the first D / 32 of these are the e4m3 K-steps of the single 128-byte atom)
         if (!mbar_wait(&s.k_full[ks], (j / KST) & 1, abort_flag, 0x202)) break;
         if (chunk_start && !mbar_wait(&s.m_full[ci & 1], (ci >> 1) & 1, abort_flag, 0x203)) break;
         if (j >= 2 && !mbar_wait(&s.s_free[sb], ((j >> 1) - 1) & 1, abort_flag, 0x206)) break;
@@ -329,8 +343,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
           }
         }
         const uint32_t tS = tmem + TM::s(sb);
+        if constexpr (FP8) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) mma_ss_w(tS, qd[kk], hi_kmaj, kd[kk], hi_kmaj, id_s, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 32; ++kk)
+            mma_ss_f8_w(tS, q8_lo + ((kk * 32) >> 4), hi_kmaj, kd[kk], hi_kmaj, id_s8, kk > 0 ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) mma_ss_w(tS, qd[kk], hi_kmaj, kd[kk], hi_kmaj, id_s, kk > 0 ? 1u : 0u);
+        }
         mma_commit(&s.s_full[sb]);
         mma_commit(&s.k_empty[ks]);
         if (chunk_start) mma_commit(&s.m_empty[ci & 1]);
@@ -348,7 +368,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     if (lane == 0) {
       constexpr uint32_t id_o = idesc_f16(kTileRows, D, !F16PV, true);
       constexpr uint32_t hi_v = sdesc_hi_sw128(1024);
-      const uint32_t v_lo0 = sdesc_lo(smem_u32(s.v[0]), Smem::kKChunk);
+      const uint32_t v_lo0 = sdesc_lo(smem_u32(s.v[0]), Smem::kVChunk);
       constexpr uint32_t kVStride = sizeof(s.v[0]) >> 4;
       const uint32_t tO = tmem + TM::o;
       const uint32_t tP = tmem + TM::p;
@@ -388,8 +408,55 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     float st_acc = 0.0f, st_rec = 0.0f;  // STATS: max |accumulated score|, max |S' + c|
     bool ok = true;
 
-    for (int j = 0; j < nblk; ++j) {
+    // FP8: quantise this thread's Q row to e4m3 with the row scale sq = a / 448 (a = max |q|,
+    // inv = 448 / a, code = e4m3_rn_satfinite(q * inv), all fp32 with one rounding each) into
+    // the e4m3 Q tile, whose rows are single 128-byte swizzle atoms. Score dequantisation:
+    // S = sq * sk_j * (Q8 . K8_j), folded into the softmax's scale per block.
+    float sq = 1.0f;
+    const float* kscale_row = FP8 ? p.kscale + static_cast<size_t>(b * p.Hkv + hk) * p.nbt : nullptr;
+    float sk_next = 1.0f;
+    if constexpr (FP8) {
+      if (nblk > 0) sk_next = __ldg(kscale_row);
+      if (!mbar_wait(&s.q_full, 0, abort_flag, 0x340)) ok = false;
+      uint4 qrow[D / 8];
+#pragma unroll
+      for (int u = 0; u < D / 8; ++u)
+        qrow[u] = *reinterpret_cast<const uint4*>(s.q + (u / 8) * Smem::kQChunk + r * 128 + (((u % 8) ^ (r & 7)) * 16));
+      uint32_t amax = 0;
+#pragma unroll
+      for (int u = 0; u < D / 8; ++u) {
+        const uint32_t w4[4] = {qrow[u].x, qrow[u].y, qrow[u].z, qrow[u].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) amax = __vmaxu2(amax, w4[e] & 0x7FFF7FFFu);  // per fp16 lane
+      }
+      amax = max(amax & 0xFFFFu, amax >> 16);
+      const float a = __half2float(__ushort_as_half(static_cast<unsigned short>(amax)));
+      const float inv = a > 0.0f ? __fdiv_rn(448.0f, a) : 1.0f;
+      sq = a > 0.0f ? __fdiv_rn(a, 448.0f) : 1.0f;
+#pragma unroll
+      for (int u = 0; u < D / 16; ++u) {   // 16 codes (16 bytes) per iteration
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const __half* h = reinterpret_cast<const __half*>(&qrow[2 * u + e / 2]) + (e % 2) * 4;
+          const uint16_t c01 = pack_e4m3x2(__fmul_rn(__half2float(h[0]), inv), __fmul_rn(__half2float(h[1]), inv));
+          const uint16_t c23 = pack_e4m3x2(__fmul_rn(__half2float(h[2]), inv), __fmul_rn(__half2float(h[3]), inv));
+          w[e] = c01 | (static_cast<uint32_t>(c23) << 16);
+        }
+        *reinterpret_cast<uint4*>(s.q8 + r * 128 + ((u ^ (r & 7)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.q8_full);
+    }
+
+    for (int j = 0; ok && j < nblk; ++j) {
       const int sb = j & 1;
+      float fsc = 1.0f;   // FP8: dequantisation factor sq * sk_j of this block's scores
+      if constexpr (FP8) {
+        fsc = sq * sk_next;
+        if (j + 1 < nblk) sk_next = __ldg(kscale_row + j + 1);
+      }
       if (!mbar_wait(&s.s_full[sb], (j >> 1) & 1, abort_flag, 0x300)) { ok = false; break; }
       tc_fence_after();
       // Load the block's scores and offset, wait once, fence the registers, and release the
@@ -472,7 +539,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
           }
         }
       }
-      const float bm = (mx == -INFINITY) ? -INFINITY : (mx + c_raw) * sl2;
+      const float bm = (mx == -INFINITY) ? -INFINITY : (FP8 ? fmaf(mx, fsc, c_raw) : mx + c_raw) * sl2;
       const float m_new = fmaxf(m_run, bm);
       // Lazy rescale decision; the O rescale itself waits for PV(j-1) further down.
       float alpha = 1.0f;
@@ -514,10 +581,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         }
       } else {
         const float bias = (m_run == -INFINITY) ? 0.0f : c_raw * sl2 - m_run;
+        const float mul = FP8 ? fsc * sl2 : sl2;
 #pragma unroll
         for (int c = 0; c < kPairs; ++c) {
           float x0, x1;
-          ffma2(x0, x1, sv[2 * c], sv[2 * c + 1], sl2, sl2, bias, bias);
+          ffma2(x0, x1, sv[2 * c], sv[2 * c + 1], mul, mul, bias, bias);
           const float p0 = ex2_approx(x0);
           const float p1 = ex2_approx(x1);
           const int a = (c & 3) * 2;

@@ -16,6 +16,11 @@
 //
 // m lies on the grid of the block maximum, so K - m is exact in fp16 for most elements.
 //
+// FP8 score modes: the same kernel can instead write e4m3 codes of K' (or of the raw keys,
+// without the shift) with one scale per block: a = max |K'| over the block (all channels),
+// inv = fp32(448 / a), code = e4m3_rn_satfinite(fp32(K' * inv)), scale = fp32(a / 448)
+// (a = 0: inv = scale = 1). 448 is the largest finite e4m3 value.
+//
 // Kernel shape: one CTA of 256 threads per (batch*kv-head, key block). Each thread owns one
 // 16-byte unit (8 channels) of up to ceil(block rows / row groups) rows and keeps them in
 // registers; the per-channel max and integer sums are reduced with warp shuffles and a
@@ -33,6 +38,20 @@ namespace pasa {
 __host__ __device__ constexpr int block_rows_for(int D) { return D == 128 || D == 64 ? 128 : 0; }
 constexpr int kShiftThreads = 256;
 
+// Output of kshift_kernel.
+enum KshiftOut : int {
+  kShiftF16 = 0,    // K' in fp16 (+ means)
+  kShiftFp8 = 1,    // e4m3 codes of K' with one scale per block (+ means)
+  kRawFp8 = 2,      // e4m3 codes of the raw keys with one scale per block (no shift)
+};
+
+// Two fp32 values -> two e4m3 codes, lo in the low byte (round to nearest even, saturating).
+__device__ __forceinline__ uint16_t pack_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 // round-half-even(s / n) for integers, n > 0.
 __device__ __forceinline__ int rne_div(int s, int n) {
   const int a = s < 0 ? -s : s;
@@ -42,10 +61,10 @@ __device__ __forceinline__ int rne_div(int s, int n) {
   return s < 0 ? -q : q;
 }
 
-template <int D, int BN>
+template <int D, int BN, int OUT = kShiftF16>
 __global__ void __launch_bounds__(kShiftThreads)
-kshift_kernel(const __half* __restrict__ k, __half* __restrict__ kshift, __half* __restrict__ means, int Sk,
-              int nb) {
+kshift_kernel(const __half* __restrict__ k, void* __restrict__ kshift, __half* __restrict__ means,
+              float* __restrict__ kscale, int Sk, int nb) {
   constexpr int U = D / 8;                       // 16-byte units per row
   constexpr int R = kShiftThreads / U;           // row groups
   constexpr int RPT = (BN + R - 1) / R;          // rows per thread (upper bound)
@@ -56,6 +75,7 @@ kshift_kernel(const __half* __restrict__ k, __half* __restrict__ kshift, __half*
   __shared__ uint32_t sh_max[NW][U][4];
   __shared__ uint32_t sh_nf[NW][U][4];
   __shared__ int sh_sum[NW][U][8];
+  __shared__ uint32_t sh_amax[NW];
 
   const int j = blockIdx.x;
   const int bh = blockIdx.y;
@@ -67,7 +87,7 @@ kshift_kernel(const __half* __restrict__ k, __half* __restrict__ kshift, __half*
   const int n = min(BN, Sk - row0);
 
   const uint4* src = reinterpret_cast<const uint4*>(k + (static_cast<size_t>(bh) * Sk + row0) * D) + u;
-  uint4* dst = reinterpret_cast<uint4*>(kshift + (static_cast<size_t>(bh) * Sk + row0) * D) + u;
+  uint4* dst = reinterpret_cast<uint4*>(static_cast<__half*>(kshift) + (static_cast<size_t>(bh) * Sk + row0) * D) + u;
 
   uint4 x[RPT];
 #pragma unroll
@@ -162,26 +182,65 @@ kshift_kernel(const __half* __restrict__ k, __half* __restrict__ kshift, __half*
 #pragma unroll
     for (int w = 0; w < NW; ++w) s += sh_sum[w][u][h];
     const int mu = rne_div(s, n);
-    mf[h] = guard[h] ? 0.0f : static_cast<float>(mu) * g[h];  // exact, and exactly an fp16 value
+    mf[h] = (guard[h] || OUT == kRawFp8) ? 0.0f : static_cast<float>(mu) * g[h];  // exact, an fp16 value
     mh[h] = __float2half_rn(mf[h]);
   }
-  if (rg == 0) {
+  if (OUT != kRawFp8 && rg == 0) {
     uint4 mv;
     __half* mp = reinterpret_cast<__half*>(&mv);
 #pragma unroll
     for (int h = 0; h < 8; ++h) mp[h] = mh[h];
     reinterpret_cast<uint4*>(means + (static_cast<size_t>(bh) * nb + j) * D)[u] = mv;
   }
+  if constexpr (OUT == kShiftF16) {
 #pragma unroll
-  for (int i = 0; i < RPT; ++i) {
-    const int r = rg + i * R;
-    if (r < n) {
-      uint4 o;
-      const __half* hv = reinterpret_cast<const __half*>(&x[i]);
-      __half* op = reinterpret_cast<__half*>(&o);
+    for (int i = 0; i < RPT; ++i) {
+      const int r = rg + i * R;
+      if (r < n) {
+        uint4 o;
+        const __half* hv = reinterpret_cast<const __half*>(&x[i]);
+        __half* op = reinterpret_cast<__half*>(&o);
 #pragma unroll
-      for (int h = 0; h < 8; ++h) op[h] = __float2half_rn(__half2float(hv[h]) - mf[h]);
-      dst[static_cast<size_t>(r) * U] = o;
+        for (int h = 0; h < 8; ++h) op[h] = __float2half_rn(__half2float(hv[h]) - mf[h]);
+        dst[static_cast<size_t>(r) * U] = o;
+      }
+    }
+  } else {
+    // K' (rounded to fp16, as the fp16 modes use it) in place, and its block maximum
+    uint32_t amax = 0;
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+      const int r = rg + i * R;
+      __half* hv = reinterpret_cast<__half*>(&x[i]);
+#pragma unroll
+      for (int h = 0; h < 8; ++h) {
+        hv[h] = r < n ? __float2half_rn(__half2float(hv[h]) - mf[h]) : __ushort_as_half(0);
+        amax = max(amax, static_cast<uint32_t>(__half_as_ushort(hv[h]) & 0x7FFFu));
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if ((tid % 32) == 0) sh_amax[warp] = amax;
+    __syncthreads();
+    amax = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) amax = max(amax, sh_amax[w]);
+    const float a = __half2float(__ushort_as_half(static_cast<unsigned short>(amax)));
+    const float inv = a > 0.0f ? __fdiv_rn(448.0f, a) : 1.0f;
+    if (tid == 0) kscale[static_cast<size_t>(bh) * nb + j] = a > 0.0f ? __fdiv_rn(a, 448.0f) : 1.0f;
+    uint2* dst8 = reinterpret_cast<uint2*>(static_cast<uint8_t*>(kshift) + (static_cast<size_t>(bh) * Sk + row0) * D) + u;
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+      const int r = rg + i * R;
+      if (r < n) {
+        const __half* hv = reinterpret_cast<const __half*>(&x[i]);
+        uint16_t c[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+          c[h] = pack_e4m3x2(__fmul_rn(__half2float(hv[2 * h]), inv), __fmul_rn(__half2float(hv[2 * h + 1]), inv));
+        dst8[static_cast<size_t>(r) * U] = make_uint2(c[0] | (static_cast<uint32_t>(c[1]) << 16),
+                                                      c[2] | (static_cast<uint32_t>(c[3]) << 16));
+      }
     }
   }
 }

@@ -42,14 +42,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // 3-D fp16 view [planes, rows, D] of a contiguous tensor, 128-byte swizzled boxes of
 // 64 x box_rows x 1 elements.
-int make_map(CUtensorMap* m, const void* base, int D, long long rows, long long planes, int box_rows) {
+// 3-D map (D, rows, planes) with 128-byte rows per box chunk: 64 fp16 or 128 one-byte elements.
+int make_map(CUtensorMap* m, const void* base, int D, long long rows, long long planes, int box_rows,
+             int elem_bytes = 2) {
   auto enc = encode_fn();
   if (!enc) return cuda_fail(cudaErrorNotSupported);
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(planes)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(rows) * D * 2};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * elem_bytes, static_cast<cuuint64_t>(rows) * D * elem_bytes};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem_bytes), static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t es[3] = {1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+  CUresult r = enc(m, elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                   const_cast<void*>(base), dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
@@ -63,43 +66,62 @@ int check_device() {
   return pasa_device_supported(dev) ? PASA_OK : PASA_ERR_UNSUPPORTED;
 }
 
+bool fp8_mode(int mode) { return mode == PASA_MODE_SHIFT_FP8 || mode == PASA_MODE_NAIVE_FP8; }
+
+// Modes that shift the keys (and so need the block means).
+bool shift_mode(int mode) {
+  return mode == PASA_MODE_SHIFT_F16ACC || mode == PASA_MODE_SHIFT_F32ACC || mode == PASA_MODE_SHIFT_F16ALL ||
+         mode == PASA_MODE_SHIFT_FP8;
+}
+
+// Workspace: the keys the attention kernel reads (fp16 K', or e4m3 codes in the FP8 modes),
+// the block means [B,Hkv,nb,D] fp16 and, in the FP8 modes, the block scales [B,Hkv,nb] fp32;
+// each part 256-byte aligned.
 struct WorkspaceLayout {
-  size_t kshift_off, means_off, total;
+  size_t kshift_off, means_off, kscale_off, total;
 };
 
-WorkspaceLayout workspace_layout(int B, int Hkv, int Sk, int D) {
+WorkspaceLayout workspace_layout(int B, int Hkv, int Sk, int D, int mode) {
   const int bn = pasa::block_rows_for(D);
   const size_t nb = (static_cast<size_t>(Sk) + bn - 1) / bn;
+  const size_t eb = fp8_mode(mode) ? 1 : 2;
   WorkspaceLayout w;
   w.kshift_off = 0;
-  w.means_off = align_up(static_cast<size_t>(B) * Hkv * Sk * D * 2, 256);
-  w.total = align_up(w.means_off + static_cast<size_t>(B) * Hkv * nb * D * 2, 256);
+  w.means_off = align_up(static_cast<size_t>(B) * Hkv * Sk * D * eb, 256);
+  w.kscale_off = align_up(w.means_off + static_cast<size_t>(B) * Hkv * nb * D * 2, 256);
+  w.total = fp8_mode(mode) ? align_up(w.kscale_off + static_cast<size_t>(B) * Hkv * nb * 4, 256) : w.kscale_off;
   return w;
 }
 
-template <int D>
-int launch_kshift(const void* k, void* ks, void* means, int B, int H, int Sk, cudaStream_t st) {
+template <int D, int OUT>
+int launch_kshift(const void* k, void* ks, void* means, float* kscale, int B, int H, int Sk, cudaStream_t st) {
   constexpr int BN = pasa::block_rows_for(D);
   const int nb = (Sk + BN - 1) / BN;
   dim3 grid(nb, B * H);
-  pasa::kshift_kernel<D, BN><<<grid, pasa::kShiftThreads, 0, st>>>(
-      static_cast<const __half*>(k), static_cast<__half*>(ks), static_cast<__half*>(means), Sk, nb);
+  pasa::kshift_kernel<D, BN, OUT><<<grid, pasa::kShiftThreads, 0, st>>>(
+      static_cast<const __half*>(k), ks, static_cast<__half*>(means), kscale, Sk, nb);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? PASA_OK : cuda_fail(e);
 }
 
-int kshift_dispatch(const void* k, void* ks, void* means, int B, int H, int Sk, int D, cudaStream_t st) {
-  return D == 64 ? launch_kshift<64>(k, ks, means, B, H, Sk, st) : launch_kshift<128>(k, ks, means, B, H, Sk, st);
+// fp16 K' for the fp16 modes; e4m3 codes (of K', or of K in the naive FP8 mode) otherwise.
+int kshift_dispatch(const void* k, void* ks, void* means, float* kscale, int B, int H, int Sk, int D, int mode,
+                    cudaStream_t st) {
+  if (mode == PASA_MODE_SHIFT_FP8) return launch_kshift<128, pasa::kShiftFp8>(k, ks, means, kscale, B, H, Sk, st);
+  if (mode == PASA_MODE_NAIVE_FP8) return launch_kshift<128, pasa::kRawFp8>(k, ks, means, kscale, B, H, Sk, st);
+  return D == 64 ? launch_kshift<64, pasa::kShiftF16>(k, ks, means, nullptr, B, H, Sk, st)
+                 : launch_kshift<128, pasa::kShiftF16>(k, ks, means, nullptr, B, H, Sk, st);
 }
 
-template <int D, bool F16ACC, bool SHIFT, bool CAUSAL, bool STATS, bool F16PV = false>
+template <int D, bool F16ACC, bool SHIFT, bool CAUSAL, bool STATS, bool F16PV = false, bool FP8 = false>
 int launch_attn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mo,
                 const CUtensorMap& mm, const pasa::AttnParams& p, cudaStream_t st) {
   constexpr int BN = pasa::block_rows_for(D);
-  constexpr int KST = D == 128 ? 3 : 4;  // K ring slots (D = 128: 200 KB of shared memory)
-  constexpr int VST = D == 128 ? 2 : 4;
-  using Smem = pasa::AttnSmem<D, BN, KST, VST>;
-  auto kern = pasa::attn_fwd_kernel<D, BN, F16ACC, SHIFT, CAUSAL, KST, VST, STATS, F16PV>;
+  // ring slots: D = 128 fp16 keys: 3 K + 2 V (201 KB of shared memory); e4m3 keys: 4 + 3
+  constexpr int KST = D == 128 ? (FP8 ? 4 : 3) : 4;
+  constexpr int VST = D == 128 ? (FP8 ? 3 : 2) : 4;
+  using Smem = pasa::AttnSmem<D, BN, KST, VST, FP8>;
+  auto kern = pasa::attn_fwd_kernel<D, BN, F16ACC, SHIFT, CAUSAL, KST, VST, STATS, F16PV, FP8>;
   const int smem = static_cast<int>(sizeof(Smem)) + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -124,15 +146,20 @@ int attn_dispatch(int mode, int causal, const CUtensorMap& mq, const CUtensorMap
     case PASA_MODE_SHIFT_F16ALL:
       return causal ? launch_attn<D, true, true, true, STATS, true>(mq, mk, mv, mo, mm, p, st)
                     : launch_attn<D, true, true, false, STATS, true>(mq, mk, mv, mo, mm, p, st);
+    case PASA_MODE_SHIFT_FP8:
+    case PASA_MODE_NAIVE_FP8:
+      if constexpr (D == 128 && !STATS) {
+        if (mode == PASA_MODE_SHIFT_FP8)
+          return causal ? launch_attn<D, false, true, true, false, false, true>(mq, mk, mv, mo, mm, p, st)
+                        : launch_attn<D, false, true, false, false, false, true>(mq, mk, mv, mo, mm, p, st);
+        return causal ? launch_attn<D, false, false, true, false, false, true>(mq, mk, mv, mo, mm, p, st)
+                      : launch_attn<D, false, false, false, false, false, true>(mq, mk, mv, mo, mm, p, st);
+      }
+      return PASA_ERR_UNSUPPORTED;
     default:
       return PASA_ERR_UNSUPPORTED;
   }
 #undef PASA_CASE
-}
-
-// Modes that shift the keys (and so need the pseudo-average workspace).
-bool shift_mode(int mode) {
-  return mode == PASA_MODE_SHIFT_F16ACC || mode == PASA_MODE_SHIFT_F32ACC || mode == PASA_MODE_SHIFT_F16ALL;
 }
 
 int validate(const void* q, const void* k, const void* v, const void* o, const float* lse, int B, int Hq, int Hkv,
@@ -140,7 +167,8 @@ int validate(const void* q, const void* k, const void* v, const void* o, const f
   if (!q || !k || !v || !o) return PASA_ERR_NULLPTR;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Sk <= 0 || Hq % Hkv != 0) return PASA_ERR_SHAPE;
   if (D != 64 && D != 128) return PASA_ERR_UNSUPPORTED;
-  if (mode < PASA_MODE_SHIFT_F16ACC || mode > PASA_MODE_SHIFT_F16ALL) return PASA_ERR_UNSUPPORTED;
+  if (mode < PASA_MODE_SHIFT_F16ACC || mode > PASA_MODE_NAIVE_FP8) return PASA_ERR_UNSUPPORTED;
+  if (fp8_mode(mode) && D != 128) return PASA_ERR_UNSUPPORTED;
   // grid size, TMA plane counts and flat LSE indices fit in 32-bit signed integers
   const long long n_qblk = (static_cast<long long>(Sq) + pasa::kTileRows - 1) / pasa::kTileRows;
   if (n_qblk * Hq * B > 0x7fffffffLL) return PASA_ERR_SHAPE;
@@ -182,8 +210,9 @@ const char* pasa_strerror(int status) {
 
 size_t pasa_attn_fwd_workspace_bytes(int B, int Hkv, int Sk, int D, int mode) {
   if (B <= 0 || Hkv <= 0 || Sk <= 0 || pasa::block_rows_for(D) == 0) return 0;
-  if (!shift_mode(mode)) return 0;
-  return workspace_layout(B, Hkv, Sk, D).total;
+  if (!shift_mode(mode) && !fp8_mode(mode)) return 0;
+  if (fp8_mode(mode) && D != 128) return 0;
+  return workspace_layout(B, Hkv, Sk, D, mode).total;
 }
 
 int pasa_kshift(const void* k, void* k_shifted, void* means, int B, int H, int Sk, int D, void* stream) {
@@ -194,13 +223,26 @@ int pasa_kshift(const void* k, void* k_shifted, void* means, int B, int H, int S
   if (!aligned16(k) || !aligned16(k_shifted) || !aligned16(means)) return PASA_ERR_ALIGN;
   int rc = check_device();
   if (rc != PASA_OK) return rc;
-  return kshift_dispatch(k, k_shifted, means, B, H, Sk, D, static_cast<cudaStream_t>(stream));
+  return kshift_dispatch(k, k_shifted, means, nullptr, B, H, Sk, D, PASA_MODE_SHIFT_F16ACC,
+                         static_cast<cudaStream_t>(stream));
+}
+
+int pasa_kprep_fp8(const void* k, void* k8, void* means, float* kscale, int B, int H, int Sk, int D, int mode,
+                   void* stream) {
+  if (!k || !k8 || !kscale || (mode == PASA_MODE_SHIFT_FP8 && !means)) return PASA_ERR_NULLPTR;
+  if (B <= 0 || H <= 0 || Sk <= 0) return PASA_ERR_SHAPE;
+  if (D != 128 || !fp8_mode(mode)) return PASA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * H > 65535) return PASA_ERR_SHAPE;  // grid.y
+  if (!aligned16(k) || !aligned16(k8) || (means && !aligned16(means)) || !aligned16(kscale)) return PASA_ERR_ALIGN;
+  int rc = check_device();
+  if (rc != PASA_OK) return rc;
+  return kshift_dispatch(k, k8, means, kscale, B, H, Sk, D, mode, static_cast<cudaStream_t>(stream));
 }
 
 // Launch the attention kernel on (possibly shifted) keys `kk` and block means `mm`.
 static int attn_launch(const void* q, const void* kk, const void* mm, const void* v, void* o, float* lse, int B,
                        int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale, int mode, cudaStream_t st,
-                       float* stats = nullptr, float* block_stats = nullptr) {
+                       float* stats = nullptr, float* block_stats = nullptr, const float* kscale = nullptr) {
   const bool shift = shift_mode(mode);
   if (!(scale > 0.0f) || !std::isfinite(scale)) scale = 1.0f / std::sqrt(static_cast<float>(D));
   const int bn = pasa::block_rows_for(D);
@@ -208,7 +250,8 @@ static int attn_launch(const void* q, const void* kk, const void* mm, const void
   int rc;
   CUtensorMap mq, mk, mv, mo, mmeans;
   if ((rc = make_map(&mq, q, D, Sq, static_cast<long long>(B) * Hq, pasa::kTileRows)) != PASA_OK) return rc;
-  if ((rc = make_map(&mk, kk, D, Sk, static_cast<long long>(B) * Hkv, bn)) != PASA_OK) return rc;
+  if ((rc = make_map(&mk, kk, D, Sk, static_cast<long long>(B) * Hkv, bn, fp8_mode(mode) ? 1 : 2)) != PASA_OK)
+    return rc;
   if ((rc = make_map(&mv, v, D, Sk, static_cast<long long>(B) * Hkv, bn)) != PASA_OK) return rc;
   if ((rc = make_map(&mo, o, D, Sq, static_cast<long long>(B) * Hq, pasa::kTileRows)) != PASA_OK) return rc;
   if (shift) {
@@ -230,6 +273,7 @@ static int attn_launch(const void* q, const void* kk, const void* mm, const void
   p.stats = stats;
   p.bstats = reinterpret_cast<unsigned*>(block_stats);
   p.nbt = nb;
+  p.kscale = kscale;
   if (block_stats) {
     const cudaError_t e = cudaMemsetAsync(block_stats, 0, static_cast<size_t>(B) * Hq * nb * 2 * sizeof(float), st);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -246,6 +290,7 @@ int pasa_attn_fwd_shifted(const void* q, const void* k_shifted, const void* mean
                           int mode, void* stream) {
   int rc = validate(q, k_shifted, v, o, lse, B, Hq, Hkv, Sq, Sk, D, mode);
   if (rc != PASA_OK) return rc;
+  if (fp8_mode(mode)) return PASA_ERR_UNSUPPORTED;  // the FP8 modes read e4m3 keys, not fp16 K'
   const bool shift = shift_mode(mode);
   if (shift && !means) return PASA_ERR_NULLPTR;
   if (shift && !aligned16(means)) return PASA_ERR_ALIGN;
@@ -255,14 +300,28 @@ int pasa_attn_fwd_shifted(const void* q, const void* k_shifted, const void* mean
                      static_cast<cudaStream_t>(stream));
 }
 
+int pasa_attn_fwd_fp8(const void* q, const void* k8, const void* means, const float* kscale, const void* v, void* o,
+                      float* lse, int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale, int mode,
+                      void* stream) {
+  int rc = validate(q, k8, v, o, lse, B, Hq, Hkv, Sq, Sk, D, mode);
+  if (rc != PASA_OK) return rc;
+  if (!fp8_mode(mode)) return PASA_ERR_UNSUPPORTED;
+  if (!kscale || (mode == PASA_MODE_SHIFT_FP8 && !means)) return PASA_ERR_NULLPTR;
+  if (!aligned16(kscale) || (means && !aligned16(means))) return PASA_ERR_ALIGN;
+  rc = check_device();
+  if (rc != PASA_OK) return rc;
+  return attn_launch(q, k8, mode == PASA_MODE_SHIFT_FP8 ? means : k8, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale,
+                     mode, static_cast<cudaStream_t>(stream), nullptr, nullptr, kscale);
+}
+
 int pasa_attn_fwd_ws(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                      int Sq, int Sk, int D, int causal, float scale, int mode, void* workspace,
                      size_t workspace_bytes, void* stream) {
   int rc = validate(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, mode);
   if (rc != PASA_OK) return rc;
-  const bool shift = shift_mode(mode);
-  const WorkspaceLayout wl = workspace_layout(B, Hkv, Sk, D);
-  if (shift) {
+  const bool prep = shift_mode(mode) || fp8_mode(mode);  // the shift kernel runs first
+  const WorkspaceLayout wl = workspace_layout(B, Hkv, Sk, D, mode);
+  if (prep) {
     if (!workspace || workspace_bytes < wl.total) return PASA_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PASA_ERR_ALIGN;
     if (static_cast<long long>(B) * Hkv > 65535) return PASA_ERR_SHAPE;  // kshift grid.y
@@ -272,16 +331,18 @@ int pasa_attn_fwd_ws(const void* q, const void* k, const void* v, void* o, float
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const void* kk = k;
   const void* mm = k;
-  if (shift) {
+  float* kscale = nullptr;
+  if (prep) {
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     void* ks = ws + wl.kshift_off;
     void* means = ws + wl.means_off;
-    rc = kshift_dispatch(k, ks, means, B, Hkv, Sk, D, st);
+    if (fp8_mode(mode)) kscale = reinterpret_cast<float*>(ws + wl.kscale_off);
+    rc = kshift_dispatch(k, ks, means, kscale, B, Hkv, Sk, D, mode, st);
     if (rc != PASA_OK) return rc;
     kk = ks;
     mm = means;
   }
-  return attn_launch(q, kk, mm, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, mode, st);
+  return attn_launch(q, kk, mm, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, mode, st, nullptr, nullptr, kscale);
 }
 
 int pasa_attn_fwd_stats(const void* q, const void* k, const void* v, void* o, float* lse, float* stats,
@@ -292,8 +353,9 @@ int pasa_attn_fwd_stats(const void* q, const void* k, const void* v, void* o, fl
   if (!stats) return PASA_ERR_NULLPTR;
   if ((reinterpret_cast<uintptr_t>(stats) & 7u) != 0) return PASA_ERR_ALIGN;
   if (block_stats && (reinterpret_cast<uintptr_t>(block_stats) & 7u) != 0) return PASA_ERR_ALIGN;
+  if (fp8_mode(mode)) return PASA_ERR_UNSUPPORTED;  // no diagnostic build of the FP8 kernels
   const bool shift = shift_mode(mode);
-  const WorkspaceLayout wl = workspace_layout(B, Hkv, Sk, D);
+  const WorkspaceLayout wl = workspace_layout(B, Hkv, Sk, D, mode);
   if (shift) {
     if (!workspace || workspace_bytes < wl.total) return PASA_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PASA_ERR_ALIGN;
@@ -306,7 +368,7 @@ int pasa_attn_fwd_stats(const void* q, const void* k, const void* v, void* o, fl
   const void* mm = k;
   if (shift) {
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    rc = kshift_dispatch(k, ws + wl.kshift_off, ws + wl.means_off, B, Hkv, Sk, D, st);
+    rc = kshift_dispatch(k, ws + wl.kshift_off, ws + wl.means_off, nullptr, B, Hkv, Sk, D, mode, st);
     if (rc != PASA_OK) return rc;
     kk = ws + wl.kshift_off;
     mm = ws + wl.means_off;

@@ -320,6 +320,26 @@ __device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint3
       : "memory");
 }
 
+// kind::f8f6f4 with both operands in shared memory (e4m3 A and B with the descriptor of
+// idesc_e4m3; K = 32 elements per instruction).
+__device__ __forceinline__ void mma_ss_f8_w(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
+                                           uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "mov.b64 da, {%1, %2};\n\t"
+      "mov.b64 db, {%3, %4};\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor for tcgen05.mma kind::f8f6f4 with e4m3 A and B (format code 0 in
+// bits 7-9 and 10-12), both K-major, fp32 D.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
+  return 1u << 4 | static_cast<uint32_t>(N >> 3) << 17 | static_cast<uint32_t>(M >> 4) << 24;
+}
+
 // Instruction descriptor for tcgen05.mma kind::f16 with fp16 A and B.
 //   bits 4-5 D format (0 = f16, 1 = f32), bits 7-9 / 10-12 A / B format (0 = f16),
 //   bit 15 / 16 A / B major (0 = K-major, 1 = MN-major), bits 17-22 N >> 3, bits 24-28 M >> 4.

@@ -68,8 +68,10 @@ def test_argument_errors(lib):
     assert call(lib, Hq=3, Hkv=2) == -2
     assert call(lib, D=96) == -3
     assert call(lib, D=256) == -3
-    assert call(lib, mode=5) == -3
+    assert call(lib, mode=7) == -3
     assert call(lib, mode=-1) == -3
+    assert call(lib, mode=5, D=64) == -3               # FP8 score modes: D = 128 only
+    assert call(lib, mode=6, D=128, ws=None) == -7     # they prepare e4m3 keys in the workspace
     assert call(lib, mode=4, ws=None) == -7          # mode 4 shifts the keys: it needs the workspace
     assert call(lib, k=FAKE_MIS) == -4
     assert call(lib, lse=FAKE_MIS) == -4
@@ -102,6 +104,12 @@ def test_workspace_bytes(lib):
             assert lib.pasa_attn_fwd_workspace_bytes(B, H, Sk, D, mode) == expect(B, H, Sk, D)
         for mode in (2, 3):
             assert lib.pasa_attn_fwd_workspace_bytes(B, H, Sk, D, mode) == 0
+        # FP8 modes (D = 128): e4m3 keys [B,H,Sk,D] bytes + means fp16 + block scales fp32
+        nb = -(-Sk // 128)
+        fp8 = (-(-(-(-(-(-(B * H * Sk * D) // 256) * 256 + B * H * nb * D * 2) // 256) * 256 + B * H * nb * 4) // 256)
+               * 256)
+        for mode in (5, 6):
+            assert lib.pasa_attn_fwd_workspace_bytes(B, H, Sk, D, mode) == (fp8 if D == 128 else 0)
 
 
 def test_no_device_here_is_reported_not_launched(lib):
@@ -110,3 +118,21 @@ def test_no_device_here_is_reported_not_launched(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert lib.pasa_device_supported(0) == 0
+
+
+def test_fp8_entry_points_check_arguments(lib):
+    P = ctypes.c_void_p
+    # pasa_kprep_fp8(k, k8, means, kscale, B, H, Sk, D, mode, stream)
+    assert lib.pasa_kprep_fp8(P(FAKE), P(FAKE), None, P(FAKE), 1, 1, 64, 128, 5, None) == -1   # mode 5 needs means
+    assert lib.pasa_kprep_fp8(P(FAKE), P(FAKE), None, None, 1, 1, 64, 128, 6, None) == -1
+    assert lib.pasa_kprep_fp8(P(FAKE), P(FAKE), P(FAKE), P(FAKE), 1, 1, 64, 64, 5, None) == -3
+    assert lib.pasa_kprep_fp8(P(FAKE), P(FAKE), P(FAKE), P(FAKE), 1, 1, 64, 128, 0, None) == -3
+    assert lib.pasa_kprep_fp8(P(FAKE_MIS), P(FAKE), P(FAKE), P(FAKE), 1, 1, 64, 128, 5, None) == -4
+    # pasa_attn_fwd_fp8(q, k8, means, kscale, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, mode, stream)
+    args = [P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), 1, 2, 1, 64, 64, 128, 0, 0.0]
+    assert lib.pasa_attn_fwd_fp8(*args, 1, None) == -3            # not an FP8 mode
+    args[3] = None
+    assert lib.pasa_attn_fwd_fp8(*args, 5, None) == -1            # no block scales
+    # the fp16-key entry points refuse the FP8 modes
+    assert lib.pasa_attn_fwd_shifted(P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), 1, 2, 1, 64, 64, 128, 0, 0.0,
+                                     5, None) == -3
