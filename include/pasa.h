@@ -205,6 +205,57 @@ int pasa_attn_fwd_fp8(const void* q, const void* k8, const void* means, const fl
                       void* stream);
 
 /*
+ * Refresh of a shifted key cache after an append ("Online Pseudo-average Shifting Attention
+ * (PASA) for Robust Low-precision LLM Inference", Abstract: long-sequence inference). The
+ * pseudo-average of a key block depends on that block's rows only, so when rows are
+ * appended to a cache of Sk keys, only the blocks from first_block on change. This call
+ * recomputes exactly pasa_kshift's output for key blocks [first_block, ceil(Sk / BN)), BN =
+ * pasa_block_rows(D), and leaves every earlier block of k_shifted and means untouched.
+ * The cache holds Sk valid keys of Sk_cap allocated rows per head (Sk_cap >= Sk; pass Sk
+ * for a dense tensor): k and k_shifted fp16 [B, H, Sk_cap, D], means fp16 [B, H,
+ * ceil(Sk_cap / BN), D]; rows and blocks past Sk are neither read nor written. Other
+ * arguments as pasa_kshift; first_block outside [0, ceil(Sk / BN)), Sk_cap < Sk or
+ * B * H > 65535 is PASA_ERR_SHAPE.
+ */
+int pasa_kshift_blocks(const void* k, void* k_shifted, void* means, int B, int H, int Sk, int Sk_cap, int D,
+                       int first_block, void* stream);
+
+/*
+ * Bytes of workspace pasa_attn_fwd_decode needs for these sizes and `splits` (0 = the
+ * automatic choice): 0 when the call runs unsplit, else splits * B * Hq * Sq * (D + 1)
+ * fp32 values (partial outputs and log-sum-exps, each part 256-byte aligned). Returns 0 for
+ * invalid sizes as well.
+ */
+size_t pasa_attn_fwd_decode_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D, int splits);
+
+/*
+ * Decode attention on a key cache (the inference use of PASA, same citation as
+ * pasa_kshift_blocks): a few new query rows per head against Sk cached keys, already
+ * shifted by pasa_kshift / pasa_kshift_blocks (modes 0, 1, 4) or raw (modes 2, 3; means may
+ * be NULL). The result equals pasa_attn_fwd_shifted's on the same arguments up to the
+ * rounding of the split merge; with one split it is the same kernel arithmetic.
+ * Two changes of work layout serve the small Sq:
+ *  - the g = Hq / Hkv query heads sharing a kv head are packed into one 128-row tile
+ *    (requires g * Sq <= 128, else PASA_ERR_UNSUPPORTED), so each key block is read once
+ *    per kv head instead of once per query head;
+ *  - the key blocks are split across `splits` CTAs per kv head (0 = automatic: at most one
+ *    CTA per SM, at least two key blocks per split). Each split writes its O / l (fp32)
+ *    and m + log2 l to the workspace; a second kernel merges them:
+ *    O = sum_s w_s O_s / sum_s w_s, w_s = 2^(lse_s - max lse), and writes o (fp16) and lse.
+ * The causal mask is bottom-right aligned per head, as in pasa_attn_fwd. q, o: fp16
+ * [B, Hq, Sq, D]; the cache holds Sk valid keys of Sk_cap allocated rows per head
+ * (Sk_cap >= Sk, else PASA_ERR_SHAPE; pass Sk for dense tensors): k_shifted, v fp16
+ * [B, Hkv, Sk_cap, D], means fp16 [B, Hkv, ceil(Sk_cap / pasa_block_rows(D)), D]; rows
+ * past Sk are not read. lse: fp32 [B, Hq, Sq] or NULL. workspace: device,
+ * 256-byte aligned, at least pasa_attn_fwd_decode_workspace_bytes(...) bytes (may be NULL
+ * when that is 0); the caller owns it and it is only used on `stream`. FP8 modes and
+ * splits < 0 are PASA_ERR_UNSUPPORTED; a short workspace is PASA_ERR_WORKSPACE.
+ */
+int pasa_attn_fwd_decode(const void* q, const void* k_shifted, const void* means, const void* v, void* o, float* lse,
+                         int B, int Hq, int Hkv, int Sq, int Sk, int Sk_cap, int D, int causal, float scale, int mode,
+                         int splits, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Synchronise `stream` and read the device error word. Returns PASA_OK, PASA_ERR_TIMEOUT
  * (a pipeline wait gave up; `info`, if not NULL, receives the CTA index << 32 | wait site)
  * or PASA_ERR_CUDA. Reading the word clears it.

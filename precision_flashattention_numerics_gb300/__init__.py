@@ -48,6 +48,9 @@ SIGNATURES = {
     "pasa_kshift": ([_P, _P, _P, _I, _I, _I, _I, _P], _I),
     "pasa_kprep_fp8": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _P], _I),
     "pasa_attn_fwd_fp8": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P], _I),
+    "pasa_kshift_blocks": ([_P, _P, _P, _I, _I, _I, _I, _I, _I, _P], _I),
+    "pasa_attn_fwd_decode_workspace_bytes": ([_I, _I, _I, _I, _I, _I, _I], _SZ),
+    "pasa_attn_fwd_decode": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P], _I),
     "pasa_check_device_error": ([_P, ctypes.POINTER(ctypes.c_ulonglong)], _I),
     "pasa_strerror": ([_I], ctypes.c_char_p),
     "pasa_last_cuda_error": ([], _I),
@@ -253,6 +256,52 @@ def attn_fwd_fp8(q, k8, means, kscale, v, causal: bool = False, scale: float | N
                                float(scale) if scale is not None else 0.0, int(mode), _stream())
     if rc != 0:
         raise PasaError(rc, "pasa_attn_fwd_fp8")
+    return out, lse
+
+
+def kshift_blocks(k, k_shifted, means, first_block: int, length: int | None = None):
+    """Recompute :func:`kshift`'s output in place for key blocks first_block.. of a cache
+    k [B,H,cap,D] holding `length` valid rows (default cap): the blocks an append touched;
+    earlier blocks are left as they are."""
+    lib = library()
+    _check(k, "k"), _check(k_shifted, "k_shifted"), _check(means, "means")
+    B, H, cap, D = k.shape
+    Sk = cap if length is None else int(length)
+    rc = lib.pasa_kshift_blocks(_ptr(k), _ptr(k_shifted), _ptr(means), B, H, Sk, cap, D, int(first_block),
+                                _stream())
+    if rc != 0:
+        raise PasaError(rc, "pasa_kshift_blocks")
+    return k_shifted, means
+
+
+def decode_workspace_bytes(B: int, Hq: int, Hkv: int, Sq: int, Sk: int, D: int, splits: int = 0) -> int:
+    return library().pasa_attn_fwd_decode_workspace_bytes(B, Hq, Hkv, Sq, Sk, D, splits)
+
+
+def attn_fwd_decode(q, k_shifted, means, v, causal: bool = False, scale: float | None = None,
+                    mode: int = MODE_SHIFT_F16ACC, splits: int = 0, out=None, lse=None, workspace=None,
+                    length: int | None = None):
+    """Decode attention on a shifted key cache (modes 0/1/4) or raw keys (2/3): packed GQA
+    rows, keys split across CTAs and merged. k_shifted / v are [B,Hkv,cap,D] caches with
+    `length` valid rows (default cap). Returns (o, lse)."""
+    lib = library()
+    _check(q, "q"), _check(k_shifted, "k_shifted"), _check(v, "v")
+    if means is not None:
+        _check(means, "means")
+    B, Hq, Sq, D = q.shape
+    _, Hkv, cap, _ = k_shifted.shape
+    Sk = cap if length is None else int(length)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, Hq, Sq), device=q.device, dtype=torch.float32) if lse is None else lse
+    nbytes = lib.pasa_attn_fwd_decode_workspace_bytes(B, Hq, Hkv, Sq, Sk, D, int(splits))
+    if nbytes and (workspace is None or workspace.numel() * workspace.element_size() < nbytes):
+        workspace = torch.empty(nbytes, device=q.device, dtype=torch.uint8)
+    rc = lib.pasa_attn_fwd_decode(_ptr(q), _ptr(k_shifted), _ptr(means) if means is not None else None, _ptr(v),
+                                  _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Sk, cap, D, int(bool(causal)),
+                                  float(scale) if scale is not None else 0.0, int(mode), int(splits),
+                                  _ptr(workspace) if nbytes else None, nbytes, _stream())
+    if rc != 0:
+        raise PasaError(rc, "pasa_attn_fwd_decode")
     return out, lse
 
 

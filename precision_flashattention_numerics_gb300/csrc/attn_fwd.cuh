@@ -72,6 +72,16 @@ struct AttnParams {
   unsigned* bstats;      // STATS kernels, or nullptr: [B, Hq, nbt, 2] per key block, fp32 bits
   int nbt;               // key blocks per head, ceil(Sk / BN)
   const float* kscale;   // FP8 kernels: [B, Hkv, nbt] fp32 e4m3 scale of each key block
+  // Decode layout. sq_mod: query rows per head for the causal mask; equal to Sq, except
+  // when the g = Hq/Hkv heads of a kv group are packed into one row range ("Hq" = Hkv,
+  // "Sq" = g * sq_mod rows, row r holding query r mod sq_mod of head r / sq_mod).
+  int sq_mod;
+  // Split keys: blockIdx.y selects key blocks [y * bps, (y + 1) * bps) (0 = no split).
+  // Then each CTA writes O / l in fp32 to part_o [split][row][D] and
+  // m + log2 l to part_lse [split][row] instead of o and lse; a combine kernel merges them.
+  int bps;
+  float* part_o;
+  float* part_lse;
 };
 
 // TMEM column map (see the header comment).
@@ -196,11 +206,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
   const int hk = hq / (p.Hq / p.Hkv);
   const int q0 = qb * kTileRows;
 
+  // Key blocks of this CTA: [jb0, jb0 + nblk). The loops below count j from 0 (offsets
+  // chunks and ring slots are local to the CTA); data addresses (key rows, block means,
+  // block scales, the causal mask) use the global block jb0 + j.
+  const int split = blockIdx.y;
+  const int jb0 = split * p.bps;
   int nblk;
   {
     const int last = min(p.Sq, q0 + kTileRows) - 1;
-    const int kv_end = CAUSAL ? min(p.Sk, last + p.Sk - p.Sq + 1) : p.Sk;
+    const int i_last = p.sq_mod == p.Sq ? last : min(p.sq_mod - 1, last);   // packed rows: an upper bound
+    const int kv_end = CAUSAL ? min(p.Sk, i_last + p.Sk - p.sq_mod + 1) : p.Sk;
     nblk = kv_end > 0 ? (kv_end + BN - 1) / BN : 0;
+    if (p.bps > 0) nblk = max(0, min(p.bps, nblk - jb0));
   }
 
   if (tid == 0) {
@@ -255,7 +272,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
           mbar_arrive_expect_tx(&s.m_full[slot], Smem::kMTile);
 #pragma unroll
           for (int c = 0; c < Smem::kChunks; ++c)
-            tma_load_3d(s.m[slot] + c * Smem::kMChunk, &mapM, &s.m_full[slot], c * 64, j, kz);
+            tma_load_3d(s.m[slot] + c * Smem::kMChunk, &mapM, &s.m_full[slot], c * 64, jb0 + j, kz);
           m_issued = ci + 1;
         }
         const int ks = j % KST;
@@ -263,7 +280,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         mbar_arrive_expect_tx(&s.k_full[ks], Smem::kKTile);
 #pragma unroll
         for (int c = 0; c < Smem::kKChunks; ++c)
-          tma_load_3d(s.k[ks] + c * Smem::kKChunk, &mapK, &s.k_full[ks], c * (128 / Smem::kKB), j * BN, kz);
+          tma_load_3d(s.k[ks] + c * Smem::kKChunk, &mapK, &s.k_full[ks], c * (128 / Smem::kKB), (jb0 + j) * BN, kz);
         k_issued = j + 1;
         return true;
       };
@@ -273,7 +290,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         mbar_arrive_expect_tx(&s.v_full[vs], Smem::kVTile);
 #pragma unroll
         for (int c = 0; c < Smem::kChunks; ++c)
-          tma_load_3d(s.v[vs] + c * Smem::kVChunk, &mapV, &s.v_full[vs], c * 64, j * BN, kz);
+          tma_load_3d(s.v[vs] + c * Smem::kVChunk, &mapV, &s.v_full[vs], c * 64, (jb0 + j) * BN, kz);
         v_issued = j + 1;
         return true;
       };
@@ -401,7 +418,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     const uint32_t tO = tmem + lane_base + TM::o;
     const uint32_t tP = tmem + lane_base + TM::p;
     const int i = q0 + r;
-    const int limit = (i < p.Sq) ? (CAUSAL ? min(p.Sk, max(0, i + p.Sk - p.Sq + 1)) : p.Sk) : 0;
+    const int i_mask = i % p.sq_mod;   // the query's position within its head
+    const int limit = (i < p.Sq) ? (CAUSAL ? min(p.Sk, max(0, i_mask + p.Sk - p.sq_mod + 1)) : p.Sk) : 0;
     const float sl2 = p.scale_log2;
     constexpr int kPairs = BN / 2;
     float m_run = -INFINITY, l_run = 0.0f;
@@ -416,7 +434,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     const float* kscale_row = FP8 ? p.kscale + static_cast<size_t>(b * p.Hkv + hk) * p.nbt : nullptr;
     float sk_next = 1.0f;
     if constexpr (FP8) {
-      if (nblk > 0) sk_next = __ldg(kscale_row);
+      if (nblk > 0) sk_next = __ldg(kscale_row + jb0);
       if (!mbar_wait(&s.q_full, 0, abort_flag, 0x340)) ok = false;
       uint4 qrow[D / 8];
 #pragma unroll
@@ -455,7 +473,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
       float fsc = 1.0f;   // FP8: dequantisation factor sq * sk_j of this block's scores
       if constexpr (FP8) {
         fsc = sq * sk_next;
-        if (j + 1 < nblk) sk_next = __ldg(kscale_row + j + 1);
+        if (j + 1 < nblk) sk_next = __ldg(kscale_row + jb0 + j + 1);
       }
       if (!mbar_wait(&s.s_full[sb], (j >> 1) & 1, abort_flag, 0x300)) { ok = false; break; }
       tc_fence_after();
@@ -482,7 +500,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
       __syncwarp();
       if (lane == 0) mbar_arrive(&s.s_free[sb]);
 
-      const int cmax = limit - j * BN;
+      const int cmax = limit - (jb0 + j) * BN;
       const float c_raw = SHIFT ? __uint_as_float(cw) : 0.0f;
       float mx, mn = 0.0f;
       if constexpr (F16ACC) {
@@ -647,6 +665,49 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     if (!have_o && !mbar_wait(&s.q_full, 0, abort_flag, 0x330)) ok = false;
     tc_fence_after();
     const float inv_l = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
+    if (p.part_o != nullptr) {
+      // split keys: this CTA's O / l in fp32 and m + log2 l for the combine kernel (the TMEM
+      // loads are warp-wide; only rows that exist are stored)
+      const size_t rows_total = static_cast<size_t>(p.B) * p.Hq * p.Sq;
+      const size_t row = (static_cast<size_t>(b) * p.Hq + hq) * p.Sq + i;
+      float* dst = p.part_o + (static_cast<size_t>(split) * rows_total + row) * D;
+      const bool live = i < p.Sq;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        float f[32];
+        uint32_t w[16];
+        if (have_o && ok) {
+          if constexpr (F16PV) {
+            tmem_ld_x16_pack16(tO + c * 32, w);
+            tmem_ld_wait();
+            reg_fence<16>(w);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              f[2 * e] = __half2float(__ushort_as_half(static_cast<unsigned short>(w[e] & 0xFFFFu))) * inv_l;
+              f[2 * e + 1] = __half2float(__ushort_as_half(static_cast<unsigned short>(w[e] >> 16))) * inv_l;
+            }
+          } else {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              tmem_ld_x16(tO + c * 32 + hh * 16, w);
+              tmem_ld_wait();
+              reg_fence<16>(w);
+#pragma unroll
+              for (int e = 0; e < 16; ++e) f[hh * 16 + e] = __uint_as_float(w[e]) * inv_l;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) f[e] = 0.0f;
+        }
+        if (live) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            reinterpret_cast<float4*>(dst + c * 32)[e] = make_float4(f[4 * e], f[4 * e + 1], f[4 * e + 2], f[4 * e + 3]);
+        }
+      }
+      if (live) p.part_lse[static_cast<size_t>(split) * rows_total + row] = (l_run > 0.0f) ? m_run + log2f(l_run) : -INFINITY;
+    } else {
     uint8_t* stage = s.q;
     // 16 output columns starting at col, as 8 packed fp16 pairs, into the swizzled staging
     auto stage16 = [&](int col, const uint32_t* h) {
@@ -719,12 +780,49 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
       const float lse = (l_run > 0.0f) ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
       p.lse[(static_cast<size_t>(b) * p.Hq + hq) * p.Sq + i] = lse;
     }
+    }  // not split
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (warp == 5) tmem_dealloc(tmem, 512);
+}
+
+// Merge of split-key partials: for each row, with lse_s = m_s + log2 l_s (log2 units) and
+// O_s = O / l of split s, O = sum_s 2^(lse_s - M) O_s / sum_s 2^(lse_s - M) and
+// LSE = ln 2 * (M + log2 sum_s 2^(lse_s - M)), M = max_s lse_s (a row no split saw gets
+// O = 0 and LSE = -inf). One warp per row, D / 32 columns per lane; HBM-bound and small.
+template <int D>
+__global__ void __launch_bounds__(256) combine_splits_kernel(const float* __restrict__ part_o,
+                                                             const float* __restrict__ part_lse, int splits,
+                                                             long long rows, __half* __restrict__ o,
+                                                             float* __restrict__ lse) {
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  float mx = -INFINITY;
+  for (int s2 = 0; s2 < splits; ++s2) mx = fmaxf(mx, part_lse[s2 * rows + row]);
+  constexpr int kPer = D / 32;
+  float acc[kPer];
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) acc[e] = 0.0f;
+  float wsum = 0.0f;
+  if (mx != -INFINITY) {
+    for (int s2 = 0; s2 < splits; ++s2) {
+      const float ls = part_lse[s2 * rows + row];
+      if (ls == -INFINITY) continue;
+      const float w = exp2f(ls - mx);
+      wsum += w;
+      const float* src = part_o + (s2 * rows + row) * D + lane * kPer;
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) acc[e] = fmaf(w, src[e], acc[e]);
+    }
+  }
+  const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) o[row * D + lane * kPer + e] = __float2half_rn(acc[e] * inv);
+  if (lane == 0 && lse != nullptr) lse[row] = wsum > 0.0f ? (mx + log2f(wsum)) * 0.69314718055994531f : -INFINITY;
 }
 
 }  // namespace pasa

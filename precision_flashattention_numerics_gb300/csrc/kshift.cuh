@@ -64,7 +64,7 @@ __device__ __forceinline__ int rne_div(int s, int n) {
 template <int D, int BN, int OUT = kShiftF16>
 __global__ void __launch_bounds__(kShiftThreads)
 kshift_kernel(const __half* __restrict__ k, void* __restrict__ kshift, __half* __restrict__ means,
-              float* __restrict__ kscale, int Sk, int nb) {
+              float* __restrict__ kscale, int Sk, int nb, int j0, int cap, int nb_cap) {
   constexpr int U = D / 8;                       // 16-byte units per row
   constexpr int R = kShiftThreads / U;           // row groups
   constexpr int RPT = (BN + R - 1) / R;          // rows per thread (upper bound)
@@ -77,7 +77,9 @@ kshift_kernel(const __half* __restrict__ k, void* __restrict__ kshift, __half* _
   __shared__ int sh_sum[NW][U][8];
   __shared__ uint32_t sh_amax[NW];
 
-  const int j = blockIdx.x;
+  // blocks [j0, nb) of the Sk valid rows; planes are cap rows (means: nb_cap blocks) apart.
+  // j0 > 0 refreshes the tail of a key cache after an append.
+  const int j = j0 + blockIdx.x;
   const int bh = blockIdx.y;
   const int tid = threadIdx.x;
   const int u = tid % U;
@@ -86,8 +88,8 @@ kshift_kernel(const __half* __restrict__ k, void* __restrict__ kshift, __half* _
   const int row0 = j * BN;
   const int n = min(BN, Sk - row0);
 
-  const uint4* src = reinterpret_cast<const uint4*>(k + (static_cast<size_t>(bh) * Sk + row0) * D) + u;
-  uint4* dst = reinterpret_cast<uint4*>(static_cast<__half*>(kshift) + (static_cast<size_t>(bh) * Sk + row0) * D) + u;
+  const uint4* src = reinterpret_cast<const uint4*>(k + (static_cast<size_t>(bh) * cap + row0) * D) + u;
+  uint4* dst = reinterpret_cast<uint4*>(static_cast<__half*>(kshift) + (static_cast<size_t>(bh) * cap + row0) * D) + u;
 
   uint4 x[RPT];
 #pragma unroll
@@ -190,7 +192,7 @@ kshift_kernel(const __half* __restrict__ k, void* __restrict__ kshift, __half* _
     __half* mp = reinterpret_cast<__half*>(&mv);
 #pragma unroll
     for (int h = 0; h < 8; ++h) mp[h] = mh[h];
-    reinterpret_cast<uint4*>(means + (static_cast<size_t>(bh) * nb + j) * D)[u] = mv;
+    reinterpret_cast<uint4*>(means + (static_cast<size_t>(bh) * nb_cap + j) * D)[u] = mv;
   }
   if constexpr (OUT == kShiftF16) {
 #pragma unroll
@@ -227,8 +229,8 @@ kshift_kernel(const __half* __restrict__ k, void* __restrict__ kshift, __half* _
     for (int w = 0; w < NW; ++w) amax = max(amax, sh_amax[w]);
     const float a = __half2float(__ushort_as_half(static_cast<unsigned short>(amax)));
     const float inv = a > 0.0f ? __fdiv_rn(448.0f, a) : 1.0f;
-    if (tid == 0) kscale[static_cast<size_t>(bh) * nb + j] = a > 0.0f ? __fdiv_rn(a, 448.0f) : 1.0f;
-    uint2* dst8 = reinterpret_cast<uint2*>(static_cast<uint8_t*>(kshift) + (static_cast<size_t>(bh) * Sk + row0) * D) + u;
+    if (tid == 0) kscale[static_cast<size_t>(bh) * nb_cap + j] = a > 0.0f ? __fdiv_rn(a, 448.0f) : 1.0f;
+    uint2* dst8 = reinterpret_cast<uint2*>(static_cast<uint8_t*>(kshift) + (static_cast<size_t>(bh) * cap + row0) * D) + u;
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
       const int r = rg + i * R;

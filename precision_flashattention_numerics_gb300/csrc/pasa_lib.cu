@@ -43,12 +43,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // 3-D fp16 view [planes, rows, D] of a contiguous tensor, 128-byte swizzled boxes of
 // 64 x box_rows x 1 elements.
 // 3-D map (D, rows, planes) with 128-byte rows per box chunk: 64 fp16 or 128 one-byte elements.
+// 3-D map over [planes][rows][D] with planes stride_rows rows apart (0: rows, dense).
 int make_map(CUtensorMap* m, const void* base, int D, long long rows, long long planes, int box_rows,
-             int elem_bytes = 2) {
+             int elem_bytes = 2, long long stride_rows = 0) {
   auto enc = encode_fn();
   if (!enc) return cuda_fail(cudaErrorNotSupported);
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(planes)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * elem_bytes, static_cast<cuuint64_t>(rows) * D * elem_bytes};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * elem_bytes, static_cast<cuuint64_t>(stride_rows > 0 ? stride_rows : rows) * D * elem_bytes};
   cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem_bytes), static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = enc(m, elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
@@ -94,12 +95,15 @@ WorkspaceLayout workspace_layout(int B, int Hkv, int Sk, int D, int mode) {
 }
 
 template <int D, int OUT>
-int launch_kshift(const void* k, void* ks, void* means, float* kscale, int B, int H, int Sk, cudaStream_t st) {
+int launch_kshift(const void* k, void* ks, void* means, float* kscale, int B, int H, int Sk, cudaStream_t st,
+                  int first_block = 0, int cap = 0) {
   constexpr int BN = pasa::block_rows_for(D);
   const int nb = (Sk + BN - 1) / BN;
-  dim3 grid(nb, B * H);
+  if (cap <= 0) cap = Sk;
+  dim3 grid(nb - first_block, B * H);
   pasa::kshift_kernel<D, BN, OUT><<<grid, pasa::kShiftThreads, 0, st>>>(
-      static_cast<const __half*>(k), ks, static_cast<__half*>(means), kscale, Sk, nb);
+      static_cast<const __half*>(k), ks, static_cast<__half*>(means), kscale, Sk, nb, first_block, cap,
+      (cap + BN - 1) / BN);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? PASA_OK : cuda_fail(e);
 }
@@ -126,7 +130,8 @@ int launch_attn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap&
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e);
   const long long ctas = static_cast<long long>(p.n_qblk) * p.Hq * p.B;
-  kern<<<static_cast<unsigned>(ctas), pasa::kAttnThreads, smem, st>>>(mq, mk, mv, mo, mm, p);
+  const unsigned splits = p.bps > 0 ? static_cast<unsigned>((p.nbt + p.bps - 1) / p.bps) : 1u;
+  kern<<<dim3(static_cast<unsigned>(ctas), splits), pasa::kAttnThreads, smem, st>>>(mq, mk, mv, mo, mm, p);
   e = cudaGetLastError();
   return e == cudaSuccess ? PASA_OK : cuda_fail(e);
 }
@@ -239,6 +244,22 @@ int pasa_kprep_fp8(const void* k, void* k8, void* means, float* kscale, int B, i
   return kshift_dispatch(k, k8, means, kscale, B, H, Sk, D, mode, static_cast<cudaStream_t>(stream));
 }
 
+int pasa_kshift_blocks(const void* k, void* k_shifted, void* means, int B, int H, int Sk, int Sk_cap, int D,
+                       int first_block, void* stream) {
+  if (!k || !k_shifted || !means) return PASA_ERR_NULLPTR;
+  if (B <= 0 || H <= 0 || Sk <= 0 || Sk_cap < Sk) return PASA_ERR_SHAPE;
+  if (D != 64 && D != 128) return PASA_ERR_UNSUPPORTED;
+  const int nb = (Sk + pasa::block_rows_for(D) - 1) / pasa::block_rows_for(D);
+  if (first_block < 0 || first_block >= nb) return PASA_ERR_SHAPE;
+  if (static_cast<long long>(B) * H > 65535) return PASA_ERR_SHAPE;  // grid.y
+  if (!aligned16(k) || !aligned16(k_shifted) || !aligned16(means)) return PASA_ERR_ALIGN;
+  int rc = check_device();
+  if (rc != PASA_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return D == 64 ? launch_kshift<64, pasa::kShiftF16>(k, k_shifted, means, nullptr, B, H, Sk, st, first_block, Sk_cap)
+                 : launch_kshift<128, pasa::kShiftF16>(k, k_shifted, means, nullptr, B, H, Sk, st, first_block, Sk_cap);
+}
+
 // Launch the attention kernel on (possibly shifted) keys `kk` and block means `mm`.
 static int attn_launch(const void* q, const void* kk, const void* mm, const void* v, void* o, float* lse, int B,
                        int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale, int mode, cudaStream_t st,
@@ -274,6 +295,10 @@ static int attn_launch(const void* q, const void* kk, const void* mm, const void
   p.bstats = reinterpret_cast<unsigned*>(block_stats);
   p.nbt = nb;
   p.kscale = kscale;
+  p.sq_mod = Sq;
+  p.bps = 0;
+  p.part_o = nullptr;
+  p.part_lse = nullptr;
   if (block_stats) {
     const cudaError_t e = cudaMemsetAsync(block_stats, 0, static_cast<size_t>(B) * Hq * nb * 2 * sizeof(float), st);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -312,6 +337,106 @@ int pasa_attn_fwd_fp8(const void* q, const void* k8, const void* means, const fl
   if (rc != PASA_OK) return rc;
   return attn_launch(q, k8, mode == PASA_MODE_SHIFT_FP8 ? means : k8, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale,
                      mode, static_cast<cudaStream_t>(stream), nullptr, nullptr, kscale);
+}
+
+// Decode path: key-block split and its partial-result workspace. By default at most one
+// wave of CTAs (152 SMs, one attention CTA each) and at least two key blocks per split.
+static int decode_split(int B, int Hkv, int Sk, int D, int splits_req, int* splits_out) {
+  const int bn = pasa::block_rows_for(D);
+  const int nb = (Sk + bn - 1) / bn;
+  const long long units = static_cast<long long>(B) * Hkv;
+  int splits = splits_req > 0 ? splits_req : static_cast<int>(std::min<long long>(152 / units, nb / 2));
+  splits = std::max(1, std::min(std::min(splits, nb), 65535));   // grid.y
+  const int bps = (nb + splits - 1) / splits;
+  splits = (nb + bps - 1) / bps;
+  *splits_out = splits;
+  return splits > 1 ? bps : 0;
+}
+
+size_t pasa_attn_fwd_decode_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D, int splits) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Sk <= 0 || Hq % Hkv != 0 || pasa::block_rows_for(D) == 0) return 0;
+  int sp = 1;
+  if (decode_split(B, Hkv, Sk, D, splits, &sp) == 0) return 0;
+  const size_t rows = static_cast<size_t>(B) * Hq * Sq;
+  return align_up(static_cast<size_t>(sp) * rows * D * 4, 256) + align_up(static_cast<size_t>(sp) * rows * 4, 256);
+}
+
+int pasa_attn_fwd_decode(const void* q, const void* k_shifted, const void* means, const void* v, void* o, float* lse,
+                         int B, int Hq, int Hkv, int Sq, int Sk, int Sk_cap, int D, int causal, float scale, int mode,
+                         int splits, void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = validate(q, k_shifted, v, o, lse, B, Hq, Hkv, Sq, Sk, D, mode);
+  if (rc != PASA_OK) return rc;
+  if (Sk_cap < Sk) return PASA_ERR_SHAPE;
+  if (fp8_mode(mode) || splits < 0) return PASA_ERR_UNSUPPORTED;
+  const int g = Hq / Hkv;
+  if (static_cast<long long>(g) * Sq > pasa::kTileRows) return PASA_ERR_UNSUPPORTED;  // one tile per kv group
+  const bool shift = shift_mode(mode);
+  if (shift && !means) return PASA_ERR_NULLPTR;
+  if (shift && !aligned16(means)) return PASA_ERR_ALIGN;
+  int sp = 1;
+  const int bps = decode_split(B, Hkv, Sk, D, splits, &sp);
+  const size_t need = pasa_attn_fwd_decode_workspace_bytes(B, Hq, Hkv, Sq, Sk, D, splits);
+  if (bps > 0) {
+    if (!workspace || workspace_bytes < need) return PASA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PASA_ERR_ALIGN;
+  }
+  rc = check_device();
+  if (rc != PASA_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (!(scale > 0.0f) || !std::isfinite(scale)) scale = 1.0f / std::sqrt(static_cast<float>(D));
+  const int bn = pasa::block_rows_for(D);
+  const int nb = (Sk + bn - 1) / bn;
+  // Q and O viewed as [B * Hkv, g * Sq, D]: the query rows of a kv group's g heads, contiguous
+  const int rows = g * Sq;
+  CUtensorMap mq, mk, mv, mo, mmeans;
+  if ((rc = make_map(&mq, q, D, rows, static_cast<long long>(B) * Hkv, pasa::kTileRows)) != PASA_OK) return rc;
+  // the cache: Sk valid rows of Sk_cap per head (reads past Sk are zero-filled and masked)
+  const long long planes = static_cast<long long>(B) * Hkv;
+  if ((rc = make_map(&mk, k_shifted, D, Sk, planes, bn, 2, Sk_cap)) != PASA_OK) return rc;
+  if ((rc = make_map(&mv, v, D, Sk, planes, bn, 2, Sk_cap)) != PASA_OK) return rc;
+  if ((rc = make_map(&mo, o, D, rows, planes, pasa::kTileRows)) != PASA_OK) return rc;
+  if (shift) {
+    if ((rc = make_map(&mmeans, means, D, nb, planes, pasa::kChunkBlocks, 2, (Sk_cap + bn - 1) / bn)) != PASA_OK)
+      return rc;
+  } else {
+    mmeans = mk;
+  }
+  pasa::AttnParams p;
+  p.lse = lse;
+  p.B = B;
+  p.Hq = Hkv;
+  p.Hkv = Hkv;
+  p.Sq = rows;
+  p.Sk = Sk;
+  p.n_qblk = 1;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.inv_scale_log2 = 1.0f / p.scale_log2;
+  p.stats = nullptr;
+  p.bstats = nullptr;
+  p.nbt = nb;
+  p.kscale = nullptr;
+  p.sq_mod = Sq;
+  p.bps = bps;
+  p.part_o = nullptr;
+  p.part_lse = nullptr;
+  const size_t nrows = static_cast<size_t>(B) * Hq * Sq;
+  if (bps > 0) {
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    p.part_o = reinterpret_cast<float*>(ws);
+    p.part_lse = reinterpret_cast<float*>(ws + align_up(static_cast<size_t>(sp) * nrows * D * 4, 256));
+  }
+  rc = D == 64 ? attn_dispatch<64, false>(mode, causal, mq, mk, mv, mo, mmeans, p, st)
+               : attn_dispatch<128, false>(mode, causal, mq, mk, mv, mo, mmeans, p, st);
+  if (rc != PASA_OK || bps == 0) return rc;
+  const unsigned cblocks = static_cast<unsigned>((nrows + 7) / 8);
+  if (D == 64)
+    pasa::combine_splits_kernel<64><<<cblocks, 256, 0, st>>>(p.part_o, p.part_lse, sp, static_cast<long long>(nrows),
+                                                             static_cast<__half*>(o), lse);
+  else
+    pasa::combine_splits_kernel<128><<<cblocks, 256, 0, st>>>(p.part_o, p.part_lse, sp, static_cast<long long>(nrows),
+                                                              static_cast<__half*>(o), lse);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? PASA_OK : cuda_fail(e);
 }
 
 int pasa_attn_fwd_ws(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,

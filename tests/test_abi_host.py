@@ -136,3 +136,59 @@ def test_fp8_entry_points_check_arguments(lib):
     # the fp16-key entry points refuse the FP8 modes
     assert lib.pasa_attn_fwd_shifted(P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), 1, 2, 1, 64, 64, 128, 0, 0.0,
                                      5, None) == -3
+
+
+def test_decode_entry_points_check_arguments(lib):
+    P = ctypes.c_void_p
+
+    # pasa_attn_fwd_decode(q, k_shifted, means, v, o, lse, B, Hq, Hkv, Sq, Sk, Sk_cap, D, causal, scale, mode,
+    #                      splits, workspace, workspace_bytes, stream)
+    def dec(q=FAKE, means=FAKE, B=1, Hq=8, Hkv=1, Sq=1, Sk=5000, cap=5000, D=128, mode=0, splits=0, ws=None,
+            ws_bytes=0):
+        return lib.pasa_attn_fwd_decode(P(q), P(FAKE), P(means) if means else None, P(FAKE), P(FAKE), P(FAKE), B, Hq,
+                                        Hkv, Sq, Sk, cap, D, 1, 0.0, mode, splits, P(ws) if ws else None, ws_bytes,
+                                        None)
+
+    assert dec(q=0) == -1
+    assert dec(cap=4999) == -2                 # the cache holds fewer rows than Sk
+    assert dec(Sq=17) == -3                    # 8 heads x 17 rows do not fit one 128-row tile
+    assert dec(mode=5) == -3 and dec(mode=6) == -3
+    assert dec(splits=-1) == -3
+    assert dec(means=0) == -1                  # the shift modes read the block means
+    assert dec(means=FAKE_MIS) == -4
+    assert dec(mode=3, means=0) == -7          # 40 key blocks split: the partials need a workspace
+    need = lib.pasa_attn_fwd_decode_workspace_bytes(1, 8, 1, 1, 5000, 128, 0)
+    assert need > 0
+    assert dec(ws=FAKE, ws_bytes=need - 1) == -7
+    assert dec(ws=FAKE + 16, ws_bytes=need) == -4   # 256-byte aligned
+    # pasa_kshift_blocks(k, k_shifted, means, B, H, Sk, Sk_cap, D, first_block, stream)
+    kb = lib.pasa_kshift_blocks
+    assert kb(None, P(FAKE), P(FAKE), 1, 1, 300, 300, 128, 0, None) == -1
+    assert kb(P(FAKE), P(FAKE), P(FAKE), 1, 1, 300, 299, 128, 0, None) == -2
+    assert kb(P(FAKE), P(FAKE), P(FAKE), 1, 1, 300, 300, 128, 3, None) == -2   # 300 rows: blocks 0..2
+    assert kb(P(FAKE), P(FAKE), P(FAKE), 1, 1, 300, 300, 128, -1, None) == -2
+    assert kb(P(FAKE), P(FAKE), P(FAKE), 1, 1, 300, 300, 96, 0, None) == -3
+    assert kb(P(FAKE), P(FAKE_MIS), P(FAKE), 1, 1, 300, 300, 128, 0, None) == -4
+
+
+def test_decode_workspace_bytes(lib):
+    # split choice: `splits` if given, else at most one CTA per SM (152) over the B * Hkv
+    # kv heads and at least two key blocks per split; blocks spread evenly; no workspace
+    # when that leaves one split. Partials: fp32 O [splits, B*Hq*Sq, D] and lse, 256-aligned.
+    def expect(B, Hq, Hkv, Sq, Sk, D, splits):
+        nb = -(-Sk // 128)
+        sp = splits if splits > 0 else min(152 // (B * Hkv), nb // 2)
+        sp = max(1, min(sp, nb, 65535))
+        bps = -(-nb // sp)
+        sp = -(-nb // bps)
+        if sp == 1:
+            return 0
+        rows = B * Hq * Sq
+        a = lambda x: -(-x // 256) * 256
+        return a(sp * rows * D * 4) + a(sp * rows * 4)
+
+    for args in [(1, 8, 8, 1, 32768, 128, 0), (8, 28, 4, 1, 32768, 128, 0), (1, 8, 8, 1, 640, 128, 0),
+                 (4, 32, 8, 4, 8192, 64, 0), (1, 8, 8, 1, 32768, 128, 5), (1, 28, 4, 1, 131072, 128, 0),
+                 (1, 8, 8, 1, 128, 128, 0), (1, 2, 1, 64, 777, 128, 100), (200, 8, 1, 1, 4096, 128, 0)]:
+        assert lib.pasa_attn_fwd_decode_workspace_bytes(*args) == expect(*args), args
+    assert lib.pasa_attn_fwd_decode_workspace_bytes(1, 3, 2, 1, 100, 128, 0) == 0   # Hq % Hkv != 0

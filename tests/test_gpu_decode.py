@@ -1,0 +1,213 @@
+"""GPU parity of the decode path: a few query rows per head against a key cache.
+
+"Online Pseudo-average Shifting Attention (PASA) for Robust Low-precision LLM Inference"
+(arXiv 2503.01873), Abstract: the method targets long-sequence inference. In decoding the
+keys live in a cache; the pseudo-average of a key block depends on that block's rows
+alone, so the shifted cache and its block means stay valid as rows are appended, and only
+the block that an append touches is recomputed (pasa_kshift_blocks). pasa_attn_fwd_decode
+packs the g query heads of a kv group into one tile and splits the key blocks across CTAs;
+the split results are merged by their log-sum-exps. The result must be attention up to
+rounding: the same gates as the prefill parity tests, against the same fp64 oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from gpu_helpers import f16all_bound, lse_tolerance, rel_errors, to_dev
+
+pytestmark = pytest.mark.gpu
+
+MODES = [0, 1, 2, 3, 4]
+MODE_NAMES = {0: "shift_f16acc", 1: "shift_f32acc", 2: "naive_f16acc", 3: "noshift_f32acc", 4: "shift_f16all"}
+BN = 128   # key block rows (both head dims)
+
+
+def pasa():
+    import precision_flashattention_numerics_gb300 as p
+
+    return p
+
+
+def inputs(B, Hq, Hkv, Sq, Sk, D, kind, seed, **params):
+    w = wl.Workload("decode", B, Hq, Hkv, Sq, Sk, D, False, kind, seed, tuple(sorted(params.items())))
+    return wl.make_inputs(w)
+
+
+def prepared(k, mode):
+    """Device cache for `mode`: shifted keys and means (modes 0, 1, 4) or raw keys."""
+    p = pasa()
+    (kt,) = to_dev(k)
+    if mode in (0, 1, 4):
+        return p.kshift(kt)
+    return kt, None
+
+
+def decode(q, k, v, causal, mode, splits=0):
+    p = pasa()
+    qt, vt = to_dev(q, v)
+    ks, means = prepared(k, mode)
+    o, lse = p.attn_fwd_decode(qt, ks, means, vt, causal=causal, mode=mode, splits=splits)
+    p.check_device_error()
+    return o, lse
+
+
+def gate(kind, mode):
+    if mode == 2 and kind != "iid":
+        return (5e-2, 2e-1)   # the naive fp16 kernel is only expected to stay finite here
+    if kind != "iid":
+        return (5e-3, 5e-2)
+    return (2e-3, 1e-2)
+
+
+CASES = [
+    # (B, Hq, Hkv, Sq, Sk, D, causal, kind, params, splits)
+    (1, 8, 1, 1, 5000, 128, False, "kbias", {"bias_std": 20.0}, 0),      # g = 8, one row per head
+    (2, 28, 4, 4, 3001, 128, True, "kbias_t3", {"bias_std": 10.0, "t_dof": 3, "t_scale": 4.0}, 0),  # g = 7
+    (1, 4, 4, 16, 1000, 64, True, "iid", {}, 3),
+    (1, 16, 2, 8, 2049, 64, False, "iid", {}, 0),                       # 64 packed rows
+    (1, 2, 1, 64, 777, 128, True, "iid", {}, 100),                      # 128 packed rows, a split per block
+    (3, 6, 3, 1, 130, 128, True, "iid", {}, 0),                         # two blocks: unsplit
+    (1, 4, 2, 2, 20000, 128, True, "kbias", {"bias_std": 20.0}, 0),
+]
+
+
+@pytest.mark.parametrize("mode", MODES, ids=[MODE_NAMES[m] for m in MODES])
+@pytest.mark.parametrize("case", range(len(CASES)))
+def test_decode_parity(case, mode):
+    B, Hq, Hkv, Sq, Sk, D, causal, kind, params, splits = CASES[case]
+    q, k, v = inputs(B, Hq, Hkv, Sq, Sk, D, kind, 500 + case, **params)
+    o, lse = decode(q, k, v, causal, mode, splits)
+    o_ref, lse_ref = oracle.attention(q, k, v, causal=causal)
+    og = o.double().cpu().numpy()
+    lg = lse.double().cpu().numpy()
+    assert np.isfinite(og).all()
+    if mode == 4:
+        # the fp16 accumulation bound over all of the cache's blocks also covers a split,
+        # whose fp16 accumulator sees fewer of them
+        base = 5e-2 if kind != "iid" else 1e-2
+        bound = base * np.abs(o_ref).max() + f16all_bound(Sk) * float(np.abs(v.astype(np.float64)).max())
+        assert np.abs(og - o_ref).max() <= bound
+    else:
+        rmse, rmax = rel_errors(og, o_ref)
+        tol = gate(kind, mode)
+        assert rmse <= tol[0] and rmax <= tol[1], (rmse, rmax)
+    fin = np.isfinite(lse_ref)
+    assert np.all(np.isneginf(lg[~fin]))
+    assert np.max(np.abs(lg[fin] - lse_ref[fin])) <= lse_tolerance(q, k, causal, mode, D)
+
+
+@pytest.mark.parametrize("mode", MODES, ids=[MODE_NAMES[m] for m in MODES])
+@pytest.mark.parametrize("g,Sq,causal", [(1, 1, False), (4, 3, True), (7, 16, True)])
+def test_unsplit_decode_is_the_prefill_kernel(g, Sq, causal, mode):
+    """One split: every packed row goes through the same per-row arithmetic as in the
+    unpacked kernel, so O and LSE are bit-identical to pasa_attn_fwd_shifted's."""
+    p = pasa()
+    Hkv, Sk, D = 2, 1500, 128
+    q, k, v = inputs(2, g * Hkv, Hkv, Sq, Sk, D, "kbias", 40 + g, bias_std=10.0)
+    qt, vt = to_dev(q, v)
+    ks, means = prepared(k, mode)
+    o1, l1 = p.attn_fwd_decode(qt, ks, means, vt, causal=causal, mode=mode, splits=1)
+    o2, l2 = p.attn_fwd_shifted(qt, ks, means, vt, causal=causal, mode=mode)
+    p.check_device_error()
+    assert torch.equal(o1, o2)
+    assert torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("mode", [0, 3])
+def test_cache_rows_past_the_length_are_not_read(mode):
+    """A cache of cap rows holding Sk valid ones: rows past Sk (here NaN, and means blocks
+    past the last one, also NaN) must not reach the result, which equals the dense call."""
+    p = pasa()
+    B, Hq, Hkv, Sq, Sk, cap, D = 2, 8, 2, 2, 1300, 2000, 128
+    q, k, v = inputs(B, Hq, Hkv, Sq, Sk, D, "kbias", 77, bias_std=20.0)
+    qt, kt, vt = to_dev(q, k, v)
+    nan = float("nan")
+    kc = torch.full((B, Hkv, cap, D), nan, device="cuda", dtype=torch.float16)
+    vc = torch.full((B, Hkv, cap, D), nan, device="cuda", dtype=torch.float16)
+    kc[:, :, :Sk] = kt
+    vc[:, :, :Sk] = vt
+    nbc = -(-cap // BN)
+    ksc = torch.full_like(kc, nan)
+    mc = torch.full((B, Hkv, nbc, D), nan, device="cuda", dtype=torch.float16)
+    if mode == 0:
+        p.kshift_blocks(kc, ksc, mc, 0, length=Sk)
+        ks, means = p.kshift(kt)
+        nb = -(-Sk // BN)
+        assert torch.equal(ksc[:, :, :Sk], ks) and torch.equal(mc[:, :, :nb], means)
+        assert torch.isnan(ksc[:, :, Sk:]).all() and torch.isnan(mc[:, :, nb:]).all()
+    else:
+        ksc, mc, ks, means = kc, None, kt, None
+    for splits in (0, 1, 4):
+        o1, l1 = p.attn_fwd_decode(qt, ksc, mc, vc, causal=True, mode=mode, splits=splits, length=Sk)
+        o2, l2 = p.attn_fwd_decode(qt, ks, means, vt, causal=True, mode=mode, splits=splits)
+        p.check_device_error()
+        assert torch.isfinite(o1).all()
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_kshift_blocks_after_append(D):
+    """Shift a cache of 300 rows, append 250 and refresh from the block the append touched
+    (block 2, which held 44 rows): every row and mean equals a full pasa_kshift of the 550
+    rows, and nothing past them is written."""
+    p = pasa()
+    B, H, cap, S0, S1 = 2, 3, 1000, 300, 550
+    _, k, _ = inputs(B, H, H, 1, cap, D, "kbias", 9, bias_std=20.0)
+    (kc,) = to_dev(k)
+    sentinel = 1234.0
+    ksc = torch.full_like(kc, sentinel)
+    mc = torch.full((B, H, -(-cap // BN), D), sentinel, device="cuda", dtype=torch.float16)
+    p.kshift_blocks(kc, ksc, mc, 0, length=S0)
+    ks0, m0 = p.kshift(kc[:, :, :S0].contiguous())
+    assert torch.equal(ksc[:, :, :S0], ks0) and torch.equal(mc[:, :, :3], m0)
+    assert (ksc[:, :, S0:] == sentinel).all() and (mc[:, :, 3:] == sentinel).all()
+    p.kshift_blocks(kc, ksc, mc, S0 // BN, length=S1)
+    ks1, m1 = p.kshift(kc[:, :, :S1].contiguous())
+    p.check_device_error()
+    assert torch.equal(ksc[:, :, :S1], ks1) and torch.equal(mc[:, :, :5], m1)
+    assert (ksc[:, :, S1:] == sentinel).all() and (mc[:, :, 5:] == sentinel).all()
+
+
+def test_decode_loop_against_the_oracle():
+    """Prefill 250 keys, then 6 decode steps of one query row per head, each appending its
+    key/value row to the cache, refreshing the touched block and attending causally."""
+    p = pasa()
+    B, Hq, Hkv, D, S0, steps, cap = 1, 8, 2, 128, 250, 6, 512
+    q, k, v = inputs(B, Hq, Hkv, steps, S0 + steps, D, "kbias", 123, bias_std=20.0)
+    (kt, vt) = to_dev(k, v)
+    kc = torch.zeros((B, Hkv, cap, D), device="cuda", dtype=torch.float16)
+    vc = torch.zeros_like(kc)
+    ksc = torch.zeros_like(kc)
+    mc = torch.zeros((B, Hkv, cap // BN, D), device="cuda", dtype=torch.float16)
+    kc[:, :, :S0], vc[:, :, :S0] = kt[:, :, :S0], vt[:, :, :S0]
+    p.kshift_blocks(kc, ksc, mc, 0, length=S0)
+    for t in range(steps):
+        Sk = S0 + t + 1
+        kc[:, :, Sk - 1], vc[:, :, Sk - 1] = kt[:, :, Sk - 1], vt[:, :, Sk - 1]
+        p.kshift_blocks(kc, ksc, mc, (Sk - 1) // BN, length=Sk)
+        qs = np.ascontiguousarray(q[:, :, t:t + 1])
+        (qt,) = to_dev(qs)
+        o, lse = p.attn_fwd_decode(qt, ksc, mc, vc, causal=True, mode=0, length=Sk)
+        p.check_device_error()
+        o_ref, lse_ref = oracle.attention(qs, k[:, :, :Sk], v[:, :, :Sk], causal=True)
+        rmse, rmax = rel_errors(o.double().cpu().numpy(), o_ref)
+        assert rmse <= 5e-3 and rmax <= 5e-2, (t, rmse, rmax)
+        assert np.abs(lse.double().cpu().numpy() - lse_ref).max() <= lse_tolerance(qs, k[:, :, :Sk], True, 0, D)
+
+
+def test_full_size_decode():
+    """The decode workload at full cache length (Qwen2-7B-like heads: Hq = 28, Hkv = 4,
+    D = 128; 32768 cached keys with a heavy-tailed sequence-dimension bias), B = 2 here to
+    bound host memory; automatic split, compared row by row with the oracle."""
+    B, Hq, Hkv, Sq, Sk, D = 2, 28, 4, 1, 32768, 128
+    q, k, v = inputs(B, Hq, Hkv, Sq, Sk, D, "kbias_t3", 2024, bias_std=10.0, t_dof=3, t_scale=4.0)
+    o_ref, lse_ref = oracle.attention(q, k, v, causal=True)
+    for mode in (0, 1, 3):
+        o, lse = decode(q, k, v, True, mode)
+        og = o.double().cpu().numpy()
+        rmse, rmax = rel_errors(og, o_ref)
+        assert np.isfinite(og).all()
+        assert rmse <= 5e-3 and rmax <= 5e-2, (mode, rmse, rmax)
+        assert np.abs(lse.double().cpu().numpy() - lse_ref).max() <= lse_tolerance(q, k, True, mode, D)
