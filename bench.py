@@ -36,6 +36,7 @@ import workloads as wl  # noqa: E402
 
 DEFAULT_WORKLOAD = "kbias10_t3_b1h28g4_s32768_d128_causal"
 ALSO_WORKLOADS = ["iid_b4h32g8_s8192_d128_causal"]
+DECODE_WORKLOAD = "kbias10_t3_b8h28g4_q1_s32768_d128_decode"
 MODE_NAMES = {0: "shift_f16acc", 1: "shift_f32acc", 2: "naive_f16acc", 3: "noshift_f32acc", 4: "shift_f16all",
               5: "shift_fp8", 6: "naive_fp8"}
 SHIFT_MODES = (0, 1, 4)     # a pseudo-average shift kernel (fp16 K') runs before the attention kernel
@@ -44,26 +45,39 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one attention-kernel launch,
 # from an ncu capture of a quarter of the 32K workload (7 of 28 query heads, 1 of 4 kv heads:
-# 75.79 MB read + 24.62 MB written) scaled x4 to a full launch; the traffic is per head, so it
+# 75.65 MB read + 24.45 MB written) scaled x4 to a full launch; the traffic is per head, so it
 # grows in proportion. Summary and command: profiles/attn_fwd_kbias10_t3_b1h7g1_s32768_full.md.
 # Reported only while the kernel source is the one the counters were taken on.
 TRAFFIC_WORKLOAD = "kbias10_t3_b1h28g4_s32768_d128_causal"
 TRAFFIC_MODE = 0
-TRAFFIC_BYTES = 4 * (75.793920e6 + 24.617216e6)
-TRAFFIC_KERNEL_SHA = "fe4170540f6e40a7"
+TRAFFIC_BYTES = 4 * (75.650304e6 + 24.449280e6)
+TRAFFIC_KERNEL_SHA = "6f9b9da0b6ed3e12"
+# The same for one decode-kernel launch on the decode workload (captured at full size:
+# 539.11 MB read + 3.19 MB written); profiles/decode_fwd_kbias10_t3_b8h28g4_q1_s32768_full.md.
+DECODE_TRAFFIC_BYTES = 539106560 + 3187456
+DECODE_TRAFFIC_SHA = "5245f38722c68c80"
+
+
+def _source_sha(name):
+    src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "precision_flashattention_numerics_gb300",
+                       "csrc", name)
+    try:
+        with open(src, "rb") as f:
+            return hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        return None
 
 
 def measured_traffic(w, mode):
-    src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "precision_flashattention_numerics_gb300",
-                       "csrc", "attn_fwd.cuh")
-    try:
-        with open(src, "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()[:16]
-    except OSError:
-        return None
-    if w.name != TRAFFIC_WORKLOAD or mode != TRAFFIC_MODE or sha != TRAFFIC_KERNEL_SHA:
+    if w.name != TRAFFIC_WORKLOAD or mode != TRAFFIC_MODE or _source_sha("attn_fwd.cuh") != TRAFFIC_KERNEL_SHA:
         return None
     return round(TRAFFIC_BYTES)
+
+
+def measured_decode_traffic(mode):
+    if mode != 0 or _source_sha("decode_fwd.cuh") != DECODE_TRAFFIC_SHA:
+        return None
+    return DECODE_TRAFFIC_BYTES
 
 
 def load_peaks():
@@ -309,6 +323,105 @@ def bench_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int, also
     return res
 
 
+def bench_decode(args, w: wl.Workload, local_rank: int, sampler=None):
+    """One decode step: refresh the shifted cache's last block (where the new key row lands:
+    pasa_kshift_blocks) and attend (pasa_attn_fwd_decode: decode kernel + split merge).
+    The cache is shifted once before timing, as a prefill would leave it."""
+    import torch
+
+    import precision_flashattention_numerics_gb300 as pasa
+
+    dev = torch.device("cuda", local_rank)
+    q, k, v = wl.make_inputs(w)
+    qt, kt, vt = (torch.from_numpy(x).to(dev) for x in (q, k, v))
+    mode = args.mode if args.mode in MODE_NAMES and args.mode not in FP8_MODES else 0
+    shift = mode in SHIFT_MODES
+    ks, means = pasa.kshift(kt) if shift else (kt, None)
+    o = torch.empty_like(qt)
+    lse = torch.empty((w.B, w.Hq, w.Sq), device=dev, dtype=torch.float32)
+    nbytes = pasa.decode_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D)
+    ws = torch.empty(max(nbytes, 256), device=dev, dtype=torch.uint8)
+    bn = pasa.block_rows(w.D)
+    last = (w.Sk - 1) // bn
+    stream = torch.cuda.current_stream()
+
+    def refresh():
+        if shift:
+            pasa.kshift_blocks(kt, ks, means, last)
+
+    def attend():
+        pasa.attn_fwd_decode(qt, ks, means, vt, causal=w.causal, mode=mode, out=o, lse=lse, workspace=ws)
+
+    for _ in range(max(3, args.warmup)):
+        refresh()
+        attend()
+    torch.cuda.synchronize()
+    pasa.check_device_error()
+    n = args.steps if args.decode else max(args.steps, 20)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    if sampler:
+        sampler.__enter__()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(n):
+        ev[i][0].record(stream)
+        refresh()
+        ev[i][1].record(stream)
+        attend()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    wall_ms = (time.perf_counter() - t0) * 1e3 / n
+    if sampler:
+        sampler.__exit__(None, None, None)
+    pasa.check_device_error()
+    step_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][2]) for i in range(n))
+    attn_ms = statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for i in range(n))
+    nb = -(-w.Sk // bn)
+    # algorithmic bytes of the attention: the cache (K' or K, and V), the block means, q, o, lse
+    cache = 2 * w.B * w.Hkv * w.Sk * w.D * 2
+    moved = cache + (w.B * w.Hkv * nb * w.D * 2 if shift else 0) + 2 * w.B * w.Hq * w.Sq * w.D * 2 \
+        + w.B * w.Hq * w.Sq * 4
+    gbs = moved / (attn_ms * 1e-3) / 1e9
+    return {
+        "workload": w.name, "mode": MODE_NAMES[mode], "tokens_per_s": round(w.B * w.Sq / (step_ms * 1e-3), 1),
+        "ms_per_step": round(step_ms, 5), "attn_ms": round(attn_ms, 5), "host_ms_per_step": round(wall_ms, 5),
+        "attn_bytes": moved, "attn_gbs": round(gbs, 1), "finite": bool(torch.isfinite(o).all().item()),
+        "launches_per_step": (1 if shift else 0) + (2 if nbytes else 1),
+    }
+
+
+def decode_main(args, rank: int, world: int, local_rank: int):
+    """`--decode`: one JSON line for the decode step alone (tokens/s; roofline against HBM)."""
+    w = wl.WORKLOADS[DECODE_WORKLOAD]
+    if args.impl == "reference" or world > 1:
+        if rank == 0:
+            print(json.dumps({"impl": args.impl, "unavailable": "the decode line is single-GPU, pasa arm only"}))
+        return
+    import torch
+
+    torch.cuda.set_device(local_rank)
+    peaks, peak_src = load_peaks()
+    sampler = ClockSampler(local_rank)
+    dec = bench_decode(args, w, local_rank, sampler)
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    out = {
+        "metric": "PASA decode tokens/s at 1 GB300 (one new query row per head per step)",
+        "value": dec["tokens_per_s"], "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": dec["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk, "D": w.D,
+                   "mode": dec["mode"], "l2": "the K/V cache (537 MB) is larger than L2; no flush"},
+        "roofline": {"kernel": "decode_fwd_kernel + combine_splits_kernel", "bound": "hbm",
+                     "achieved": dec["attn_gbs"], "peak": hbm, "unit": "GB/s",
+                     "frac": round(dec["attn_gbs"] / hbm, 4),
+                     "traffic": measured_decode_traffic(args.mode if args.mode in (0, 1, 2, 3, 4) else 0),
+                     "peak_source": f"{peak_src} copy bandwidth"},
+        "gpu_launches": dec["launches_per_step"] * args.steps, "clocks": sampler.summary(),
+        "finite_output": dec["finite"], "decode": dec,
+    }
+    print(json.dumps(out))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -320,9 +433,14 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-also", action="store_true")
+    ap.add_argument("--decode", action="store_true",
+                    help="time only the decode step (refresh the cache's last block + attend) on the decode workload")
     args = ap.parse_args()
 
     rank, world, local_rank = dist_env()
+    if args.decode:
+        decode_main(args, rank, world, local_rank)
+        return
     w = wl.WORKLOADS[args.workload]
     peaks, peak_src = load_peaks()
     config = {
@@ -372,6 +490,8 @@ def main():
             also[name] = {"tflops": round(ra["tflops"], 1), "ms_per_step": round(ra["ms_per_step"], 4),
                           "attn_ms": round(ra["attn_ms"], 4), "kshift_ms": round(ra["kshift_ms"], 4),
                           "finite": ra["finite"]}
+        if args.mode not in FP8_MODES:
+            also[DECODE_WORKLOAD] = bench_decode(args, wl.WORKLOADS[DECODE_WORKLOAD], local_rank)
 
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))  # fp16 dense = bf16 dense rate
     peak_note = f"{peak_src} bf16 dense burst (fp16 dense has the same nominal rate)"
@@ -402,6 +522,13 @@ def main():
         kshift_kernel = {"kernel": "kshift_kernel", "bound": "hbm", "achieved": round(gbs, 1), "peak": hbm,
                          "unit": "GB/s", "frac": round(gbs / hbm, 4), "bytes_per_launch": kb,
                          "ms": round(res["kshift_ms"], 5)}
+    dec = also.get(DECODE_WORKLOAD)
+    if dec is not None:
+        hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        dec["roofline"] = {"kernel": "decode_fwd_kernel + combine_splits_kernel", "bound": "hbm",
+                           "achieved": dec["attn_gbs"], "peak": hbm, "unit": "GB/s",
+                           "frac": round(dec["attn_gbs"] / hbm, 4),
+                           "traffic": measured_decode_traffic(args.mode), "peak_source": f"{peak_src} copy bandwidth"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -233,13 +233,17 @@ size_t pasa_attn_fwd_decode_workspace_bytes(int B, int Hq, int Hkv, int Sq, int 
  * pasa_kshift_blocks): a few new query rows per head against Sk cached keys, already
  * shifted by pasa_kshift / pasa_kshift_blocks (modes 0, 1, 4) or raw (modes 2, 3; means may
  * be NULL). The result equals pasa_attn_fwd_shifted's on the same arguments up to the
- * rounding of the split merge; with one split it is the same kernel arithmetic.
+ * rounding: the split merge, and in the decode kernel the order of the row sums and the
+ * offsets (fp32 dot products on the CUDA cores instead of the tensor cores).
  * Two changes of work layout serve the small Sq:
- *  - the g = Hq / Hkv query heads sharing a kv head are packed into one 128-row tile
- *    (requires g * Sq <= 128, else PASA_ERR_UNSUPPORTED), so each key block is read once
- *    per kv head instead of once per query head;
+ *  - the g = Hq / Hkv query heads sharing a kv head are packed into rows = g * Sq query
+ *    rows (requires rows <= 128, else PASA_ERR_UNSUPPORTED), so each key block is read
+ *    once per kv head instead of once per query head. With D = 128 and rows <= 32 a
+ *    decode kernel puts the 128 keys of a block on the MMA's M side and the packed rows
+ *    (padded to 16 or 32) on its N side; otherwise the attention kernel runs on the
+ *    packed rows as one 128-row tile;
  *  - the key blocks are split across `splits` CTAs per kv head (0 = automatic: at most one
- *    CTA per SM, at least two key blocks per split). Each split writes its O / l (fp32)
+ *    CTA per SM, at least eight key blocks per split). Each split writes its O / l (fp32)
  *    and m + log2 l to the workspace; a second kernel merges them:
  *    O = sum_s w_s O_s / sum_s w_s, w_s = 2^(lse_s - max lse), and writes o (fp16) and lse.
  * The causal mask is bottom-right aligned per head, as in pasa_attn_fwd. q, o: fp16

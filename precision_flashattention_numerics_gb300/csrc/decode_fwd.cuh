@@ -1,0 +1,598 @@
+// PASA decode attention on sm_103a: a few query rows per kv head against a key cache, with
+// the MMA operands swapped so that the 128 keys of a block fill the tcgen05 M dimension.
+//
+// Method: "Online Pseudo-average Shifting Attention (PASA) for Robust Low-precision LLM
+// Inference" (arXiv 2503.01873), Abstract: FlashAttention in half precision where each key
+// block K_j is shifted by its pseudo-average m_j before the fp16 score GEMM, and the offsets
+// q . m_j are added back in fp32 to the online max and sum. The method targets long-sequence
+// inference; there a kv head meets only rows = g * Sq query rows per step (the g query heads
+// that share it, Sq new tokens each), far fewer than the 128 rows of a tcgen05 MMA. This
+// kernel therefore computes the transposed products, with NQ = 16 or 32 >= rows (the packed
+// query rows, zero-padded by TMA):
+//   S'^T (128 keys x NQ) = K'_j Q^T        A = K'_j  (K-major, as TMA writes it)
+//                                          B = Q     (K-major)
+//   O^T  (128 dims x NQ) += V_j^T P_j^T    A = V_j   (MN-major: the same tile, read along D)
+//                                          B = P_j   (K-major, fp16, written by the softmax)
+// Thread t of the four softmax warps owns TMEM lane t: key t of the current block for the
+// scores and output dim t for O. The max of a query column over the block's keys is a
+// reduction across the 128 threads: in each warp a reduce-scatter over shuffles (each level
+// halves the values a lane holds, so NQ values take NQ + 0-1 shuffles instead of 5 NQ), then
+// the four warps' results through shared memory. Each thread sums the probabilities of its
+// own key (rescaled with its column's max); the 128 partial sums are reduced once at the end.
+// The offsets q . m_j of a 16-block chunk are computed on the CUDA cores (NQ x 16 dot
+// products of length 128 in fp32) when the chunk's means arrive.
+//
+// Score modes as in attn_fwd_kernel: F16ACC (fp16 score accumulator) or fp32, SHIFT (K' and
+// offsets) or raw keys, F16PV (fp16 O accumulator and fp16 per-thread row sums, added in
+// fp32 across threads at the end and rounded to fp16 once). Lazy rescaling: a column's max
+// moves only when a block raises it by more than kRescaleLog2; every thread takes the same
+// decision from the same shared maxima.
+//
+// Warp roles (192 threads): warps 0-3 softmax + epilogue; warp 4 TMA producer (Q once, K'_j
+// one block ahead of V_j, 16-block means chunks); warp 5 TMEM owner, one thread issuing
+// QK(j+1) before PV(j). Split keys (grid.y) as in attn_fwd_kernel: a split writes O / l in
+// fp32 and m + log2 l for combine_splits_kernel.
+//
+// Every wait is bounded (see ptx.cuh). The softmax warps meet at named barriers inside the
+// block loop, so after a failed wait they keep iterating (skipping the work, not the
+// barriers) instead of leaving the loop early.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include "attn_fwd.cuh"
+#include "ptx.cuh"
+
+namespace pasa {
+
+constexpr int kDecThreads = 192;
+
+struct DecodeParams {
+  __half* o;          // [planes][rows][128] fp16 (the [B, Hq, Sq, D] output)
+  float* lse;         // [planes * rows] natural-log LSE, or nullptr (unsplit launches)
+  float* part_o;      // split keys: [splits][planes * rows][128] fp32 O / l, else nullptr
+  float* part_lse;    // split keys: [splits][planes * rows] m + log2 l
+  int rows;           // packed query rows per kv head, g * sq <= NQ
+  int sq;             // query rows per head: packed row r is query r mod sq of head r / sq
+  int Sk, nbt;        // keys in the cache and key blocks, ceil(Sk / 128)
+  int bps;            // key blocks per split, 0 = one CTA per kv head
+  int causal;
+  float scale_log2;   // softmax scale * log2(e)
+};
+
+template <int NQ, int KST, int VST>
+struct DecodeSmem {
+  static constexpr int D = 128, BN = 128;
+  static constexpr int kTile = BN * D * 2;            // one fp16 block of K' or V
+  static constexpr int kChunk = BN * 128;             // one 64-column (128-byte) atom column of it
+  static constexpr int kQTile = NQ * D * 2, kQChunk = NQ * 128;
+  static constexpr int kPTile = NQ * BN * 2, kPChunk = NQ * 128;
+  static constexpr int kMTile = kChunkBlocks * D * 2, kMChunk = kChunkBlocks * 128;
+  alignas(1024) uint8_t k[KST][kTile];
+  alignas(1024) uint8_t v[VST][kTile];
+  alignas(1024) uint8_t q[kQTile];
+  alignas(1024) uint8_t pt[2][kPTile];                // P_j (rows = queries, K = keys), by block parity
+  alignas(1024) uint8_t m[2][kMTile];
+  alignas(16) float cv[2][kChunkBlocks][NQ];          // offsets q . m_j of a chunk, by chunk parity
+  alignas(16) float red[2][4][NQ];                    // per-warp column maxima, by block parity
+  uint64_t q_full;
+  uint64_t k_full[KST], k_empty[KST];
+  uint64_t v_full[VST], v_empty[VST];
+  uint64_t m_full[2], m_empty[2];
+  uint64_t s_full[2], s_free[2];
+  uint64_t p_full[2], p_free[2];
+  uint64_t o_full, drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// Bounded wait by every lane of a warp; the result is made warp-uniform.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, uint32_t site) {
+  const bool ok = mbar_wait(bar, parity, abort_flag, site);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Warp reduce-scatter of NQ per-lane values (NQ = 16 or 32), one shuffle level per call: at
+// lane offset OFF (16, 8, ..., 1) a lane keeps the half of its values selected by its lane
+// bit OFF and receives the other half from lane ^ OFF. The result, left in v[0], is the
+// reduction over all 32 lanes of column lane >> 1 (NQ = 16) or lane (NQ = 32).
+template <int NQ, bool MAX, int OFF>
+__device__ __forceinline__ void reduce_scatter_level(float* v, int lane) {
+  constexpr int n = NQ * OFF / 16;   // values a lane still holds
+  if constexpr (n >= 2) {
+    constexpr int h = n / 2;
+    const bool hi = (lane & OFF) != 0;
+#pragma unroll
+    for (int i = 0; i < h; ++i) {
+      const float send = hi ? v[i] : v[i + h];
+      const float keep = hi ? v[i + h] : v[i];
+      const float got = __shfl_xor_sync(0xffffffffu, send, OFF);
+      v[i] = MAX ? fmaxf(keep, got) : keep + got;
+    }
+  } else {
+    const float got = __shfl_xor_sync(0xffffffffu, v[0], OFF);
+    v[0] = MAX ? fmaxf(v[0], got) : v[0] + got;
+  }
+  if constexpr (OFF > 1) reduce_scatter_level<NQ, MAX, OFF / 2>(v, lane);
+}
+
+template <int NQ, bool MAX>
+__device__ __forceinline__ float warp_reduce_scatter(float* v, int lane) {
+  static_assert(NQ == 16 || NQ == 32, "columns");
+  reduce_scatter_level<NQ, MAX, 16>(v, lane);
+  return v[0];
+}
+
+template <int NQ, bool F16ACC, bool SHIFT, bool F16PV, int KST, int VST>
+__global__ void __launch_bounds__(kDecThreads, 1)
+decode_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
+                  const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapM,
+                  const DecodeParams p) {
+  static_assert(!F16PV || F16ACC, "fp16 PV accumulation is a variant of the fp16-score mode");
+  using Smem = DecodeSmem<NQ, KST, VST>;
+  static_assert(sizeof(Smem) + 1024 <= 227 * 1024, "shared memory per CTA");
+  constexpr int D = 128, BN = 128;
+  constexpr uint32_t kTmemCols = NQ == 16 ? 64 : 128;   // S_0, S_1, O: 3 * NQ columns
+  extern __shared__ uint8_t smem_raw[];
+  Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int plane = blockIdx.x;          // b * Hkv + kv head
+  const int split = blockIdx.y;
+  const int jb0 = split * p.bps;
+  const int nblk = p.bps > 0 ? max(0, min(p.bps, p.nbt - jb0)) : p.nbt;
+
+  if (tid == 0) {
+    mbar_init(&s.q_full, 1);
+    for (int i = 0; i < KST; ++i) { mbar_init(&s.k_full[i], 1); mbar_init(&s.k_empty[i], 1); }
+    for (int i = 0; i < VST; ++i) { mbar_init(&s.v_full[i], 1); mbar_init(&s.v_empty[i], 1); }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.m_full[i], 1);
+      mbar_init(&s.m_empty[i], 4);
+      mbar_init(&s.s_full[i], 1);
+      mbar_init(&s.s_free[i], 4);
+      mbar_init(&s.p_full[i], 4);
+      mbar_init(&s.p_free[i], 1);
+    }
+    mbar_init(&s.o_full, 1);
+    mbar_init(&s.drain, 1);
+    s.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&s.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s.tmem_base;
+  volatile int* abort_flag = &s.abort_flag;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&mapQ);
+      tma_prefetch_desc(&mapK);
+      tma_prefetch_desc(&mapV);
+      if (SHIFT) tma_prefetch_desc(&mapM);
+      mbar_arrive_expect_tx(&s.q_full, Smem::kQTile);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) tma_load_3d(s.q + c * Smem::kQChunk, &mapQ, &s.q_full, c * 64, 0, plane);
+      int k_issued = 0, v_issued = 0, m_issued = 0;
+      auto load_k = [&](int j) -> bool {
+        if (SHIFT && (j % kChunkBlocks) == 0) {
+          const int ci = j / kChunkBlocks, slot = ci & 1;
+          if (!mbar_wait(&s.m_empty[slot], ((ci >> 1) & 1) ^ 1, abort_flag, 0x501)) return false;
+          mbar_arrive_expect_tx(&s.m_full[slot], Smem::kMTile);
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+            tma_load_3d(s.m[slot] + c * Smem::kMChunk, &mapM, &s.m_full[slot], c * 64, jb0 + j, plane);
+          m_issued = ci + 1;
+        }
+        const int ks = j % KST;
+        if (!mbar_wait(&s.k_empty[ks], ((j / KST) & 1) ^ 1, abort_flag, 0x502)) return false;
+        mbar_arrive_expect_tx(&s.k_full[ks], Smem::kTile);
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+          tma_load_3d(s.k[ks] + c * Smem::kChunk, &mapK, &s.k_full[ks], c * 64, (jb0 + j) * BN, plane);
+        k_issued = j + 1;
+        return true;
+      };
+      auto load_v = [&](int j) -> bool {
+        const int vs = j % VST;
+        if (!mbar_wait(&s.v_empty[vs], ((j / VST) & 1) ^ 1, abort_flag, 0x503)) return false;
+        mbar_arrive_expect_tx(&s.v_full[vs], Smem::kTile);
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+          tma_load_3d(s.v[vs] + c * Smem::kChunk, &mapV, &s.v_full[vs], c * 64, (jb0 + j) * BN, plane);
+        v_issued = j + 1;
+        return true;
+      };
+      bool pok = nblk == 0 || load_k(0);
+      for (int j = 0; pok && j < nblk; ++j) {
+        if (j + 1 < nblk && !load_k(j + 1)) break;
+        if (!load_v(j)) break;
+      }
+      if (*abort_flag) {
+        // every copy this thread issued lands before the CTA's shared memory goes away
+        const uint64_t t0 = globaltimer_ns();
+        auto drain = [&](uint64_t* bar, uint32_t parity) {
+          while (!mbar_try_wait(bar, parity) && globaltimer_ns() - t0 < kWaitTimeoutNs) {
+          }
+        };
+        drain(&s.q_full, 0);
+        for (int j = max(0, k_issued - KST); j < k_issued; ++j) drain(&s.k_full[j % KST], (j / KST) & 1);
+        for (int j = max(0, v_issued - VST); j < v_issued; ++j) drain(&s.v_full[j % VST], (j / VST) & 1);
+        for (int ci = max(0, m_issued - 2); ci < m_issued; ++ci) drain(&s.m_full[ci & 1], (ci >> 1) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ------------------------------------------------------------------ MMA thread
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_f16_ab(BN, NQ, !F16ACC, false, false);
+      constexpr uint32_t id_o = idesc_f16_ab(D, NQ, !F16PV, true, false);
+      constexpr uint32_t hi = sdesc_hi_sw128(1024);
+      const uint32_t q_lo = sdesc_lo(smem_u32(s.q), 16);
+      const uint32_t k_lo0 = sdesc_lo(smem_u32(s.k[0]), 16);
+      const uint32_t v_lo0 = sdesc_lo(smem_u32(s.v[0]), Smem::kChunk);   // MN-major: atoms along D are kChunk apart
+      const uint32_t p_lo0 = sdesc_lo(smem_u32(s.pt[0]), 16);
+      constexpr uint32_t kKStride = sizeof(s.k[0]) >> 4, kVStride = sizeof(s.v[0]) >> 4;
+      constexpr uint32_t kPStride = sizeof(s.pt[0]) >> 4;
+      const uint32_t tO = tmem + 2 * NQ;
+      auto qk = [&](int j) -> bool {
+        const int ks = j % KST, sb = j & 1;
+        if (!mbar_wait(&s.k_full[ks], (j / KST) & 1, abort_flag, 0x601)) return false;
+        if (j >= 2 && !mbar_wait(&s.s_free[sb], ((j >> 1) - 1) & 1, abort_flag, 0x602)) return false;
+        tc_fence_after();
+        const uint32_t k_lo = k_lo0 + ks * kKStride;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off_k = ((kk / 4) * Smem::kChunk + (kk % 4) * 32) >> 4;
+          const uint32_t off_q = ((kk / 4) * Smem::kQChunk + (kk % 4) * 32) >> 4;
+          mma_ss_w(tmem + sb * NQ, k_lo + off_k, hi, q_lo + off_q, hi, id_s, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&s.s_full[sb]);
+        mma_commit(&s.k_empty[ks]);
+        return true;
+      };
+      auto pv = [&](int j) -> bool {
+        const int vs = j % VST, pb = j & 1;
+        if (!mbar_wait(&s.v_full[vs], (j / VST) & 1, abort_flag, 0x603)) return false;
+        if (!mbar_wait(&s.p_full[pb], (j >> 1) & 1, abort_flag, 0x604)) return false;
+        tc_fence_after();
+        const uint32_t v_lo = v_lo0 + vs * kVStride, p_lo = p_lo0 + pb * kPStride;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          const uint32_t off_p = ((kk / 4) * Smem::kPChunk + (kk % 4) * 32) >> 4;
+          mma_ss_w(tO, v_lo + kk * (2048 >> 4), hi, p_lo + off_p, hi, id_o, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&s.p_free[pb]);
+        mma_commit(&s.v_empty[vs]);
+        if (j == nblk - 1) mma_commit(&s.o_full);
+        return true;
+      };
+      bool ok = mbar_wait(&s.q_full, 0, abort_flag, 0x600);
+      if (ok && nblk > 0) ok = qk(0);
+      for (int j = 0; ok && j < nblk; ++j) {
+        if (j + 1 < nblk && !qk(j + 1)) break;
+        if (!pv(j)) break;
+      }
+      // every MMA issued here completes before TMEM is released
+      mma_commit(&s.drain);
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(&s.drain, 0) && globaltimer_ns() - t0 < kWaitTimeoutNs) {
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ softmax + epilogue
+    const int t = tid;   // TMEM lane: key t of a block, output dim t
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const float sl2 = p.scale_log2;
+    constexpr int kLaneShift = NQ == 16 ? 1 : 0;
+    const int q_of_lane = lane >> kLaneShift;              // column held after a reduce-scatter
+    const bool writer = (lane & ((1 << kLaneShift) - 1)) == 0;
+    // keys visible to every query row (causal: row r sees keys < Sk - sq + 1 + r mod sq)
+    const int kv_all = p.causal ? p.Sk - p.sq + 1 : p.Sk;
+    float m_run[NQ], lsum[NQ];
+    uint32_t lsum_h[NQ / 2];   // F16PV: fp16 partial row sums, two per register
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      m_run[q] = -INFINITY;
+      lsum[q] = 0.0f;
+    }
+#pragma unroll
+    for (int e = 0; e < NQ / 2; ++e) lsum_h[e] = 0u;
+    bool ok = true;
+    if (SHIFT) ok = warp_wait(&s.q_full, 0, abort_flag, 0x700);
+
+    for (int j = 0; j < nblk; ++j) {
+      const int sb = j & 1;
+      const int jg = jb0 + j;
+      if (SHIFT && (j % kChunkBlocks) == 0) {
+        // offsets of the chunk's 16 blocks: thread t takes block t % 16 and the query rows
+        // t / 16 + 8 e; fp32 dot products over the 128 dims (both tiles 128-byte swizzled)
+        const int ci = j / kChunkBlocks;
+        if (ok) ok = warp_wait(&s.m_full[ci & 1], (ci >> 1) & 1, abort_flag, 0x701);
+        if (ok) {
+          const int blk = t & 15, qg = t >> 4;
+          const uint8_t* mrow = s.m[ci & 1] + blk * 128;
+          float acc[NQ / 8];
+#pragma unroll
+          for (int e = 0; e < NQ / 8; ++e) acc[e] = 0.0f;
+#pragma unroll 4
+          for (int u = 0; u < 16; ++u) {
+            const int c = u >> 3, uu = u & 7;
+            const uint4 mv = *reinterpret_cast<const uint4*>(mrow + c * Smem::kMChunk + ((uu ^ (blk & 7)) << 4));
+            const __half2* mh = reinterpret_cast<const __half2*>(&mv);
+#pragma unroll
+            for (int e = 0; e < NQ / 8; ++e) {
+              const int qr = qg + 8 * e;
+              const uint4 qv =
+                  *reinterpret_cast<const uint4*>(s.q + c * Smem::kQChunk + qr * 128 + ((uu ^ (qr & 7)) << 4));
+              const __half2* qh = reinterpret_cast<const __half2*>(&qv);
+#pragma unroll
+              for (int h = 0; h < 4; ++h) {
+                const float2 mf = __half22float2(mh[h]);
+                const float2 qf = __half22float2(qh[h]);
+                acc[e] = fmaf(qf.x, mf.x, acc[e]);
+                acc[e] = fmaf(qf.y, mf.y, acc[e]);
+              }
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < NQ / 8; ++e) s.cv[ci & 1][blk][qg + 8 * e] = acc[e];
+        }
+        named_bar_sync(1, 128);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.m_empty[ci & 1]);
+      }
+
+      // scores of block j: this thread's key against the NQ query columns
+      if (ok) ok = warp_wait(&s.s_full[sb], (j >> 1) & 1, abort_flag, 0x702);
+      tc_fence_after();
+      float y[NQ];
+      {
+        const uint32_t tS = tmem + lane_base + sb * NQ;
+        if constexpr (F16ACC) {
+          uint32_t h[NQ / 2];
+#pragma unroll
+          for (int c = 0; c < NQ / 16; ++c) tmem_ld_x8_pack16(tS + c * 16, h + c * 8);
+          tmem_ld_wait();
+          reg_fence<NQ / 2>(h);
+#pragma unroll
+          for (int e = 0; e < NQ / 2; ++e) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[e]));
+            y[2 * e] = f.x;
+            y[2 * e + 1] = f.y;
+          }
+        } else {
+          uint32_t w[NQ];
+#pragma unroll
+          for (int c = 0; c < NQ / 16; ++c) tmem_ld_x16(tS + c * 16, w + c * 16);
+          tmem_ld_wait();
+          reg_fence<NQ>(w);
+#pragma unroll
+          for (int q = 0; q < NQ; ++q) y[q] = __uint_as_float(w[q]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.s_free[sb]);
+
+      // recovered scores in log2 units, masked
+      if constexpr (SHIFT) {
+        const float4* cr = reinterpret_cast<const float4*>(s.cv[(j / kChunkBlocks) & 1][j % kChunkBlocks]);
+#pragma unroll
+        for (int c4 = 0; c4 < NQ / 4; ++c4) {
+          const float4 c = cr[c4];
+          y[4 * c4] = (y[4 * c4] + c.x) * sl2;
+          y[4 * c4 + 1] = (y[4 * c4 + 1] + c.y) * sl2;
+          y[4 * c4 + 2] = (y[4 * c4 + 2] + c.z) * sl2;
+          y[4 * c4 + 3] = (y[4 * c4 + 3] + c.w) * sl2;
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) y[q] *= sl2;
+      }
+      const int key = jg * BN + t;
+      if ((jg + 1) * BN > kv_all) {   // a block some row does not see whole (uniform branch)
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+          const int lim = p.causal ? min(p.Sk, kv_all + q % p.sq) : p.Sk;
+          if (key >= lim) y[q] = -INFINITY;
+        }
+      }
+
+      // column maxima over the block's 128 keys
+      {
+        float v[NQ];
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) v[q] = y[q];
+        const float mx = warp_reduce_scatter<NQ, true>(v, lane);
+        if (writer) s.red[sb][warp][q_of_lane] = mx;
+      }
+      named_bar_sync(1, 128);
+      float alpha[NQ];
+      bool resc = false;
+      {
+        const float4* r4 = reinterpret_cast<const float4*>(s.red[sb]);
+#pragma unroll
+        for (int c4 = 0; c4 < NQ / 4; ++c4) {
+          const float4 a = r4[c4], b = r4[NQ / 4 + c4], c = r4[2 * (NQ / 4) + c4], d = r4[3 * (NQ / 4) + c4];
+          const float bm[4] = {fmaxf(fmaxf(a.x, b.x), fmaxf(c.x, d.x)), fmaxf(fmaxf(a.y, b.y), fmaxf(c.y, d.y)),
+                               fmaxf(fmaxf(a.z, b.z), fmaxf(c.z, d.z)), fmaxf(fmaxf(a.w, b.w), fmaxf(c.w, d.w))};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int q = 4 * c4 + e;
+            alpha[q] = 1.0f;
+            if (bm[e] > m_run[q] + kRescaleLog2) {   // also when m_run is still -inf
+              alpha[q] = ex2_approx(m_run[q] - bm[e]);
+              m_run[q] = bm[e];
+              resc = true;
+            }
+          }
+        }
+      }
+
+      // probabilities, this thread's row sums, and P_j (fp16) into shared memory
+      float pe[NQ];
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) pe[q] = ex2_approx(y[q] - (m_run[q] == -INFINITY ? 0.0f : m_run[q]));
+      uint32_t ph[NQ / 2];
+#pragma unroll
+      for (int e = 0; e < NQ / 2; ++e) ph[e] = pack_half2(pe[2 * e], pe[2 * e + 1]);
+      if constexpr (F16PV) {
+#pragma unroll
+        for (int e = 0; e < NQ / 2; ++e) {
+          const uint32_t l2 = resc ? hmul2(lsum_h[e], pack_half2(alpha[2 * e], alpha[2 * e + 1])) : lsum_h[e];
+          lsum_h[e] = hadd2(l2, ph[e]);
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) lsum[q] = (resc ? lsum[q] * alpha[q] : lsum[q]) + pe[q];
+      }
+      // P_(j-2) (same buffer) has been consumed by PV(j-2); a rescale of O needs PV(j-1) done
+      if (ok && j >= 2) ok = warp_wait(&s.p_free[sb], ((j >> 1) - 1) & 1, abort_flag, 0x703);
+      if (resc && j >= 1) {
+        if (ok) ok = warp_wait(&s.p_free[sb ^ 1], ((j - 1) >> 1) & 1, abort_flag, 0x704);
+        tc_fence_after();
+        const uint32_t tO = tmem + lane_base + 2 * NQ;
+        if constexpr (F16PV) {
+          uint32_t w[NQ / 2];
+#pragma unroll
+          for (int c = 0; c < NQ / 16; ++c) tmem_ld_x8_pack16(tO + c * 16, w + c * 8);
+          tmem_ld_wait();
+          reg_fence<NQ / 2>(w);
+#pragma unroll
+          for (int e = 0; e < NQ / 2; ++e) w[e] = hmul2(w[e], pack_half2(alpha[2 * e], alpha[2 * e + 1]));
+#pragma unroll
+          for (int c = 0; c < NQ / 16; ++c) tmem_st_x8_unpack16(tO + c * 16, w + c * 8);
+        } else {
+          uint32_t w[NQ];
+#pragma unroll
+          for (int c = 0; c < NQ / 16; ++c) tmem_ld_x16(tO + c * 16, w + c * 16);
+          tmem_ld_wait();
+          reg_fence<NQ>(w);
+#pragma unroll
+          for (int q = 0; q < NQ; ++q) w[q] = __float_as_uint(__uint_as_float(w[q]) * alpha[q]);
+#pragma unroll
+          for (int c = 0; c < NQ / 16; ++c) tmem_st_x16(tO + c * 16, w + c * 16);
+        }
+        tmem_st_wait();
+      }
+      {
+        // element (query q, key t) of the K-major, 128-byte swizzled P tile
+        uint8_t* prow = s.pt[sb] + (t >> 6) * Smem::kPChunk + (t & 7) * 2;
+        const int u = (t & 63) >> 3;
+#pragma unroll
+        for (int e = 0; e < NQ / 2; ++e) {
+          const int q0 = 2 * e;
+          *reinterpret_cast<__half*>(prow + q0 * 128 + ((u ^ (q0 & 7)) << 4)) =
+              __ushort_as_half(static_cast<unsigned short>(ph[e] & 0xFFFFu));
+          *reinterpret_cast<__half*>(prow + (q0 + 1) * 128 + ((u ^ ((q0 + 1) & 7)) << 4)) =
+              __ushort_as_half(static_cast<unsigned short>(ph[e] >> 16));
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.p_full[sb]);
+    }
+
+    // ------------------------------------------------------------------ epilogue
+    if (ok && nblk > 0) ok = warp_wait(&s.o_full, 0, abort_flag, 0x705);
+    tc_fence_after();
+    // row sums: the 128 threads' partial sums per column (F16PV: fp16 partials added in
+    // fp32, the total rounded to fp16)
+    float lt[NQ];
+    {
+      float v[NQ];
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        if constexpr (F16PV) {
+          const uint32_t w = lsum_h[q / 2];
+          v[q] = __half2float(__ushort_as_half(static_cast<unsigned short>((q & 1) ? (w >> 16) : (w & 0xFFFFu))));
+        } else {
+          v[q] = lsum[q];
+        }
+      }
+      const float sum = warp_reduce_scatter<NQ, false>(v, lane);
+      if (writer) s.red[nblk & 1][warp][q_of_lane] = sum;
+      named_bar_sync(1, 128);
+      const float4* r4 = reinterpret_cast<const float4*>(s.red[nblk & 1]);
+#pragma unroll
+      for (int c4 = 0; c4 < NQ / 4; ++c4) {
+        const float4 a = r4[c4], b = r4[NQ / 4 + c4], c = r4[2 * (NQ / 4) + c4], d = r4[3 * (NQ / 4) + c4];
+        lt[4 * c4] = (a.x + b.x) + (c.x + d.x);
+        lt[4 * c4 + 1] = (a.y + b.y) + (c.y + d.y);
+        lt[4 * c4 + 2] = (a.z + b.z) + (c.z + d.z);
+        lt[4 * c4 + 3] = (a.w + b.w) + (c.w + d.w);
+      }
+      if constexpr (F16PV) {
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) lt[q] = __half2float(__float2half_rn(lt[q]));
+      }
+    }
+    // O^T lane t is output dim t of every query column
+    float ov[NQ];
+    if (ok && nblk > 0) {
+      const uint32_t tO = tmem + lane_base + 2 * NQ;
+      if constexpr (F16PV) {
+        uint32_t w[NQ / 2];
+#pragma unroll
+        for (int c = 0; c < NQ / 16; ++c) tmem_ld_x8_pack16(tO + c * 16, w + c * 8);
+        tmem_ld_wait();
+        reg_fence<NQ / 2>(w);
+#pragma unroll
+        for (int e = 0; e < NQ / 2; ++e) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+          ov[2 * e] = f.x;
+          ov[2 * e + 1] = f.y;
+        }
+      } else {
+        uint32_t w[NQ];
+#pragma unroll
+        for (int c = 0; c < NQ / 16; ++c) tmem_ld_x16(tO + c * 16, w + c * 16);
+        tmem_ld_wait();
+        reg_fence<NQ>(w);
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) ov[q] = __uint_as_float(w[q]);
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) ov[q] = 0.0f;
+    }
+    const size_t rows_total = static_cast<size_t>(gridDim.x) * p.rows;
+    const size_t row0 = static_cast<size_t>(plane) * p.rows;
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      if (q < p.rows) {
+        const float inv_l = lt[q] > 0.0f ? 1.0f / lt[q] : 0.0f;
+        const float val = ov[q] * inv_l;
+        const float l2 = lt[q] > 0.0f ? m_run[q] + log2f(lt[q]) : -INFINITY;
+        if (p.part_o != nullptr) {
+          const size_t idx = static_cast<size_t>(split) * rows_total + row0 + q;
+          p.part_o[idx * D + t] = val;
+          if (t == q) p.part_lse[idx] = l2;
+        } else {
+          p.o[(row0 + q) * D + t] = __float2half_rn(val);
+          if (t == q && p.lse != nullptr) p.lse[row0 + q] = l2 * 0.69314718055994531f;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace pasa

@@ -11,6 +11,7 @@
 
 #include "../../include/pasa.h"
 #include "attn_fwd.cuh"
+#include "decode_fwd.cuh"
 #include "kshift.cuh"
 #include "ptx.cuh"
 
@@ -184,6 +185,36 @@ int validate(const void* q, const void* k, const void* v, const void* o, const f
   return PASA_OK;
 }
 
+// The swapped-operand decode kernel (D = 128, at most 32 packed query rows per kv head).
+template <int NQ, bool F16ACC, bool SHIFT, bool F16PV>
+int launch_decode(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mm,
+                         const pasa::DecodeParams& p, long long planes, int splits, cudaStream_t st) {
+  // ring slots: NQ = 16: 3 K' + 3 V (211 KB of shared memory); NQ = 32: 3 + 2
+  constexpr int KST = 3, VST = NQ == 16 ? 3 : 2;
+  auto kern = pasa::decode_fwd_kernel<NQ, F16ACC, SHIFT, F16PV, KST, VST>;
+  const int smem = static_cast<int>(sizeof(pasa::DecodeSmem<NQ, KST, VST>)) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return cuda_fail(e);
+  kern<<<dim3(static_cast<unsigned>(planes), static_cast<unsigned>(splits)), pasa::kDecThreads, smem, st>>>(mq, mk, mv,
+                                                                                                           mm, p);
+  e = cudaGetLastError();
+  return e == cudaSuccess ? PASA_OK : cuda_fail(e);
+}
+
+template <int NQ>
+int decode_dispatch(int mode, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                           const CUtensorMap& mm, const pasa::DecodeParams& p, long long planes, int splits,
+                           cudaStream_t st) {
+  switch (mode) {
+    case PASA_MODE_SHIFT_F16ACC: return launch_decode<NQ, true, true, false>(mq, mk, mv, mm, p, planes, splits, st);
+    case PASA_MODE_SHIFT_F32ACC: return launch_decode<NQ, false, true, false>(mq, mk, mv, mm, p, planes, splits, st);
+    case PASA_MODE_NAIVE_F16ACC: return launch_decode<NQ, true, false, false>(mq, mk, mv, mm, p, planes, splits, st);
+    case PASA_MODE_NOSHIFT_F32ACC: return launch_decode<NQ, false, false, false>(mq, mk, mv, mm, p, planes, splits, st);
+    case PASA_MODE_SHIFT_F16ALL: return launch_decode<NQ, true, true, true>(mq, mk, mv, mm, p, planes, splits, st);
+    default: return PASA_ERR_UNSUPPORTED;
+  }
+}
+
 }  // namespace
 
 extern "C" {
@@ -340,12 +371,13 @@ int pasa_attn_fwd_fp8(const void* q, const void* k8, const void* means, const fl
 }
 
 // Decode path: key-block split and its partial-result workspace. By default at most one
-// wave of CTAs (152 SMs, one attention CTA each) and at least two key blocks per split.
+// wave of CTAs (152 SMs, one CTA each) and at least eight key blocks per split, so that a
+// CTA's fixed start-up and pipeline fill stay small against its streaming time.
 static int decode_split(int B, int Hkv, int Sk, int D, int splits_req, int* splits_out) {
   const int bn = pasa::block_rows_for(D);
   const int nb = (Sk + bn - 1) / bn;
   const long long units = static_cast<long long>(B) * Hkv;
-  int splits = splits_req > 0 ? splits_req : static_cast<int>(std::min<long long>(152 / units, nb / 2));
+  int splits = splits_req > 0 ? splits_req : static_cast<int>(std::min<long long>(152 / units, nb / 8));
   splits = std::max(1, std::min(std::min(splits, nb), 65535));   // grid.y
   const int bps = (nb + splits - 1) / splits;
   splits = (nb + bps - 1) / bps;
@@ -388,52 +420,75 @@ int pasa_attn_fwd_decode(const void* q, const void* k_shifted, const void* means
   const int nb = (Sk + bn - 1) / bn;
   // Q and O viewed as [B * Hkv, g * Sq, D]: the query rows of a kv group's g heads, contiguous
   const int rows = g * Sq;
-  CUtensorMap mq, mk, mv, mo, mmeans;
-  if ((rc = make_map(&mq, q, D, rows, static_cast<long long>(B) * Hkv, pasa::kTileRows)) != PASA_OK) return rc;
-  // the cache: Sk valid rows of Sk_cap per head (reads past Sk are zero-filled and masked)
   const long long planes = static_cast<long long>(B) * Hkv;
+  const size_t nrows = static_cast<size_t>(B) * Hq * Sq;
+  float* part_o = nullptr;
+  float* part_lse = nullptr;
+  if (bps > 0) {
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    part_o = reinterpret_cast<float*>(ws);
+    part_lse = reinterpret_cast<float*>(ws + align_up(static_cast<size_t>(sp) * nrows * D * 4, 256));
+  }
+  CUtensorMap mq, mk, mv, mo, mmeans;
+  // the cache: Sk valid rows of Sk_cap per head (reads past Sk are zero-filled and masked)
   if ((rc = make_map(&mk, k_shifted, D, Sk, planes, bn, 2, Sk_cap)) != PASA_OK) return rc;
   if ((rc = make_map(&mv, v, D, Sk, planes, bn, 2, Sk_cap)) != PASA_OK) return rc;
-  if ((rc = make_map(&mo, o, D, rows, planes, pasa::kTileRows)) != PASA_OK) return rc;
   if (shift) {
     if ((rc = make_map(&mmeans, means, D, nb, planes, pasa::kChunkBlocks, 2, (Sk_cap + bn - 1) / bn)) != PASA_OK)
       return rc;
   } else {
     mmeans = mk;
   }
-  pasa::AttnParams p;
-  p.lse = lse;
-  p.B = B;
-  p.Hq = Hkv;
-  p.Hkv = Hkv;
-  p.Sq = rows;
-  p.Sk = Sk;
-  p.n_qblk = 1;
-  p.scale_log2 = scale * 1.4426950408889634f;
-  p.inv_scale_log2 = 1.0f / p.scale_log2;
-  p.stats = nullptr;
-  p.bstats = nullptr;
-  p.nbt = nb;
-  p.kscale = nullptr;
-  p.sq_mod = Sq;
-  p.bps = bps;
-  p.part_o = nullptr;
-  p.part_lse = nullptr;
-  const size_t nrows = static_cast<size_t>(B) * Hq * Sq;
-  if (bps > 0) {
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    p.part_o = reinterpret_cast<float*>(ws);
-    p.part_lse = reinterpret_cast<float*>(ws + align_up(static_cast<size_t>(sp) * nrows * D * 4, 256));
+  if (D == 128 && rows <= 32) {
+    // few rows: keys on the MMA's M side (decode_fwd_kernel)
+    const int nq = rows <= 16 ? 16 : 32;
+    if ((rc = make_map(&mq, q, D, rows, planes, nq)) != PASA_OK) return rc;
+    pasa::DecodeParams dp;
+    dp.o = static_cast<__half*>(o);
+    dp.lse = lse;
+    dp.part_o = part_o;
+    dp.part_lse = part_lse;
+    dp.rows = rows;
+    dp.sq = Sq;
+    dp.Sk = Sk;
+    dp.nbt = nb;
+    dp.bps = bps;
+    dp.causal = causal ? 1 : 0;
+    dp.scale_log2 = scale * 1.4426950408889634f;
+    rc = nq == 16 ? decode_dispatch<16>(mode, mq, mk, mv, mmeans, dp, planes, sp, st)
+                  : decode_dispatch<32>(mode, mq, mk, mv, mmeans, dp, planes, sp, st);
+  } else {
+    // query rows on the MMA's M side: the attention kernel on the packed [g * Sq] rows
+    if ((rc = make_map(&mq, q, D, rows, planes, pasa::kTileRows)) != PASA_OK) return rc;
+    if ((rc = make_map(&mo, o, D, rows, planes, pasa::kTileRows)) != PASA_OK) return rc;
+    pasa::AttnParams p;
+    p.lse = lse;
+    p.B = B;
+    p.Hq = Hkv;
+    p.Hkv = Hkv;
+    p.Sq = rows;
+    p.Sk = Sk;
+    p.n_qblk = 1;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.inv_scale_log2 = 1.0f / p.scale_log2;
+    p.stats = nullptr;
+    p.bstats = nullptr;
+    p.nbt = nb;
+    p.kscale = nullptr;
+    p.sq_mod = Sq;
+    p.bps = bps;
+    p.part_o = part_o;
+    p.part_lse = part_lse;
+    rc = D == 64 ? attn_dispatch<64, false>(mode, causal, mq, mk, mv, mo, mmeans, p, st)
+                 : attn_dispatch<128, false>(mode, causal, mq, mk, mv, mo, mmeans, p, st);
   }
-  rc = D == 64 ? attn_dispatch<64, false>(mode, causal, mq, mk, mv, mo, mmeans, p, st)
-               : attn_dispatch<128, false>(mode, causal, mq, mk, mv, mo, mmeans, p, st);
   if (rc != PASA_OK || bps == 0) return rc;
   const unsigned cblocks = static_cast<unsigned>((nrows + 7) / 8);
   if (D == 64)
-    pasa::combine_splits_kernel<64><<<cblocks, 256, 0, st>>>(p.part_o, p.part_lse, sp, static_cast<long long>(nrows),
+    pasa::combine_splits_kernel<64><<<cblocks, 256, 0, st>>>(part_o, part_lse, sp, static_cast<long long>(nrows),
                                                              static_cast<__half*>(o), lse);
   else
-    pasa::combine_splits_kernel<128><<<cblocks, 256, 0, st>>>(p.part_o, p.part_lse, sp, static_cast<long long>(nrows),
+    pasa::combine_splits_kernel<128><<<cblocks, 256, 0, st>>>(part_o, part_lse, sp, static_cast<long long>(nrows),
                                                               static_cast<__half*>(o), lse);
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? PASA_OK : cuda_fail(e);

@@ -261,6 +261,13 @@ __device__ __forceinline__ void tmem_st_x16_unpack16(uint32_t taddr, const uint3
       : "memory");
 }
 
+// 8 registers of two fp16 values each -> 16 columns.
+__device__ __forceinline__ void tmem_st_x8_unpack16(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.unpack::16b.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
 __device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t* r) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
@@ -346,6 +353,11 @@ __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool d_f32, bool b_mn_major) {
   return (d_f32 ? 1u : 0u) << 4 | (b_mn_major ? 1u : 0u) << 16 | static_cast<uint32_t>(N >> 3) << 17 |
          static_cast<uint32_t>(M >> 4) << 24;
+}
+
+// The same with either operand's major-ness chosen (bit 15 for A, bit 16 for B).
+__host__ __device__ constexpr uint32_t idesc_f16_ab(int M, int N, bool d_f32, bool a_mn_major, bool b_mn_major) {
+  return idesc_f16(M, N, d_f32, b_mn_major) | (a_mn_major ? 1u : 0u) << 15;
 }
 
 // ---------------------------------------------------------------------------------------

@@ -173,11 +173,11 @@ def test_decode_entry_points_check_arguments(lib):
 
 def test_decode_workspace_bytes(lib):
     # split choice: `splits` if given, else at most one CTA per SM (152) over the B * Hkv
-    # kv heads and at least two key blocks per split; blocks spread evenly; no workspace
+    # kv heads and at least eight key blocks per split; blocks spread evenly; no workspace
     # when that leaves one split. Partials: fp32 O [splits, B*Hq*Sq, D] and lse, 256-aligned.
     def expect(B, Hq, Hkv, Sq, Sk, D, splits):
         nb = -(-Sk // 128)
-        sp = splits if splits > 0 else min(152 // (B * Hkv), nb // 2)
+        sp = splits if splits > 0 else min(152 // (B * Hkv), nb // 8)
         sp = max(1, min(sp, nb, 65535))
         bps = -(-nb // sp)
         sp = -(-nb // bps)

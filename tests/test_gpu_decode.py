@@ -99,20 +99,31 @@ def test_decode_parity(case, mode):
 
 
 @pytest.mark.parametrize("mode", MODES, ids=[MODE_NAMES[m] for m in MODES])
-@pytest.mark.parametrize("g,Sq,causal", [(1, 1, False), (4, 3, True), (7, 16, True)])
-def test_unsplit_decode_is_the_prefill_kernel(g, Sq, causal, mode):
-    """One split: every packed row goes through the same per-row arithmetic as in the
-    unpacked kernel, so O and LSE are bit-identical to pasa_attn_fwd_shifted's."""
+@pytest.mark.parametrize("g,Sq,D,causal", [(7, 16, 128, True), (8, 2, 64, True), (1, 1, 128, False),
+                                           (4, 3, 128, True), (8, 4, 128, True)])
+def test_single_split_against_the_prefill_kernel(g, Sq, D, causal, mode):
+    """One split. More than 32 packed rows, or D = 64, run the prefill kernel on the packed
+    rows: every row goes through the same per-row arithmetic, so O and LSE are bit-identical
+    to pasa_attn_fwd_shifted's. Up to 32 rows at D = 128 run the swapped-operand decode
+    kernel: same scores, offsets and row sums summed in another order, so O agrees to a few
+    fp16 roundings of P (relative 2^-10 per term) and the LSE to fp32 rounding."""
     p = pasa()
-    Hkv, Sk, D = 2, 1500, 128
+    Hkv, Sk = 2, 1500
     q, k, v = inputs(2, g * Hkv, Hkv, Sq, Sk, D, "kbias", 40 + g, bias_std=10.0)
     qt, vt = to_dev(q, v)
     ks, means = prepared(k, mode)
     o1, l1 = p.attn_fwd_decode(qt, ks, means, vt, causal=causal, mode=mode, splits=1)
     o2, l2 = p.attn_fwd_shifted(qt, ks, means, vt, causal=causal, mode=mode)
     p.check_device_error()
-    assert torch.equal(o1, o2)
-    assert torch.equal(l1, l2)
+    if D == 64 or g * Sq > 32:
+        assert torch.equal(o1, o2)
+        assert torch.equal(l1, l2)
+    else:
+        d = (o1.double() - o2.double()).abs().max().item()
+        scale = o2.double().abs().max().item()
+        tol = f16all_bound(Sk) if mode == 4 else 2e-3
+        assert d <= tol * scale, (d, scale)
+        assert (l1.double() - l2.double()).abs().max().item() <= (f16all_bound(Sk) if mode == 4 else 1e-4)
 
 
 @pytest.mark.parametrize("mode", [0, 3])
@@ -200,14 +211,19 @@ def test_decode_loop_against_the_oracle():
 def test_full_size_decode():
     """The decode workload at full cache length (Qwen2-7B-like heads: Hq = 28, Hkv = 4,
     D = 128; 32768 cached keys with a heavy-tailed sequence-dimension bias), B = 2 here to
-    bound host memory; automatic split, compared row by row with the oracle."""
+    bound host memory; automatic split, compared row by row with the oracle. Gates as in
+    the prefill full-size tests: relRMSE <= 5e-3 on biased keys for modes 0, 1, 3; the naive
+    fp16 mode and the fp16-PV mode are reported and must stay finite."""
     B, Hq, Hkv, Sq, Sk, D = 2, 28, 4, 1, 32768, 128
     q, k, v = inputs(B, Hq, Hkv, Sq, Sk, D, "kbias_t3", 2024, bias_std=10.0, t_dof=3, t_scale=4.0)
     o_ref, lse_ref = oracle.attention(q, k, v, causal=True)
-    for mode in (0, 1, 3):
+    for mode in (0, 1, 2, 3, 4):
         o, lse = decode(q, k, v, True, mode)
         og = o.double().cpu().numpy()
         rmse, rmax = rel_errors(og, o_ref)
+        print(f"\nfull-size decode, mode {mode}: relRMSE={rmse:.3e} relMax={rmax:.3e}")
         assert np.isfinite(og).all()
-        assert rmse <= 5e-3 and rmax <= 5e-2, (mode, rmse, rmax)
+        if mode in (2, 4):
+            continue   # as in the prefill full-size tests: reported only on biased heavy-tailed keys
+        assert rmse <= 5e-3, (mode, rmse, rmax)
         assert np.abs(lse.double().cpu().numpy() - lse_ref).max() <= lse_tolerance(q, k, True, mode, D)

@@ -96,6 +96,11 @@ WORKLOADS = {
         # a quarter of the heads of the 32K biased workload, for the same reason
         Workload("kbias10_t3_b1h7g1_s32768_d128_causal", 1, 7, 1, 32768, 32768, 128, True,
                  "kbias_t3", 1045, _p(bias_std=10.0, t_scale=4.0, t_dof=3)),
+        # decode: one new query row per head of 8 sequences against a 32K-key cache (the
+        # 32K workload's heads and key distribution); the cache (537 MB of K and V) is larger
+        # than L2
+        Workload("kbias10_t3_b8h28g4_q1_s32768_d128_decode", 8, 28, 4, 1, 32768, 128, True,
+                 "kbias_t3", 1055, _p(bias_std=10.0, t_scale=4.0, t_dof=3)),
         # overflow demonstration: slow in-phase resonance with A = 48 pushes raw scores past 65504
         Workload("resonance_hot_a48_b2h5_s9216_d64", 2, 5, 5, 9216, 9216, 64, False,
                  "resonance", 1033, _p(A=48.0, noise_std=0.5, freq="slow", phase_flip=False)),
