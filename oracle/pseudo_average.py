@@ -26,6 +26,11 @@ It is a "pseudo" average: the mean of K rounded to the grid of the block's large
 magnitude. Because m sits on that grid, K - m is exact in fp16 for most elements, so
 shifting loses almost nothing even when the true mean is near zero. Parity for this
 function is pinned by closed forms and bounds in tests/test_pseudo_average_oracle.py.
+
+The alternative reading kept beside it (``rule="plain"``): steps 2-4 replaced by
+m = fp16(exact mean of the block's n values), rounded to nearest even once; the guard of
+step 5 and step 6 are the same. That is the plain fp16-rounded block mean, which the
+grid reading is compared against.
 """
 from __future__ import annotations
 
@@ -58,8 +63,26 @@ def _round_half_even_div(num: np.ndarray, den: np.ndarray) -> np.ndarray:
     return np.where(num < 0, -q, q)
 
 
-def block_pseudo_average(kb: np.ndarray) -> np.ndarray:
-    """Pseudo-average of one key block ``kb`` [n, D] fp16 (steps 1-5). Returns [D] fp16."""
+def fp16_round_rational(num: int, den: int) -> float:
+    """num / den (Python integers, den > 0) rounded to the nearest fp16 value, ties to even,
+    in exact integer arithmetic. The magnitude must stay below 65520 (no overflow)."""
+    if num == 0:
+        return 0.0
+    a = abs(num)
+    k = a.bit_length() - den.bit_length()          # 2^k <= a / den < 2^(k+1) after the fix-up
+    if (a << max(0, -k)) < (den << max(0, k)):
+        k -= 1
+    u = max(k - 10, -24)                           # exponent of the fp16 spacing at a / den
+    n2, d2 = (a, den << u) if u >= 0 else (a << -u, den)
+    q, r = divmod(n2, d2)
+    if 2 * r > d2 or (2 * r == d2 and q % 2 == 1):
+        q += 1
+    return float(np.ldexp(float(q), u)) * (1.0 if num > 0 else -1.0)
+
+
+def block_pseudo_average(kb: np.ndarray, rule: str = "grid") -> np.ndarray:
+    """Pseudo-average of one key block ``kb`` [n, D] fp16 (steps 1-5; ``rule="plain"``: the
+    exact block mean rounded once to fp16). Returns [D] fp16."""
     kb = np.asarray(kb, dtype=np.float16)
     n = kb.shape[0]
     if n == 0:
@@ -70,19 +93,26 @@ def block_pseudo_average(kb: np.ndarray) -> np.ndarray:
     M = np.max(np.abs(xm), axis=0).astype(np.float16)
     bits = M.view(np.uint16).astype(np.int64) & 0x7FFF
     E = bits >> 10
-    g = grid_step(M)
-    t = np.rint(xm / g).astype(np.int64)            # exact: g is a power of two
-    s = np.sum(t, axis=0)
-    mu = _round_half_even_div(s, np.full_like(s, n))
-    m = mu.astype(np.float64) * g
+    if rule == "plain":
+        # every fp16 value is an integer multiple of 2^-24: the sum is an exact integer
+        units = [int(v) for v in np.sum(np.rint(np.ldexp(xm, 24)).astype(np.int64), axis=0)]
+        m = np.array([fp16_round_rational(s_, n << 24) for s_ in units])
+    elif rule == "grid":
+        g = grid_step(M)
+        t = np.rint(xm / g).astype(np.int64)            # exact: g is a power of two
+        s = np.sum(t, axis=0)
+        mu = _round_half_even_div(s, np.full_like(s, n))
+        m = mu.astype(np.float64) * g
+    else:
+        raise ValueError(rule)
     m = np.where((E >= 30) | ~finite, 0.0, m)
     out = m.astype(np.float16)
     assert np.all(out.astype(np.float64) == m), "pseudo-average must be an exact fp16 value"
     return out
 
 
-def kshift(k: np.ndarray, block_rows: int | None = None):
-    """Shift every key block by its pseudo-average.
+def kshift(k: np.ndarray, block_rows: int | None = None, rule: str = "grid"):
+    """Shift every key block by its pseudo-average (``rule`` as in block_pseudo_average).
 
     k: [B, H, Sk, D] fp16. Returns (k_shifted [B, H, Sk, D] fp16,
     means [B, H, ceil(Sk / block_rows), D] fp16).
@@ -97,14 +127,20 @@ def kshift(k: np.ndarray, block_rows: int | None = None):
         for h in range(H):
             for j in range(nb):
                 r0, r1 = j * block_rows, min(Sk, (j + 1) * block_rows)
-                m = block_pseudo_average(k[b, h, r0:r1])
+                m = block_pseudo_average(k[b, h, r0:r1], rule)
                 means[b, h, j] = m
                 ks[b, h, r0:r1] = (k[b, h, r0:r1].astype(np.float64) - m.astype(np.float64)).astype(np.float16)
     return ks, means
 
 
-def kshift_fast(k: np.ndarray, block_rows: int | None = None):
-    """Same result as :func:`kshift`, vectorised over all blocks (for large inputs)."""
+def kshift_fast(k: np.ndarray, block_rows: int | None = None, rule: str = "grid"):
+    """Same result as :func:`kshift`, vectorised over all blocks (for large inputs).
+
+    rule="plain" rounds the exact mean S / n (S the exact sum, an integer multiple of
+    2^-24 below 2^22) through float64 and then to fp16. That equals one rounding of the
+    exact mean: a value S / (n 2^24) that is not itself an fp16 tie lies at least
+    2^-25 / n >= 2^-32 from every tie (ties are multiples of 2^-25), while the float64
+    division errs by at most 2^-53 * 2^15 = 2^-38."""
     k = np.asarray(k, dtype=np.float16)
     B, H, Sk, D = k.shape
     block_rows = block_rows_for(D) if block_rows is None else block_rows
@@ -122,12 +158,20 @@ def kshift_fast(k: np.ndarray, block_rows: int | None = None):
     xm = np.where(fin & vmask, x, 0.0)
     M = np.max(np.abs(xm), axis=3).astype(np.float16)
     E = (M.view(np.uint16).astype(np.int64) & 0x7FFF) >> 10
-    g = grid_step(M)
-    t = np.rint(xm / g[:, :, :, None, :]).astype(np.int64)
-    s = np.sum(t, axis=3)
     n = np.minimum(block_rows, Sk - np.arange(nb) * block_rows).astype(np.int64)
-    mu = _round_half_even_div(s, np.broadcast_to(n[None, None, :, None], s.shape))
-    m = np.where((E >= 30) | ~finite, 0.0, mu.astype(np.float64) * g)
+    if rule == "plain":
+        s = np.sum(np.rint(np.ldexp(xm, 24)).astype(np.int64), axis=3)
+        mean = s.astype(np.float64) / n[None, None, :, None]
+        mplain = np.ldexp(mean, -24).astype(np.float16).astype(np.float64)
+        m = np.where((E >= 30) | ~finite, 0.0, mplain)
+    elif rule == "grid":
+        g = grid_step(M)
+        t = np.rint(xm / g[:, :, :, None, :]).astype(np.int64)
+        s = np.sum(t, axis=3)
+        mu = _round_half_even_div(s, np.broadcast_to(n[None, None, :, None], s.shape))
+        m = np.where((E >= 30) | ~finite, 0.0, mu.astype(np.float64) * g)
+    else:
+        raise ValueError(rule)
     means = m.astype(np.float16)
     ks = (x - means.astype(np.float64)[:, :, :, None, :]).reshape(B, H, nb * block_rows, D)[:, :, :Sk]
     return ks.astype(np.float16), means

@@ -145,3 +145,109 @@ def test_recovered_score_magnitude_equals_raw_when_shift_is_exact(oracle_mod):
         rec = oracle_mod.row_max_abs_recovered(q, ks, means, 112, causal)
         np.testing.assert_array_equal(rec, raw)
         assert np.median(raw / np.maximum(oracle_mod.row_max_abs_score(q, ks, causal), 1)) > 2
+
+
+# ---------------------------------------------------------------------------------------
+# The alternative reading kept as a switch: m = the exact block mean rounded once to fp16.
+
+
+def test_fp16_round_rational_against_single_roundings():
+    # num / den exactly representable in float64 (den a power of two): numpy's float64 ->
+    # float16 conversion is then a single correct rounding to compare against
+    rng = np.random.default_rng(11)
+    for _ in range(3000):
+        e = int(rng.integers(0, 40))
+        num = int(rng.integers(-(1 << 40), 1 << 40)) >> int(rng.integers(0, 30))
+        val = num / float(1 << e)
+        if abs(val) >= 65504:
+            continue
+        assert pa.fp16_round_rational(num, 1 << e) == float(np.float16(val))
+    # ties go to the even neighbour, in the normal and the subnormal range
+    assert pa.fp16_round_rational(2049, 2) == 1024.0          # 1024.5: between 1024 and 1025
+    assert pa.fp16_round_rational(2051, 2) == 1026.0          # 1025.5: between 1025 and 1026
+    assert pa.fp16_round_rational(3, 1 << 25) == 2.0 ** -23   # 1.5 * 2^-24
+    assert pa.fp16_round_rational(1, 1 << 25) == 0.0          # 0.5 * 2^-24
+    assert pa.fp16_round_rational(1, 3) == float(np.float16(1 / 3))
+
+
+def test_plain_rule_closed_forms():
+    kb = f16([[1.0, 1024.0, 5.0, -7.0], [2.0, 1025.0, 5.0, -7.0]])
+    m = pa.block_pseudo_average(kb, "plain").astype(np.float64)
+    assert m[0] == 1.5          # exact mean, representable
+    assert m[1] == 1024.0       # 1024.5 rounds to the even neighbour
+    assert m[2] == 5.0 and m[3] == -7.0
+    # where the exact mean is on the grid of the block maximum the two readings agree
+    kb = f16(np.arange(-8, 8).reshape(16, 1) * np.ones((1, 3)))
+    np.testing.assert_array_equal(pa.block_pseudo_average(kb, "plain"), pa.block_pseudo_average(kb, "grid"))
+    # and they differ where the mean falls between grid points of the maximum: values
+    # {1000, 0.25}: mean 500.125, grid of 1000 is 0.5 (-> 500.0), fp16 spacing at 500 is
+    # 0.25 (-> 500.0 as well; a tie to even); {1000, 0.75}: mean 500.375 -> grid 500.5,
+    # plain 500.5 (tie, even); {1000, 1.5}: mean 500.75 -> grid 501.0 (tie at 0.5 spacing
+    # 500.5 / 501.0 -> even 501.0), plain 500.75
+    kb = f16([[1000.0], [1.5]])
+    assert float(pa.block_pseudo_average(kb, "grid")[0]) == 501.0
+    assert float(pa.block_pseudo_average(kb, "plain")[0]) == 500.75
+
+
+def test_plain_rule_guard_and_tail():
+    kb = f16(np.array([[40000.0, 1.0, np.inf], [-30000.0, 3.0, 2.0]]))
+    m = pa.block_pseudo_average(kb, "plain").astype(np.float64)
+    assert m[0] == 0.0 and m[1] == 2.0 and m[2] == 0.0
+    rng = np.random.default_rng(12)
+    k = f16(rng.standard_normal((2, 2, 250, 8)) * 3 + 40)
+    ks, means = pa.kshift(k, block_rows=112, rule="plain")
+    for b in range(2):
+        for h in range(2):
+            for j, (r0, r1) in enumerate([(0, 112), (112, 224), (224, 250)]):
+                ex = k[b, h, r0:r1].astype(np.float64).mean(axis=0)   # exact enough for the bound
+                mj = means[b, h, j].astype(np.float64)
+                spacing = np.abs(np.nextafter(means[b, h, j], np.float16(np.inf)).astype(np.float64) - mj)
+                assert np.all(np.abs(mj - ex) <= spacing)
+
+
+def test_plain_rule_fast_equals_exact():
+    rng = np.random.default_rng(13)
+    for scale, bias in [(1.0, 0.0), (3.0, 40.0), (1e-4, 0.0), (200.0, 3000.0)]:
+        k = f16(rng.standard_normal((1, 3, 300, 16)) * scale + bias * rng.standard_normal((1, 3, 1, 16)))
+        ks1, m1 = pa.kshift(k, block_rows=128, rule="plain")
+        ks2, m2 = pa.kshift_fast(k, block_rows=128, rule="plain")
+        np.testing.assert_array_equal(m1.view(np.uint16), m2.view(np.uint16))
+        np.testing.assert_array_equal(ks1.view(np.uint16), ks2.view(np.uint16))
+
+
+def test_grid_rule_keeps_more_shifted_keys_exact_than_plain():
+    # the reason for the grid reading: K - m stays exact in fp16 where the plain mean has
+    # bits below the keys' own spacing (a mean near zero: unbiased or resonance keys)
+    rng = np.random.default_rng(14)
+    t = np.arange(512)[None, None, :, None]
+    cases = {
+        "iid": rng.standard_normal((1, 4, 512, 64)),
+        "resonance": 30 * np.sin(t * rng.uniform(0, np.pi, (1, 4, 1, 64)) + rng.uniform(0, 6.3, (1, 4, 1, 64)))
+        + rng.normal(0, 0.5, (1, 4, 512, 64)),
+        "bias20": rng.standard_normal((1, 4, 512, 64)) + rng.normal(0, 20, (1, 4, 1, 64)),
+    }
+    for name, x in cases.items():
+        k = f16(x)
+        frac = {}
+        for rule in ("grid", "plain"):
+            ks, means = pa.kshift_fast(k, block_rows=128, rule=rule)
+            exact = ks.astype(np.float64) == k.astype(np.float64) - np.repeat(means.astype(np.float64), 128, axis=2)
+            frac[rule] = exact.mean()
+        assert frac["grid"] > 0.85, (name, frac)
+        assert frac["grid"] >= frac["plain"], (name, frac)
+        if name != "bias20":
+            assert frac["plain"] < 0.5, (name, frac)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_plain_rule_shift_then_recover_equals_plain_attention(oracle_mod, causal):
+    rng = np.random.default_rng(15)
+    q = f16(rng.integers(-3, 4, (1, 4, 40, 16)))
+    k = f16(rng.integers(-20, 21, (1, 2, 230, 16)) + rng.integers(-100, 100, (1, 2, 1, 16)))
+    v = f16(rng.standard_normal((1, 2, 230, 16)))
+    ks, means = pa.kshift(k, block_rows=112, rule="plain")
+    o0, l0 = oracle_mod.attention(q, k, v, causal=causal, scale=0.05)
+    o1, l1 = oracle_mod.attention_recovered(q, ks, means, 112, v, causal=causal, scale=0.05)
+    # K - m may be inexact here (m off the integer grid): agreement to the fp16 rounding of K'
+    np.testing.assert_allclose(o1, o0, rtol=0, atol=5e-3)
+    np.testing.assert_allclose(l1, l0, rtol=0, atol=5e-3)
