@@ -173,6 +173,24 @@ int pasa_attn_fwd_shifted(const void* q, const void* k_shifted, const void* mean
  */
 int pasa_kshift(const void* k, void* k_shifted, void* means, int B, int H, int Sk, int D, void* stream);
 
+/* Rules for the block average (the `mean_rule` argument of pasa_kshift_mean). */
+#define PASA_MEAN_GRID 0   /* the pseudo-average of pasa_kshift (the library's reading) */
+#define PASA_MEAN_PLAIN 1  /* the exact block mean rounded once to fp16 (ties to even) */
+
+/*
+ * pasa_kshift with a choice of the Abstract's undefined "pseudo-average". PASA_MEAN_GRID
+ * is pasa_kshift itself. PASA_MEAN_PLAIN writes m_j[d] = fp16_rn(sum_r k[r,d] / n), the
+ * plain fp16-rounded mean of the block's n valid rows, with the same guard (m = 0 when
+ * max |k| >= 32768 or the block/channel holds inf or NaN) and the same shift
+ * k_shifted = fp16_rn(k - m). Both keep attention exact up to rounding, since the offsets
+ * q . m_j are added back; they differ in how often k - m is exact in fp16 (the grid reading
+ * keeps it exact far more often when the mean is small against the block maximum). The
+ * output feeds pasa_attn_fwd_shifted / pasa_attn_fwd_decode unchanged. Other arguments and
+ * errors as pasa_kshift; an unknown rule is PASA_ERR_UNSUPPORTED.
+ */
+int pasa_kshift_mean(const void* k, void* k_shifted, void* means, int B, int H, int Sk, int D, int mean_rule,
+                     void* stream);
+
 /*
  * Key preparation of the FP8 score modes (D = 128): per key block j of 128 rows, with
  * a = max |x| over the block (all channels) of x = K' (mode 5, PASA_MODE_SHIFT_FP8: the

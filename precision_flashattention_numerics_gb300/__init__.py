@@ -29,6 +29,8 @@ MODE_NOSHIFT_F32ACC = 3
 MODE_SHIFT_F16ALL = 4   # mode 0 with an fp16 PV accumulator and an fp16 running row sum
 MODE_SHIFT_FP8 = 5      # e4m3 Q and shifted keys, fp32 score accumulation (D = 128)
 MODE_NAIVE_FP8 = 6      # e4m3 Q and raw keys, no shift (D = 128)
+MEAN_GRID = 0           # block average rules for kshift
+MEAN_PLAIN = 1
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_HERE, "libpasa.so")
@@ -46,6 +48,7 @@ SIGNATURES = {
     "pasa_attn_fwd_stats": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P], _I),
     "pasa_attn_fwd_shifted": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P], _I),
     "pasa_kshift": ([_P, _P, _P, _I, _I, _I, _I, _P], _I),
+    "pasa_kshift_mean": ([_P, _P, _P, _I, _I, _I, _I, _I, _P], _I),
     "pasa_kprep_fp8": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _P], _I),
     "pasa_attn_fwd_fp8": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P], _I),
     "pasa_kshift_blocks": ([_P, _P, _P, _I, _I, _I, _I, _I, _I, _P], _I),
@@ -209,8 +212,9 @@ def attn_fwd_shifted(q, k_shifted, means, v, causal: bool = False, scale: float 
     return out, lse
 
 
-def kshift(k, out=None, means=None):
-    """The pseudo-average shift step alone: returns (k_shifted [B,H,Sk,D], means [B,H,nb,D])."""
+def kshift(k, out=None, means=None, mean_rule: int = 0):
+    """The pseudo-average shift step alone: returns (k_shifted [B,H,Sk,D], means [B,H,nb,D]).
+    mean_rule: MEAN_GRID (0, the pseudo-average) or MEAN_PLAIN (1, the fp16-rounded mean)."""
     lib = library()
     _check(k, "k")
     B, H, Sk, D = k.shape
@@ -219,7 +223,10 @@ def kshift(k, out=None, means=None):
     ks = torch.empty_like(k) if out is None else out
     if means is None:
         means = torch.empty((B, H, nb, D), device=k.device, dtype=torch.float16)
-    rc = lib.pasa_kshift(_ptr(k), _ptr(ks), _ptr(means), B, H, Sk, D, _stream())
+    if mean_rule == MEAN_GRID:
+        rc = lib.pasa_kshift(_ptr(k), _ptr(ks), _ptr(means), B, H, Sk, D, _stream())
+    else:
+        rc = lib.pasa_kshift_mean(_ptr(k), _ptr(ks), _ptr(means), B, H, Sk, D, int(mean_rule), _stream())
     if rc != 0:
         raise PasaError(rc, "pasa_kshift")
     return ks, means

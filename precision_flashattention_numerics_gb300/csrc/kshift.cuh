@@ -16,6 +16,12 @@
 //
 // m lies on the grid of the block maximum, so K - m is exact in fp16 for most elements.
 //
+// PLAIN (the alternative reading, fp16 output only): m = fp16_rn(exact mean of the n
+// values). Every fp16 value is an integer multiple of 2^-24 below 2^15, so the block sum S
+// is an exact 64-bit integer in units of 2^-24; fp16_rn(fp64(S / n) * 2^-24) is one
+// rounding of the exact mean, because an exact mean that is not an fp16 tie lies at least
+// 2^-32 from every tie while the fp64 division errs by at most 2^-38. The guard is the same.
+//
 // FP8 score modes: the same kernel can instead write e4m3 codes of K' (or of the raw keys,
 // without the shift) with one scale per block: a = max |K'| over the block (all channels),
 // inv = fp32(448 / a), code = e4m3_rn_satfinite(fp32(K' * inv)), scale = fp32(a / 448)
@@ -61,7 +67,7 @@ __device__ __forceinline__ int rne_div(int s, int n) {
   return s < 0 ? -q : q;
 }
 
-template <int D, int BN, int OUT = kShiftF16>
+template <int D, int BN, int OUT = kShiftF16, bool PLAIN = false>
 __global__ void __launch_bounds__(kShiftThreads)
 kshift_kernel(const __half* __restrict__ k, void* __restrict__ kshift, __half* __restrict__ means,
               float* __restrict__ kscale, int Sk, int nb, int j0, int cap, int nb_cap) {
@@ -74,7 +80,9 @@ kshift_kernel(const __half* __restrict__ k, void* __restrict__ kshift, __half* _
 
   __shared__ uint32_t sh_max[NW][U][4];
   __shared__ uint32_t sh_nf[NW][U][4];
+  static_assert(!PLAIN || OUT == kShiftF16, "the plain-mean reading has the fp16 output only");
   __shared__ int sh_sum[NW][U][8];
+  __shared__ long long sh_sum64[PLAIN ? NW : 1][U][8];
   __shared__ uint32_t sh_amax[NW];
 
   // blocks [j0, nb) of the Sk valid rows; planes are cap rows (means: nb_cap blocks) apart.
@@ -152,26 +160,49 @@ kshift_kernel(const __half* __restrict__ k, void* __restrict__ kshift, __half* _
     inv_g[h] = __int_as_float((127 - e) << 23);
     guard[h] = (E >= 30) || (((nf[h / 2] >> (16 * (h & 1))) & 0xFFFFu) != 0);
   }
-  int sum[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  if constexpr (PLAIN) {
+    // exact sums in units of 2^-24 (f * 2^24 is exact in fp32: an fp16 value has 11 bits)
+    long long sum[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
-  for (int i = 0; i < RPT; ++i) {
-    const __half* hv = reinterpret_cast<const __half*>(&x[i]);
+    for (int i = 0; i < RPT; ++i) {
+      const __half* hv = reinterpret_cast<const __half*>(&x[i]);
 #pragma unroll
-    for (int h = 0; h < 8; ++h) {
-      const float f = __half2float(hv[h]);
-      // rows >= n hold zeros; non-finite values only occur in guarded channels
-      const float t = isfinite(f) ? f * inv_g[h] : 0.0f;  // exact: power-of-two scale
-      sum[h] += __float2int_rn(t);
+      for (int h = 0; h < 8; ++h) {
+        const float f = __half2float(hv[h]);
+        sum[h] += isfinite(f) ? __float2ll_rn(f * 16777216.0f) : 0ll;
+      }
     }
-  }
 #pragma unroll
-  for (int off = U; off < 32; off *= 2) {
+    for (int off = U; off < 32; off *= 2) {
 #pragma unroll
-    for (int h = 0; h < 8; ++h) sum[h] += __shfl_xor_sync(0xffffffffu, sum[h], off);
-  }
-  if ((tid % 32) < U) {
+      for (int h = 0; h < 8; ++h) sum[h] += __shfl_xor_sync(0xffffffffu, sum[h], off);
+    }
+    if ((tid % 32) < U) {
 #pragma unroll
-    for (int h = 0; h < 8; ++h) sh_sum[warp][u][h] = sum[h];
+      for (int h = 0; h < 8; ++h) sh_sum64[warp][u][h] = sum[h];
+    }
+  } else {
+    int sum[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+      const __half* hv = reinterpret_cast<const __half*>(&x[i]);
+#pragma unroll
+      for (int h = 0; h < 8; ++h) {
+        const float f = __half2float(hv[h]);
+        // rows >= n hold zeros; non-finite values only occur in guarded channels
+        const float t = isfinite(f) ? f * inv_g[h] : 0.0f;  // exact: power-of-two scale
+        sum[h] += __float2int_rn(t);
+      }
+    }
+#pragma unroll
+    for (int off = U; off < 32; off *= 2) {
+#pragma unroll
+      for (int h = 0; h < 8; ++h) sum[h] += __shfl_xor_sync(0xffffffffu, sum[h], off);
+    }
+    if ((tid % 32) < U) {
+#pragma unroll
+      for (int h = 0; h < 8; ++h) sh_sum[warp][u][h] = sum[h];
+    }
   }
   __syncthreads();
 
@@ -180,12 +211,20 @@ kshift_kernel(const __half* __restrict__ k, void* __restrict__ kshift, __half* _
   __half mh[8];
 #pragma unroll
   for (int h = 0; h < 8; ++h) {
-    int s = 0;
+    if constexpr (PLAIN) {
+      long long s = 0;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) s += sh_sum[w][u][h];
-    const int mu = rne_div(s, n);
-    mf[h] = (guard[h] || OUT == kRawFp8) ? 0.0f : static_cast<float>(mu) * g[h];  // exact, an fp16 value
-    mh[h] = __float2half_rn(mf[h]);
+      for (int w = 0; w < NW; ++w) s += sh_sum64[w][u][h];
+      mh[h] = guard[h] ? __float2half_rn(0.0f) : __double2half(static_cast<double>(s) / n * 0x1p-24);
+      mf[h] = __half2float(mh[h]);
+    } else {
+      int s = 0;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) s += sh_sum[w][u][h];
+      const int mu = rne_div(s, n);
+      mf[h] = (guard[h] || OUT == kRawFp8) ? 0.0f : static_cast<float>(mu) * g[h];  // exact, an fp16 value
+      mh[h] = __float2half_rn(mf[h]);
+    }
   }
   if (OUT != kRawFp8 && rg == 0) {
     uint4 mv;

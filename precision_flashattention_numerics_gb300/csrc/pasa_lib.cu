@@ -95,14 +95,14 @@ WorkspaceLayout workspace_layout(int B, int Hkv, int Sk, int D, int mode) {
   return w;
 }
 
-template <int D, int OUT>
+template <int D, int OUT, bool PLAIN = false>
 int launch_kshift(const void* k, void* ks, void* means, float* kscale, int B, int H, int Sk, cudaStream_t st,
                   int first_block = 0, int cap = 0) {
   constexpr int BN = pasa::block_rows_for(D);
   const int nb = (Sk + BN - 1) / BN;
   if (cap <= 0) cap = Sk;
   dim3 grid(nb - first_block, B * H);
-  pasa::kshift_kernel<D, BN, OUT><<<grid, pasa::kShiftThreads, 0, st>>>(
+  pasa::kshift_kernel<D, BN, OUT, PLAIN><<<grid, pasa::kShiftThreads, 0, st>>>(
       static_cast<const __half*>(k), ks, static_cast<__half*>(means), kscale, Sk, nb, first_block, cap,
       (cap + BN - 1) / BN);
   cudaError_t e = cudaGetLastError();
@@ -261,6 +261,22 @@ int pasa_kshift(const void* k, void* k_shifted, void* means, int B, int H, int S
   if (rc != PASA_OK) return rc;
   return kshift_dispatch(k, k_shifted, means, nullptr, B, H, Sk, D, PASA_MODE_SHIFT_F16ACC,
                          static_cast<cudaStream_t>(stream));
+}
+
+int pasa_kshift_mean(const void* k, void* k_shifted, void* means, int B, int H, int Sk, int D, int mean_rule,
+                     void* stream) {
+  if (mean_rule == PASA_MEAN_GRID) return pasa_kshift(k, k_shifted, means, B, H, Sk, D, stream);
+  if (mean_rule != PASA_MEAN_PLAIN) return PASA_ERR_UNSUPPORTED;
+  if (!k || !k_shifted || !means) return PASA_ERR_NULLPTR;
+  if (B <= 0 || H <= 0 || Sk <= 0) return PASA_ERR_SHAPE;
+  if (D != 64 && D != 128) return PASA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * H > 65535) return PASA_ERR_SHAPE;  // grid.y
+  if (!aligned16(k) || !aligned16(k_shifted) || !aligned16(means)) return PASA_ERR_ALIGN;
+  int rc = check_device();
+  if (rc != PASA_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return D == 64 ? launch_kshift<64, pasa::kShiftF16, true>(k, k_shifted, means, nullptr, B, H, Sk, st)
+                 : launch_kshift<128, pasa::kShiftF16, true>(k, k_shifted, means, nullptr, B, H, Sk, st);
 }
 
 int pasa_kprep_fp8(const void* k, void* k8, void* means, float* kscale, int B, int H, int Sk, int D, int mode,

@@ -86,6 +86,14 @@ def test_argument_errors(lib):
 
 def test_kshift_argument_errors(lib):
     P = ctypes.c_void_p
+    # pasa_kshift_mean(k, k_shifted, means, B, H, Sk, D, mean_rule, stream)
+    assert lib.pasa_kshift_mean(P(FAKE), P(FAKE), P(FAKE), 1, 1, 64, 64, 2, None) == -3
+    assert lib.pasa_kshift_mean(P(FAKE), P(FAKE), P(FAKE), 1, 1, 64, 64, -1, None) == -3
+    assert lib.pasa_kshift_mean(None, P(FAKE), P(FAKE), 1, 1, 64, 64, 1, None) == -1
+    assert lib.pasa_kshift_mean(P(FAKE), P(FAKE), P(FAKE), 1, 1, 64, 96, 1, None) == -3
+    assert lib.pasa_kshift_mean(P(FAKE_MIS), P(FAKE), P(FAKE), 1, 1, 64, 64, 1, None) == -4
+    assert lib.pasa_kshift_mean(P(FAKE), P(FAKE), P(FAKE), 1, 1, 64, 64, 0, None) == lib.pasa_kshift(
+        P(FAKE), P(FAKE), P(FAKE), 1, 1, 64, 64, None)   # rule 0 is pasa_kshift (no device here)
     assert lib.pasa_kshift(None, P(FAKE), P(FAKE), 1, 1, 64, 64, None) == -1
     assert lib.pasa_kshift(P(FAKE), P(FAKE), P(FAKE), 1, 1, 0, 64, None) == -2
     assert lib.pasa_kshift(P(FAKE), P(FAKE), P(FAKE), 1, 1, 64, 32, None) == -3

@@ -126,6 +126,20 @@ def test_single_split_against_the_prefill_kernel(g, Sq, D, causal, mode):
         assert (l1.double() - l2.double()).abs().max().item() <= (f16all_bound(Sk) if mode == 4 else 1e-4)
 
 
+def test_fp16_pv_decode_differs_from_fp32_pv():
+    """Mode 4 keeps O and the row sums in fp16: on flat attention (iid keys, 5000 cached)
+    its result must differ from mode 0 somewhere, and stay within the fp16 bound."""
+    p = pasa()
+    B, Hq, Hkv, Sq, Sk, D = 1, 8, 2, 1, 5000, 128
+    q, k, v = inputs(B, Hq, Hkv, Sq, Sk, D, "iid", 4242)
+    o0, _ = decode(q, k, v, True, 0)
+    o4, _ = decode(q, k, v, True, 4)
+    o_ref, _ = oracle.attention(q, k, v, causal=True)
+    assert not torch.equal(o0, o4)
+    d4 = np.abs(o4.double().cpu().numpy() - o_ref).max()
+    assert d4 <= 1e-2 * np.abs(o_ref).max() + f16all_bound(Sk) * float(np.abs(v.astype(np.float64)).max())
+
+
 @pytest.mark.parametrize("mode", [0, 3])
 def test_cache_rows_past_the_length_are_not_read(mode):
     """A cache of cap rows holding Sk valid ones: rows past Sk (here NaN, and means blocks
