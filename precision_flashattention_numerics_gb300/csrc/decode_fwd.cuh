@@ -31,7 +31,10 @@
 // Warp roles (192 threads): warps 0-3 softmax + epilogue; warp 4 TMA producer (Q once, K'_j
 // one block ahead of V_j, 16-block means chunks); warp 5 TMEM owner, one thread issuing
 // QK(j+1) before PV(j). Split keys (grid.y) as in attn_fwd_kernel: a split writes O / l in
-// fp32 and m + log2 l for combine_splits_kernel.
+// fp32 and m + log2 l for combine_splits_kernel; or, with `cluster`, the splits of a kv head
+// run as one thread-block cluster: each leaves its unnormalised O (in the shared memory of
+// its first K' slot), m and l, and after a cluster barrier the CTA of rank r merges the rows
+// q = r, r + splits, ... reading every split's values through distributed shared memory.
 //
 // Every wait is bounded (see ptx.cuh). The softmax warps meet at named barriers inside the
 // block loop, so after a failed wait they keep iterating (skipping the work, not the
@@ -60,6 +63,8 @@ struct DecodeParams {
   int bps;            // key blocks per split, 0 = one CTA per kv head
   int causal;
   float scale_log2;   // softmax scale * log2(e)
+  int cluster;        // 1: the splits of a kv head form one thread-block cluster (grid.y) and
+                      // merge their partial results through distributed shared memory
 };
 
 template <int NQ, int KST, int VST>
@@ -77,6 +82,7 @@ struct DecodeSmem {
   alignas(1024) uint8_t m[2][kMTile];
   alignas(16) float cv[2][kChunkBlocks][NQ];          // offsets q . m_j of a chunk, by chunk parity
   alignas(16) float red[2][4][NQ];                    // per-warp column maxima, by block parity
+  float cm[NQ], cl[NQ];                               // cluster merge: this split's m (log2) and l
   uint64_t q_full;
   uint64_t k_full[KST], k_empty[KST];
   uint64_t v_full[VST], v_empty[VST];
@@ -571,9 +577,22 @@ decode_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
     }
     const size_t rows_total = static_cast<size_t>(gridDim.x) * p.rows;
     const size_t row0 = static_cast<size_t>(plane) * p.rows;
+    if (p.cluster) {
+      // this split's unnormalised O (column q, dim t), m and l, for the cluster merge below;
+      // every load and MMA that used the first K' slot is done
+      float* po = reinterpret_cast<float*>(s.k[0]);
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        po[q * D + t] = ov[q];
+        if (t == q) {
+          s.cm[q] = lt[q] > 0.0f ? m_run[q] : -INFINITY;
+          s.cl[q] = lt[q];
+        }
+      }
+    }
 #pragma unroll
     for (int q = 0; q < NQ; ++q) {
-      if (q < p.rows) {
+      if (q < p.rows && !p.cluster) {
         const float inv_l = lt[q] > 0.0f ? 1.0f / lt[q] : 0.0f;
         const float val = ov[q] * inv_l;
         const float l2 = lt[q] > 0.0f ? m_run[q] + log2f(lt[q]) : -INFINITY;
@@ -587,6 +606,47 @@ decode_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
         }
       }
     }
+  }
+
+  if (p.cluster) {
+    // merge of the cluster's splits: O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,
+    // M = max_s m_s; LSE = ln 2 * (M + log2 of the denominator)
+    cluster_sync_all();
+    if (warp < 4) {
+      const int t = tid;
+      const int ns = static_cast<int>(gridDim.y);
+      const uint32_t po = smem_u32(s.k[0]), pm = smem_u32(s.cm), pl = smem_u32(s.cl);
+      const size_t row0 = static_cast<size_t>(plane) * p.rows;
+      for (int q = static_cast<int>(cluster_ctarank()); q < p.rows; q += ns) {
+        float ms[8], ls[8];
+        float M = -INFINITY;
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          ms[r] = -INFINITY;
+          ls[r] = 0.0f;
+          if (r < ns) {
+            ms[r] = ld_shared_cluster_f32(mapa_shared(pm + q * 4, r));
+            ls[r] = ld_shared_cluster_f32(mapa_shared(pl + q * 4, r));
+            if (ls[r] > 0.0f) M = fmaxf(M, ms[r]);
+          }
+        }
+        float num = 0.0f, den = 0.0f;
+        if (M != -INFINITY) {
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            if (r < ns && ls[r] > 0.0f) {
+              const float wgt = ex2_approx(ms[r] - M);
+              den = fmaf(wgt, ls[r], den);
+              num = fmaf(wgt, ld_shared_cluster_f32(mapa_shared(po + (q * D + t) * 4, r)), num);
+            }
+          }
+        }
+        p.o[(row0 + q) * D + t] = __float2half_rn(den > 0.0f ? num / den : 0.0f);
+        if (t == 0 && p.lse != nullptr)
+          p.lse[row0 + q] = den > 0.0f ? (M + log2f(den)) * 0.69314718055994531f : -INFINITY;
+      }
+    }
+    cluster_sync_all();   // no CTA leaves while another still reads its shared memory
   }
 
   tc_fence_before();

@@ -195,8 +195,23 @@ int launch_decode(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMa
   const int smem = static_cast<int>(sizeof(pasa::DecodeSmem<NQ, KST, VST>)) + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e);
-  kern<<<dim3(static_cast<unsigned>(planes), static_cast<unsigned>(splits)), pasa::kDecThreads, smem, st>>>(mq, mk, mv,
-                                                                                                           mm, p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(planes), static_cast<unsigned>(splits));
+  cfg.blockDim = dim3(pasa::kDecThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  if (p.cluster) {
+    // the splits of a kv head as one cluster (at most 8: the portable cluster size)
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = static_cast<unsigned>(splits);
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mm, p);
+  if (e != cudaSuccess) return cuda_fail(e);
   e = cudaGetLastError();
   return e == cudaSuccess ? PASA_OK : cuda_fail(e);
 }
@@ -401,10 +416,16 @@ static int decode_split(int B, int Hkv, int Sk, int D, int splits_req, int* spli
   return splits > 1 ? bps : 0;
 }
 
+// The swapped-operand decode kernel merges up to 8 splits of a kv head inside one cluster.
+static bool decode_cluster_merge(int D, long long rows, int splits) {
+  return D == 128 && rows <= 32 && splits >= 2 && splits <= 8;
+}
+
 size_t pasa_attn_fwd_decode_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D, int splits) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Sk <= 0 || Hq % Hkv != 0 || pasa::block_rows_for(D) == 0) return 0;
   int sp = 1;
   if (decode_split(B, Hkv, Sk, D, splits, &sp) == 0) return 0;
+  if (decode_cluster_merge(D, static_cast<long long>(Hq / Hkv) * Sq, sp)) return 0;
   const size_t rows = static_cast<size_t>(B) * Hq * Sq;
   return align_up(static_cast<size_t>(sp) * rows * D * 4, 256) + align_up(static_cast<size_t>(sp) * rows * 4, 256);
 }
@@ -424,7 +445,8 @@ int pasa_attn_fwd_decode(const void* q, const void* k_shifted, const void* means
   int sp = 1;
   const int bps = decode_split(B, Hkv, Sk, D, splits, &sp);
   const size_t need = pasa_attn_fwd_decode_workspace_bytes(B, Hq, Hkv, Sq, Sk, D, splits);
-  if (bps > 0) {
+  const bool cluster = bps > 0 && decode_cluster_merge(D, static_cast<long long>(g) * Sq, sp);
+  if (bps > 0 && !cluster) {
     if (!workspace || workspace_bytes < need) return PASA_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PASA_ERR_ALIGN;
   }
@@ -440,7 +462,7 @@ int pasa_attn_fwd_decode(const void* q, const void* k_shifted, const void* means
   const size_t nrows = static_cast<size_t>(B) * Hq * Sq;
   float* part_o = nullptr;
   float* part_lse = nullptr;
-  if (bps > 0) {
+  if (bps > 0 && !cluster) {
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     part_o = reinterpret_cast<float*>(ws);
     part_lse = reinterpret_cast<float*>(ws + align_up(static_cast<size_t>(sp) * nrows * D * 4, 256));
@@ -471,6 +493,7 @@ int pasa_attn_fwd_decode(const void* q, const void* k_shifted, const void* means
     dp.bps = bps;
     dp.causal = causal ? 1 : 0;
     dp.scale_log2 = scale * 1.4426950408889634f;
+    dp.cluster = cluster ? 1 : 0;
     rc = nq == 16 ? decode_dispatch<16>(mode, mq, mk, mv, mmeans, dp, planes, sp, st)
                   : decode_dispatch<32>(mode, mq, mk, mv, mmeans, dp, planes, sp, st);
   } else {
@@ -498,7 +521,7 @@ int pasa_attn_fwd_decode(const void* q, const void* k_shifted, const void* means
     rc = D == 64 ? attn_dispatch<64, false>(mode, causal, mq, mk, mv, mo, mmeans, p, st)
                  : attn_dispatch<128, false>(mode, causal, mq, mk, mv, mo, mmeans, p, st);
   }
-  if (rc != PASA_OK || bps == 0) return rc;
+  if (rc != PASA_OK || bps == 0 || cluster) return rc;
   const unsigned cblocks = static_cast<unsigned>((nrows + 7) / 8);
   if (D == 64)
     pasa::combine_splits_kernel<64><<<cblocks, 256, 0, st>>>(part_o, part_lse, sp, static_cast<long long>(nrows),

@@ -164,11 +164,14 @@ def test_decode_entry_points_check_arguments(lib):
     assert dec(splits=-1) == -3
     assert dec(means=0) == -1                  # the shift modes read the block means
     assert dec(means=FAKE_MIS) == -4
-    assert dec(mode=3, means=0) == -7          # 40 key blocks split: the partials need a workspace
-    need = lib.pasa_attn_fwd_decode_workspace_bytes(1, 8, 1, 1, 5000, 128, 0)
+    # 40 key blocks in 10 splits: more than one cluster holds, so the partials need a workspace
+    assert dec(mode=3, means=0, splits=10) == -7
+    need = lib.pasa_attn_fwd_decode_workspace_bytes(1, 8, 1, 1, 5000, 128, 10)
     assert need > 0
-    assert dec(ws=FAKE, ws_bytes=need - 1) == -7
-    assert dec(ws=FAKE + 16, ws_bytes=need) == -4   # 256-byte aligned
+    assert dec(splits=10, ws=FAKE, ws_bytes=need - 1) == -7
+    assert dec(splits=10, ws=FAKE + 16, ws_bytes=need) == -4   # 256-byte aligned
+    # up to 8 splits of at most 32 packed rows at D = 128 merge inside a cluster: no workspace
+    assert lib.pasa_attn_fwd_decode_workspace_bytes(1, 8, 1, 1, 5000, 128, 8) == 0
     # pasa_kshift_blocks(k, k_shifted, means, B, H, Sk, Sk_cap, D, first_block, stream)
     kb = lib.pasa_kshift_blocks
     assert kb(None, P(FAKE), P(FAKE), 1, 1, 300, 300, 128, 0, None) == -1
@@ -191,12 +194,15 @@ def test_decode_workspace_bytes(lib):
         sp = -(-nb // bps)
         if sp == 1:
             return 0
+        if D == 128 and (Hq // Hkv) * Sq <= 32 and sp <= 8:
+            return 0      # merged inside a thread-block cluster
         rows = B * Hq * Sq
         a = lambda x: -(-x // 256) * 256
         return a(sp * rows * D * 4) + a(sp * rows * 4)
 
     for args in [(1, 8, 8, 1, 32768, 128, 0), (8, 28, 4, 1, 32768, 128, 0), (1, 8, 8, 1, 640, 128, 0),
                  (4, 32, 8, 4, 8192, 64, 0), (1, 8, 8, 1, 32768, 128, 5), (1, 28, 4, 1, 131072, 128, 0),
-                 (1, 8, 8, 1, 128, 128, 0), (1, 2, 1, 64, 777, 128, 100), (200, 8, 1, 1, 4096, 128, 0)]:
+                 (1, 8, 8, 1, 128, 128, 0), (1, 2, 1, 64, 777, 128, 100), (200, 8, 1, 1, 4096, 128, 0),
+                 (1, 8, 1, 1, 5000, 128, 12), (2, 28, 4, 4, 3001, 128, 0), (1, 16, 2, 8, 2049, 64, 0)]:
         assert lib.pasa_attn_fwd_decode_workspace_bytes(*args) == expect(*args), args
     assert lib.pasa_attn_fwd_decode_workspace_bytes(1, 3, 2, 1, 100, 128, 0) == 0   # Hq % Hkv != 0

@@ -6,7 +6,8 @@ keys live in a cache; the pseudo-average of a key block depends on that block's 
 alone, so the shifted cache and its block means stay valid as rows are appended, and only
 the block that an append touches is recomputed (pasa_kshift_blocks). pasa_attn_fwd_decode
 packs the g query heads of a kv group into one tile and splits the key blocks across CTAs;
-the split results are merged by their log-sum-exps. The result must be attention up to
+the split results are merged by their log-sum-exps (inside a thread-block cluster for up
+to 8 splits at D = 128, else by a second kernel). The result must be attention up to
 rounding: the same gates as the prefill parity tests, against the same fp64 oracle.
 """
 import numpy as np
@@ -70,6 +71,8 @@ CASES = [
     (1, 2, 1, 64, 777, 128, True, "iid", {}, 100),                      # 128 packed rows, a split per block
     (3, 6, 3, 1, 130, 128, True, "iid", {}, 0),                         # two blocks: unsplit
     (1, 4, 2, 2, 20000, 128, True, "kbias", {"bias_std": 20.0}, 0),
+    (1, 8, 1, 1, 5000, 128, True, "kbias", {"bias_std": 20.0}, 12),     # > 8 splits: the merge kernel
+    (2, 14, 2, 2, 3000, 128, True, "iid", {}, 8),                       # 8 splits: one cluster of 8
 ]
 
 
