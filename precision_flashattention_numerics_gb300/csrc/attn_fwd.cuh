@@ -505,12 +505,24 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
       float mx, mn = 0.0f;
       if constexpr (F16ACC) {
         if constexpr (STATS) {
-          uint32_t tmp[kPairs];
+          // block min in eight f16x2 accumulators (+inf where masked)
+          auto masked = [&](int c) {
+            return ((2 * c < cmax) ? (hp[c] & 0xFFFFu) : 0x7C00u) |
+                   ((2 * c + 1 < cmax) ? (hp[c] & 0xFFFF0000u) : 0x7C000000u);
+          };
+          uint32_t tmp[8];
+          if (cmax >= BN) {   // no key of the block is masked for this row
 #pragma unroll
-          for (int c = 0; c < kPairs; ++c)
-            tmp[c] = ((2 * c < cmax) ? (hp[c] & 0xFFFFu) : 0x7C00u) |
-                     ((2 * c + 1 < cmax) ? (hp[c] & 0xFFFF0000u) : 0x7C000000u);  // +inf when masked
-          const uint32_t n1 = tree_h2<kPairs, false>(tmp);
+            for (int k = 0; k < 8; ++k) tmp[k] = hp[k];
+#pragma unroll
+            for (int c = 8; c < kPairs; ++c) tmp[c & 7] = hmin2(tmp[c & 7], hp[c]);
+          } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) tmp[k] = masked(k);
+#pragma unroll
+            for (int c = 8; c < kPairs; ++c) tmp[c & 7] = hmin2(tmp[c & 7], masked(c));
+          }
+          const uint32_t n1 = tree_h2<8, false>(tmp);
           mn = fminf(half_lo_to_float(n1), half_lo_to_float(n1 >> 16));
         }
         if (cmax < BN) {
