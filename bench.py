@@ -45,17 +45,17 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one attention-kernel launch,
 # from an ncu capture of a quarter of the 32K workload (7 of 28 query heads, 1 of 4 kv heads:
-# 75.65 MB read + 24.45 MB written) scaled x4 to a full launch; the traffic is per head, so it
+# 75.63 MB read + 24.46 MB written) scaled x4 to a full launch; the traffic is per head, so it
 # grows in proportion. Summary and command: profiles/attn_fwd_kbias10_t3_b1h7g1_s32768_full.md.
 # Reported only while the kernel source is the one the counters were taken on.
 TRAFFIC_WORKLOAD = "kbias10_t3_b1h28g4_s32768_d128_causal"
 TRAFFIC_MODE = 0
-TRAFFIC_BYTES = 4 * (75.650304e6 + 24.449280e6)
-TRAFFIC_KERNEL_SHA = "6f9b9da0b6ed3e12"
+TRAFFIC_BYTES = 4 * (75.631872e6 + 24.462592e6)
+TRAFFIC_KERNEL_SHA = "ae9385673b602f59"
 # The same for one decode-kernel launch on the decode workload (captured at full size:
-# 539.11 MB read + 3.19 MB written); profiles/decode_fwd_kbias10_t3_b8h28g4_q1_s32768_full.md.
-DECODE_TRAFFIC_BYTES = 539106560 + 3187456
-DECODE_TRAFFIC_SHA = "5245f38722c68c80"
+# 539.11 MB read + 3.16 MB written); profiles/decode_fwd_kbias10_t3_b8h28g4_q1_s32768_full.md.
+DECODE_TRAFFIC_BYTES = 539112960 + 3155968
+DECODE_TRAFFIC_SHA = "4d577a9029edc3b8"
 
 
 def _source_sha(name):
