@@ -53,9 +53,9 @@ TRAFFIC_MODE = 0
 TRAFFIC_BYTES = 4 * (75.631872e6 + 24.462592e6)
 TRAFFIC_KERNEL_SHA = "ae9385673b602f59"
 # The same for one decode-kernel launch on the decode workload (captured at full size:
-# 539.11 MB read + 3.16 MB written); profiles/decode_fwd_kbias10_t3_b8h28g4_q1_s32768_full.md.
-DECODE_TRAFFIC_BYTES = 539112960 + 3155968
-DECODE_TRAFFIC_SHA = "4d577a9029edc3b8"
+# 539.11 MB read + 3.06 MB written); profiles/decode_fwd_kbias10_t3_b8h28g4_q1_s32768_full.md.
+DECODE_TRAFFIC_BYTES = 539113984 + 3058688
+DECODE_TRAFFIC_SHA = "7554aed3cf7c75ba"
 
 
 def _source_sha(name):
@@ -334,9 +334,14 @@ def bench_decode(args, w: wl.Workload, local_rank: int, sampler=None):
     dev = torch.device("cuda", local_rank)
     q, k, v = wl.make_inputs(w)
     qt, kt, vt = (torch.from_numpy(x).to(dev) for x in (q, k, v))
-    mode = args.mode if args.mode in MODE_NAMES and args.mode not in FP8_MODES else 0
+    mode = args.mode if args.mode in MODE_NAMES else 0
     shift = mode in SHIFT_MODES
-    ks, means = pasa.kshift(kt) if shift else (kt, None)
+    fp8 = mode in FP8_MODES
+    kscale = None
+    if fp8:   # e4m3 cache: codes, block scales, means (mode 5)
+        ks, means, kscale = pasa.kprep_fp8(kt, mode=mode)
+    else:
+        ks, means = pasa.kshift(kt) if shift else (kt, None)
     o = torch.empty_like(qt)
     lse = torch.empty((w.B, w.Hq, w.Sq), device=dev, dtype=torch.float32)
     nbytes = pasa.decode_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D)
@@ -346,11 +351,17 @@ def bench_decode(args, w: wl.Workload, local_rank: int, sampler=None):
     stream = torch.cuda.current_stream()
 
     def refresh():
-        if shift:
+        if fp8:
+            pasa.kprep_fp8_blocks(kt, ks, means, kscale, last, mode=mode)
+        elif shift:
             pasa.kshift_blocks(kt, ks, means, last)
 
     def attend():
-        pasa.attn_fwd_decode(qt, ks, means, vt, causal=w.causal, mode=mode, out=o, lse=lse, workspace=ws)
+        if fp8:
+            pasa.attn_fwd_decode_fp8(qt, ks, means, kscale, vt, causal=w.causal, mode=mode, out=o, lse=lse,
+                                     workspace=ws)
+        else:
+            pasa.attn_fwd_decode(qt, ks, means, vt, causal=w.causal, mode=mode, out=o, lse=lse, workspace=ws)
 
     for _ in range(max(3, args.warmup)):
         refresh()
@@ -377,16 +388,17 @@ def bench_decode(args, w: wl.Workload, local_rank: int, sampler=None):
     step_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][2]) for i in range(n))
     attn_ms = statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for i in range(n))
     nb = -(-w.Sk // bn)
-    # algorithmic bytes of the attention: the cache (K' or K, and V), the block means, q, o, lse
-    cache = 2 * w.B * w.Hkv * w.Sk * w.D * 2
-    moved = cache + (w.B * w.Hkv * nb * w.D * 2 if shift else 0) + 2 * w.B * w.Hq * w.Sq * w.D * 2 \
-        + w.B * w.Hq * w.Sq * 4
+    # algorithmic bytes of the attention: the cache (K' or K: fp16, or e4m3 codes and block
+    # scales; V fp16), the block means, q, o, lse
+    cache = w.B * w.Hkv * w.Sk * w.D * (1 if fp8 else 2) + w.B * w.Hkv * w.Sk * w.D * 2
+    moved = cache + (w.B * w.Hkv * nb * w.D * 2 if (shift or mode == 5) else 0) + (w.B * w.Hkv * nb * 4 if fp8 else 0) \
+        + 2 * w.B * w.Hq * w.Sq * w.D * 2 + w.B * w.Hq * w.Sq * 4
     gbs = moved / (attn_ms * 1e-3) / 1e9
     return {
         "workload": w.name, "mode": MODE_NAMES[mode], "tokens_per_s": round(w.B * w.Sq / (step_ms * 1e-3), 1),
         "ms_per_step": round(step_ms, 5), "attn_ms": round(attn_ms, 5), "host_ms_per_step": round(wall_ms, 5),
         "attn_bytes": moved, "attn_gbs": round(gbs, 1), "finite": bool(torch.isfinite(o).all().item()),
-        "launches_per_step": (1 if shift else 0) + (2 if nbytes else 1),
+        "launches_per_step": (1 if (shift or fp8) else 0) + (2 if nbytes else 1),
         "merge": "combine_splits_kernel" if nbytes else "in the decode kernel (thread-block cluster)",
     }
 
@@ -409,14 +421,15 @@ def decode_main(args, rank: int, world: int, local_rank: int):
         "metric": "PASA decode tokens/s at 1 GB300 (one new query row per head per step)",
         "value": dec["tokens_per_s"], "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": dec["ms_per_step"], "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3+f16" if args.mode in FP8_MODES else "f16",
+        "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk, "D": w.D,
                    "mode": dec["mode"], "l2": "the K/V cache (537 MB) is larger than L2; no flush"},
         "roofline": {"kernel": "decode_fwd_kernel" + (" + combine_splits_kernel" if dec["launches_per_step"] > 2
                                                         else ""), "bound": "hbm",
                      "achieved": dec["attn_gbs"], "peak": hbm, "unit": "GB/s",
                      "frac": round(dec["attn_gbs"] / hbm, 4),
-                     "traffic": measured_decode_traffic(args.mode if args.mode in (0, 1, 2, 3, 4) else 0),
+                     "traffic": measured_decode_traffic(args.mode),
                      "peak_source": f"{peak_src} copy bandwidth"},
         "gpu_launches": dec["launches_per_step"] * args.steps, "clocks": sampler.summary(),
         "finite_output": dec["finite"], "decode": dec,
@@ -492,8 +505,7 @@ def main():
             also[name] = {"tflops": round(ra["tflops"], 1), "ms_per_step": round(ra["ms_per_step"], 4),
                           "attn_ms": round(ra["attn_ms"], 4), "kshift_ms": round(ra["kshift_ms"], 4),
                           "finite": ra["finite"]}
-        if args.mode not in FP8_MODES:
-            also[DECODE_WORKLOAD] = bench_decode(args, wl.WORKLOADS[DECODE_WORKLOAD], local_rank)
+        also[DECODE_WORKLOAD] = bench_decode(args, wl.WORKLOADS[DECODE_WORKLOAD], local_rank)
 
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))  # fp16 dense = bf16 dense rate
     peak_note = f"{peak_src} bf16 dense burst (fp16 dense has the same nominal rate)"

@@ -250,7 +250,8 @@ size_t pasa_attn_fwd_decode_workspace_bytes(int B, int Hq, int Hkv, int Sq, int 
  * Decode attention on a key cache (the inference use of PASA, same citation as
  * pasa_kshift_blocks): a few new query rows per head against Sk cached keys, already
  * shifted by pasa_kshift / pasa_kshift_blocks (modes 0, 1, 4) or raw (modes 2, 3; means may
- * be NULL). The result equals pasa_attn_fwd_shifted's on the same arguments up to the
+ * be NULL; FP8 caches: pasa_attn_fwd_decode_fp8). The result equals pasa_attn_fwd_shifted's
+ * on the same arguments up to the
  * rounding: the split merge, and in the decode kernel the order of the row sums and the
  * offsets (fp32 dot products on the CUDA cores instead of the tensor cores).
  * Two changes of work layout serve the small Sq:
@@ -276,6 +277,34 @@ size_t pasa_attn_fwd_decode_workspace_bytes(int B, int Hq, int Hkv, int Sq, int 
 int pasa_attn_fwd_decode(const void* q, const void* k_shifted, const void* means, const void* v, void* o, float* lse,
                          int B, int Hq, int Hkv, int Sq, int Sk, int Sk_cap, int D, int causal, float scale, int mode,
                          int splits, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Decode on an FP8 key cache (modes 5 and 6; the FP8 score modes of pasa_attn_fwd_fp8 on
+ * the decode work layout of pasa_attn_fwd_decode). The cache holds e4m3 codes k8 [B, Hkv,
+ * Sk_cap, D] uint8 with one fp32 scale per 128-key block, kscale [B, Hkv,
+ * ceil(Sk_cap / 128)], as pasa_kprep_fp8 / pasa_kprep_fp8_blocks write them, plus (mode 5)
+ * the block means [B, Hkv, ceil(Sk_cap / 128), D] fp16; v fp16 [B, Hkv, Sk_cap, D]. The new
+ * query rows are quantised in the kernel exactly as in pasa_attn_fwd_fp8 (one scale per
+ * row). Only the swapped-operand decode kernel takes e4m3 keys: D = 128 and g * Sq <= 32,
+ * else PASA_ERR_UNSUPPORTED; kscale NULL is PASA_ERR_NULLPTR. Workspace, splits, causal
+ * mask and other arguments as pasa_attn_fwd_decode (pasa_attn_fwd_decode_workspace_bytes
+ * applies unchanged).
+ */
+int pasa_attn_fwd_decode_fp8(const void* q, const void* k8, const void* means, const float* kscale, const void* v,
+                             void* o, float* lse, int B, int Hq, int Hkv, int Sq, int Sk, int Sk_cap, int D, int causal,
+                             float scale, int mode, int splits, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * pasa_kprep_fp8 for key blocks [first_block, ceil(Sk / 128)) of a cache of Sk valid keys in
+ * Sk_cap allocated rows per head (the FP8 counterpart of pasa_kshift_blocks): after an
+ * append only the blocks it wrote into change. k fp16 [B, H, Sk_cap, D]; k8 uint8 [B, H,
+ * Sk_cap, D]; kscale fp32 [B, H, ceil(Sk_cap / 128)]; means (mode 5) fp16 [B, H,
+ * ceil(Sk_cap / 128), D]. Earlier blocks and rows past Sk are left untouched. Errors as
+ * pasa_kprep_fp8, plus PASA_ERR_SHAPE for first_block outside [0, ceil(Sk / 128)) or
+ * Sk_cap < Sk.
+ */
+int pasa_kprep_fp8_blocks(const void* k, void* k8, void* means, float* kscale, int B, int H, int Sk, int Sk_cap, int D,
+                          int mode, int first_block, void* stream);
 
 /*
  * Synchronise `stream` and read the device error word. Returns PASA_OK, PASA_ERR_TIMEOUT

@@ -54,6 +54,9 @@ SIGNATURES = {
     "pasa_kshift_blocks": ([_P, _P, _P, _I, _I, _I, _I, _I, _I, _P], _I),
     "pasa_attn_fwd_decode_workspace_bytes": ([_I, _I, _I, _I, _I, _I, _I], _SZ),
     "pasa_attn_fwd_decode": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P], _I),
+    "pasa_attn_fwd_decode_fp8": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P],
+                                 _I),
+    "pasa_kprep_fp8_blocks": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P], _I),
     "pasa_check_device_error": ([_P, ctypes.POINTER(ctypes.c_ulonglong)], _I),
     "pasa_strerror": ([_I], ctypes.c_char_p),
     "pasa_last_cuda_error": ([], _I),
@@ -309,6 +312,44 @@ def attn_fwd_decode(q, k_shifted, means, v, causal: bool = False, scale: float |
                                   _ptr(workspace) if nbytes else None, nbytes, _stream())
     if rc != 0:
         raise PasaError(rc, "pasa_attn_fwd_decode")
+    return out, lse
+
+
+def kprep_fp8_blocks(k, k8, means, kscale, first_block: int, mode: int = MODE_SHIFT_FP8, length: int | None = None):
+    """:func:`kprep_fp8` in place for key blocks first_block.. of a cache k [B,H,cap,D] holding
+    `length` valid rows (default cap)."""
+    lib = library()
+    _check(k, "k")
+    B, H, cap, D = k.shape
+    Sk = cap if length is None else int(length)
+    rc = lib.pasa_kprep_fp8_blocks(_ptr(k), _ptr(k8), _ptr(means) if means is not None else None, _ptr(kscale), B, H,
+                                   Sk, cap, D, int(mode), int(first_block), _stream())
+    if rc != 0:
+        raise PasaError(rc, "pasa_kprep_fp8_blocks")
+    return k8, means, kscale
+
+
+def attn_fwd_decode_fp8(q, k8, means, kscale, v, causal: bool = False, scale: float | None = None,
+                        mode: int = MODE_SHIFT_FP8, splits: int = 0, out=None, lse=None, workspace=None,
+                        length: int | None = None):
+    """Decode on an e4m3 key cache from :func:`kprep_fp8` (k8 [B,Hkv,cap,D] uint8, kscale
+    [B,Hkv,ceil(cap/128)], means for mode 5) with `length` valid rows. Returns (o, lse)."""
+    lib = library()
+    _check(q, "q"), _check(v, "v")
+    B, Hq, Sq, D = q.shape
+    _, Hkv, cap, _ = v.shape
+    Sk = cap if length is None else int(length)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, Hq, Sq), device=q.device, dtype=torch.float32) if lse is None else lse
+    nbytes = lib.pasa_attn_fwd_decode_workspace_bytes(B, Hq, Hkv, Sq, Sk, D, int(splits))
+    if nbytes and (workspace is None or workspace.numel() * workspace.element_size() < nbytes):
+        workspace = torch.empty(nbytes, device=q.device, dtype=torch.uint8)
+    rc = lib.pasa_attn_fwd_decode_fp8(_ptr(q), _ptr(k8), _ptr(means) if means is not None else None, _ptr(kscale),
+                                      _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Sk, cap, D, int(bool(causal)),
+                                      float(scale) if scale is not None else 0.0, int(mode), int(splits),
+                                      _ptr(workspace) if nbytes else None, nbytes, _stream())
+    if rc != 0:
+        raise PasaError(rc, "pasa_attn_fwd_decode_fp8")
     return out, lse
 
 

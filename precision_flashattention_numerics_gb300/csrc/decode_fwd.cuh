@@ -65,25 +65,32 @@ struct DecodeParams {
   float scale_log2;   // softmax scale * log2(e)
   int cluster;        // 1: the splits of a kv head form one thread-block cluster (grid.y) and
                       // merge their partial results through distributed shared memory
+  const float* kscale;  // FP8: [planes][kstride] fp32 e4m3 scale of each key block
+  int kstride;
 };
 
-template <int NQ, int KST, int VST>
+template <int NQ, int KST, int VST, bool FP8 = false>
 struct DecodeSmem {
   static constexpr int D = 128, BN = 128;
-  static constexpr int kTile = BN * D * 2;            // one fp16 block of K' or V
+  static constexpr int kTile = BN * D * 2;            // one fp16 block of V (or K')
+  static constexpr int kKTile = BN * D * (FP8 ? 1 : 2);   // one block of keys: fp16, or e4m3 codes
+  static constexpr int kKChunks = FP8 ? 1 : 2;        // 128-byte atom columns of a key row
   static constexpr int kChunk = BN * 128;             // one 64-column (128-byte) atom column of it
   static constexpr int kQTile = NQ * D * 2, kQChunk = NQ * 128;
   static constexpr int kPTile = NQ * BN * 2, kPChunk = NQ * 128;
   static constexpr int kMTile = kChunkBlocks * D * 2, kMChunk = kChunkBlocks * 128;
-  alignas(1024) uint8_t k[KST][kTile];
+  alignas(1024) uint8_t k[KST][kKTile];
   alignas(1024) uint8_t v[VST][kTile];
   alignas(1024) uint8_t q[kQTile];
+  alignas(1024) uint8_t q8[FP8 ? NQ * 128 : 16];        // FP8: e4m3 codes of Q, one atom per row
   alignas(1024) uint8_t pt[2][kPTile];                // P_j (rows = queries, K = keys), by block parity
   alignas(1024) uint8_t m[2][kMTile];
   alignas(16) float cv[2][kChunkBlocks][NQ];          // offsets q . m_j of a chunk, by chunk parity
   alignas(16) float red[2][4][NQ];                    // per-warp column maxima, by block parity
   float cm[NQ], cl[NQ];                               // cluster merge: this split's m (log2) and l
+  float sqs[NQ];                                      // FP8: the e4m3 scale of each query row
   uint64_t q_full;
+  uint64_t q8_full;                                   // FP8: the softmax warps wrote Q's codes (4)
   uint64_t k_full[KST], k_empty[KST];
   uint64_t v_full[VST], v_empty[VST];
   uint64_t m_full[2], m_empty[2];
@@ -131,13 +138,14 @@ __device__ __forceinline__ float warp_reduce_scatter(float* v, int lane) {
   return v[0];
 }
 
-template <int NQ, bool F16ACC, bool SHIFT, bool F16PV, int KST, int VST>
+template <int NQ, bool F16ACC, bool SHIFT, bool F16PV, int KST, int VST, bool FP8 = false>
 __global__ void __launch_bounds__(kDecThreads, 1)
 decode_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                   const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapM,
                   const DecodeParams p) {
   static_assert(!F16PV || F16ACC, "fp16 PV accumulation is a variant of the fp16-score mode");
-  using Smem = DecodeSmem<NQ, KST, VST>;
+  static_assert(!FP8 || (!F16ACC && !F16PV), "FP8 scores accumulate in fp32");
+  using Smem = DecodeSmem<NQ, KST, VST, FP8>;
   static_assert(sizeof(Smem) + 1024 <= 227 * 1024, "shared memory per CTA");
   constexpr int D = 128, BN = 128;
   constexpr uint32_t kTmemCols = NQ == 16 ? 64 : 128;   // S_0, S_1, O: 3 * NQ columns
@@ -154,6 +162,7 @@ decode_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
 
   if (tid == 0) {
     mbar_init(&s.q_full, 1);
+    mbar_init(&s.q8_full, 4);
     for (int i = 0; i < KST; ++i) { mbar_init(&s.k_full[i], 1); mbar_init(&s.k_empty[i], 1); }
     for (int i = 0; i < VST; ++i) { mbar_init(&s.v_full[i], 1); mbar_init(&s.v_empty[i], 1); }
     for (int i = 0; i < 2; ++i) {
@@ -202,9 +211,9 @@ decode_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
         }
         const int ks = j % KST;
         if (!mbar_wait(&s.k_empty[ks], ((j / KST) & 1) ^ 1, abort_flag, 0x502)) return false;
-        mbar_arrive_expect_tx(&s.k_full[ks], Smem::kTile);
+        mbar_arrive_expect_tx(&s.k_full[ks], Smem::kKTile);
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < Smem::kKChunks; ++c)
           tma_load_3d(s.k[ks] + c * Smem::kChunk, &mapK, &s.k_full[ks], c * 64, (jb0 + j) * BN, plane);
         k_issued = j + 1;
         return true;
@@ -248,6 +257,8 @@ decode_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
       const uint32_t k_lo0 = sdesc_lo(smem_u32(s.k[0]), 16);
       const uint32_t v_lo0 = sdesc_lo(smem_u32(s.v[0]), Smem::kChunk);   // MN-major: atoms along D are kChunk apart
       const uint32_t p_lo0 = sdesc_lo(smem_u32(s.pt[0]), 16);
+      const uint32_t q8_lo = sdesc_lo(smem_u32(s.q8), 16);
+      constexpr uint32_t id_s8 = idesc_e4m3(BN, NQ);
       constexpr uint32_t kKStride = sizeof(s.k[0]) >> 4, kVStride = sizeof(s.v[0]) >> 4;
       constexpr uint32_t kPStride = sizeof(s.pt[0]) >> 4;
       const uint32_t tO = tmem + 2 * NQ;
@@ -257,11 +268,19 @@ decode_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
         if (j >= 2 && !mbar_wait(&s.s_free[sb], ((j >> 1) - 1) & 1, abort_flag, 0x602)) return false;
         tc_fence_after();
         const uint32_t k_lo = k_lo0 + ks * kKStride;
+        if constexpr (FP8) {
+          // e4m3 codes of K and Q, one 128-byte atom per row: four K-steps of 32 (32 bytes)
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off_k = ((kk / 4) * Smem::kChunk + (kk % 4) * 32) >> 4;
-          const uint32_t off_q = ((kk / 4) * Smem::kQChunk + (kk % 4) * 32) >> 4;
-          mma_ss_w(tmem + sb * NQ, k_lo + off_k, hi, q_lo + off_q, hi, id_s, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 32; ++kk)
+            mma_ss_f8_w(tmem + sb * NQ, k_lo + ((kk * 32) >> 4), hi, q8_lo + ((kk * 32) >> 4), hi, id_s8,
+                        kk > 0 ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off_k = ((kk / 4) * Smem::kChunk + (kk % 4) * 32) >> 4;
+            const uint32_t off_q = ((kk / 4) * Smem::kQChunk + (kk % 4) * 32) >> 4;
+            mma_ss_w(tmem + sb * NQ, k_lo + off_k, hi, q_lo + off_q, hi, id_s, kk > 0 ? 1u : 0u);
+          }
         }
         mma_commit(&s.s_full[sb]);
         mma_commit(&s.k_empty[ks]);
@@ -283,7 +302,7 @@ decode_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
         if (j == nblk - 1) mma_commit(&s.o_full);
         return true;
       };
-      bool ok = mbar_wait(&s.q_full, 0, abort_flag, 0x600);
+      bool ok = mbar_wait(FP8 ? &s.q8_full : &s.q_full, 0, abort_flag, 0x600);
       if (ok && nblk > 0) ok = qk(0);
       for (int j = 0; ok && j < nblk; ++j) {
         if (j + 1 < nblk && !qk(j + 1)) break;
@@ -316,11 +335,65 @@ decode_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
 #pragma unroll
     for (int e = 0; e < NQ / 2; ++e) lsum_h[e] = 0u;
     bool ok = true;
-    if (SHIFT) ok = warp_wait(&s.q_full, 0, abort_flag, 0x700);
+    if (SHIFT || FP8) ok = warp_wait(&s.q_full, 0, abort_flag, 0x700);
+    float sqv[FP8 ? NQ : 1];   // FP8: the e4m3 scale of each query row
+    if constexpr (FP8) {
+      // quantise Q to e4m3, one scale per row: sq = fp32(a / 448), a = max |q_row|,
+      // code = e4m3_rn_satfinite(fp32(q * fp32(448 / a))) (a = 0: both 1). TPR consecutive
+      // threads share a row, EPT elements each; the row maximum is a shuffle reduction.
+      constexpr int TPR = 128 / NQ, EPT = D / TPR;
+      const int qr = t / TPR, part = t % TPR;
+      uint4 xv[EPT / 8];
+#pragma unroll
+      for (int i = 0; i < EPT / 8; ++i) {
+        const int u = part * (EPT / 8) + i;   // 16-byte unit of the fp16 row
+        xv[i] = *reinterpret_cast<const uint4*>(s.q + (u / 8) * Smem::kQChunk + qr * 128 + (((u % 8) ^ (qr & 7)) << 4));
+      }
+      uint32_t amax = 0;
+#pragma unroll
+      for (int i = 0; i < EPT / 8; ++i) {
+        const uint32_t w4[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) amax = __vmaxu2(amax, w4[e] & 0x7FFF7FFFu);
+      }
+      amax = max(amax & 0xFFFFu, amax >> 16);
+#pragma unroll
+      for (int off = 1; off < TPR; off <<= 1) amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+      const float a = __half2float(__ushort_as_half(static_cast<unsigned short>(amax)));
+      const float inv = a > 0.0f ? __fdiv_rn(448.0f, a) : 1.0f;
+      if (part == 0) s.sqs[qr] = a > 0.0f ? __fdiv_rn(a, 448.0f) : 1.0f;
+#pragma unroll
+      for (int i = 0; i < EPT / 16; ++i) {   // 16 codes (one 16-byte unit of the e4m3 row) each
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const __half* h = reinterpret_cast<const __half*>(&xv[2 * i + e / 2]) + (e % 2) * 4;
+          const uint16_t c01 = pack_e4m3x2(__fmul_rn(__half2float(h[0]), inv), __fmul_rn(__half2float(h[1]), inv));
+          const uint16_t c23 = pack_e4m3x2(__fmul_rn(__half2float(h[2]), inv), __fmul_rn(__half2float(h[3]), inv));
+          w[e] = c01 | (static_cast<uint32_t>(c23) << 16);
+        }
+        const int wu = part * (EPT / 16) + i;
+        *reinterpret_cast<uint4*>(s.q8 + qr * 128 + ((wu ^ (qr & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.q8_full);
+      named_bar_sync(1, 128);   // every row's scale is in shared memory
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) sqv[q] = s.sqs[q];
+    }
 
+    // FP8: block scales, loaded one block ahead so the load is off the score path
+    const float* kscale_row = FP8 ? p.kscale + static_cast<size_t>(plane) * p.kstride : nullptr;
+    float sk_next = (FP8 && nblk > 0) ? __ldg(kscale_row + jb0) : 1.0f;
     for (int j = 0; j < nblk; ++j) {
       const int sb = j & 1;
       const int jg = jb0 + j;
+      float sk = 1.0f;
+      if constexpr (FP8) {
+        sk = sk_next;
+        if (j + 1 < nblk) sk_next = __ldg(kscale_row + jg + 1);
+      }
       if (SHIFT && (j % kChunkBlocks) == 0) {
         // offsets of the chunk's 16 blocks: thread t takes block t % 16 and the query rows
         // t / 16 + 8 e; fp32 dot products over the 128 dims (both tiles 128-byte swizzled)
@@ -393,6 +466,10 @@ decode_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
       if (lane == 0) mbar_arrive(&s.s_free[sb]);
 
       // recovered scores in log2 units, masked
+      if constexpr (FP8) {   // dequantise: S = sq_q * sk_j * (codes product)
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) y[q] *= sqv[q] * sk;
+      }
       if constexpr (SHIFT) {
         const float4* cr = reinterpret_cast<const float4*>(s.cv[(j / kChunkBlocks) & 1][j % kChunkBlocks]);
 #pragma unroll

@@ -186,13 +186,14 @@ int validate(const void* q, const void* k, const void* v, const void* o, const f
 }
 
 // The swapped-operand decode kernel (D = 128, at most 32 packed query rows per kv head).
-template <int NQ, bool F16ACC, bool SHIFT, bool F16PV>
+template <int NQ, bool F16ACC, bool SHIFT, bool F16PV, bool FP8 = false>
 int launch_decode(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mm,
                          const pasa::DecodeParams& p, long long planes, int splits, cudaStream_t st) {
-  // ring slots: NQ = 16: 3 K' + 3 V (211 KB of shared memory); NQ = 32: 3 + 2
-  constexpr int KST = 3, VST = NQ == 16 ? 3 : 2;
-  auto kern = pasa::decode_fwd_kernel<NQ, F16ACC, SHIFT, F16PV, KST, VST>;
-  const int smem = static_cast<int>(sizeof(pasa::DecodeSmem<NQ, KST, VST>)) + 1024;
+  // ring slots: fp16 keys, NQ = 16: 3 K' + 3 V (211 KB of shared memory); NQ = 32: 3 + 2;
+  // e4m3 keys (16 KB a block): 4 + 4 at NQ = 16 (213 KB), 4 + 3 at NQ = 32
+  constexpr int KST = FP8 ? 4 : 3, VST = FP8 ? (NQ == 16 ? 4 : 3) : (NQ == 16 ? 3 : 2);
+  auto kern = pasa::decode_fwd_kernel<NQ, F16ACC, SHIFT, F16PV, KST, VST, FP8>;
+  const int smem = static_cast<int>(sizeof(pasa::DecodeSmem<NQ, KST, VST, FP8>)) + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e);
   cudaLaunchConfig_t cfg = {};
@@ -226,6 +227,8 @@ int decode_dispatch(int mode, const CUtensorMap& mq, const CUtensorMap& mk, cons
     case PASA_MODE_NAIVE_F16ACC: return launch_decode<NQ, true, false, false>(mq, mk, mv, mm, p, planes, splits, st);
     case PASA_MODE_NOSHIFT_F32ACC: return launch_decode<NQ, false, false, false>(mq, mk, mv, mm, p, planes, splits, st);
     case PASA_MODE_SHIFT_F16ALL: return launch_decode<NQ, true, true, true>(mq, mk, mv, mm, p, planes, splits, st);
+    case PASA_MODE_SHIFT_FP8: return launch_decode<NQ, false, true, false, true>(mq, mk, mv, mm, p, planes, splits, st);
+    case PASA_MODE_NAIVE_FP8: return launch_decode<NQ, false, false, false, true>(mq, mk, mv, mm, p, planes, splits, st);
     default: return PASA_ERR_UNSUPPORTED;
   }
 }
@@ -430,15 +433,22 @@ size_t pasa_attn_fwd_decode_workspace_bytes(int B, int Hq, int Hkv, int Sq, int 
   return align_up(static_cast<size_t>(sp) * rows * D * 4, 256) + align_up(static_cast<size_t>(sp) * rows * 4, 256);
 }
 
-int pasa_attn_fwd_decode(const void* q, const void* k_shifted, const void* means, const void* v, void* o, float* lse,
-                         int B, int Hq, int Hkv, int Sq, int Sk, int Sk_cap, int D, int causal, float scale, int mode,
-                         int splits, void* workspace, size_t workspace_bytes, void* stream) {
+// Decode on a key cache: fp16 keys (K' or K) for modes 0-4, e4m3 codes with block scales
+// `kscale` for modes 5 and 6.
+static int decode_impl(const void* q, const void* k_shifted, const void* means, const float* kscale, const void* v,
+                       void* o, float* lse, int B, int Hq, int Hkv, int Sq, int Sk, int Sk_cap, int D, int causal,
+                       float scale, int mode, int splits, void* workspace, size_t workspace_bytes, void* stream) {
   int rc = validate(q, k_shifted, v, o, lse, B, Hq, Hkv, Sq, Sk, D, mode);
   if (rc != PASA_OK) return rc;
   if (Sk_cap < Sk) return PASA_ERR_SHAPE;
-  if (fp8_mode(mode) || splits < 0) return PASA_ERR_UNSUPPORTED;
+  if (splits < 0) return PASA_ERR_UNSUPPORTED;
   const int g = Hq / Hkv;
   if (static_cast<long long>(g) * Sq > pasa::kTileRows) return PASA_ERR_UNSUPPORTED;  // one tile per kv group
+  const bool fp8 = fp8_mode(mode);
+  // e4m3 keys run on the swapped-operand decode kernel only (D = 128, up to 32 packed rows)
+  if (fp8 && (D != 128 || static_cast<long long>(g) * Sq > 32)) return PASA_ERR_UNSUPPORTED;
+  if (fp8 && !kscale) return PASA_ERR_NULLPTR;
+  if (fp8 && !aligned16(kscale)) return PASA_ERR_ALIGN;
   const bool shift = shift_mode(mode);
   if (shift && !means) return PASA_ERR_NULLPTR;
   if (shift && !aligned16(means)) return PASA_ERR_ALIGN;
@@ -469,7 +479,7 @@ int pasa_attn_fwd_decode(const void* q, const void* k_shifted, const void* means
   }
   CUtensorMap mq, mk, mv, mo, mmeans;
   // the cache: Sk valid rows of Sk_cap per head (reads past Sk are zero-filled and masked)
-  if ((rc = make_map(&mk, k_shifted, D, Sk, planes, bn, 2, Sk_cap)) != PASA_OK) return rc;
+  if ((rc = make_map(&mk, k_shifted, D, Sk, planes, bn, fp8 ? 1 : 2, Sk_cap)) != PASA_OK) return rc;
   if ((rc = make_map(&mv, v, D, Sk, planes, bn, 2, Sk_cap)) != PASA_OK) return rc;
   if (shift) {
     if ((rc = make_map(&mmeans, means, D, nb, planes, pasa::kChunkBlocks, 2, (Sk_cap + bn - 1) / bn)) != PASA_OK)
@@ -494,6 +504,8 @@ int pasa_attn_fwd_decode(const void* q, const void* k_shifted, const void* means
     dp.causal = causal ? 1 : 0;
     dp.scale_log2 = scale * 1.4426950408889634f;
     dp.cluster = cluster ? 1 : 0;
+    dp.kscale = kscale;
+    dp.kstride = (Sk_cap + bn - 1) / bn;
     rc = nq == 16 ? decode_dispatch<16>(mode, mq, mk, mv, mmeans, dp, planes, sp, st)
                   : decode_dispatch<32>(mode, mq, mk, mv, mmeans, dp, planes, sp, st);
   } else {
@@ -531,6 +543,39 @@ int pasa_attn_fwd_decode(const void* q, const void* k_shifted, const void* means
                                                               static_cast<__half*>(o), lse);
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? PASA_OK : cuda_fail(e);
+}
+
+int pasa_attn_fwd_decode(const void* q, const void* k_shifted, const void* means, const void* v, void* o, float* lse,
+                         int B, int Hq, int Hkv, int Sq, int Sk, int Sk_cap, int D, int causal, float scale, int mode,
+                         int splits, void* workspace, size_t workspace_bytes, void* stream) {
+  if (fp8_mode(mode)) return PASA_ERR_UNSUPPORTED;   // e4m3 caches: pasa_attn_fwd_decode_fp8
+  return decode_impl(q, k_shifted, means, nullptr, v, o, lse, B, Hq, Hkv, Sq, Sk, Sk_cap, D, causal, scale, mode,
+                     splits, workspace, workspace_bytes, stream);
+}
+
+int pasa_attn_fwd_decode_fp8(const void* q, const void* k8, const void* means, const float* kscale, const void* v,
+                             void* o, float* lse, int B, int Hq, int Hkv, int Sq, int Sk, int Sk_cap, int D, int causal,
+                             float scale, int mode, int splits, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!fp8_mode(mode)) return PASA_ERR_UNSUPPORTED;
+  return decode_impl(q, k8, means, kscale, v, o, lse, B, Hq, Hkv, Sq, Sk, Sk_cap, D, causal, scale, mode, splits,
+                     workspace, workspace_bytes, stream);
+}
+
+int pasa_kprep_fp8_blocks(const void* k, void* k8, void* means, float* kscale, int B, int H, int Sk, int Sk_cap, int D,
+                          int mode, int first_block, void* stream) {
+  if (!k || !k8 || !kscale || (mode == PASA_MODE_SHIFT_FP8 && !means)) return PASA_ERR_NULLPTR;
+  if (B <= 0 || H <= 0 || Sk <= 0 || Sk_cap < Sk) return PASA_ERR_SHAPE;
+  if (D != 128 || !fp8_mode(mode)) return PASA_ERR_UNSUPPORTED;
+  const int nb = (Sk + 127) / 128;
+  if (first_block < 0 || first_block >= nb) return PASA_ERR_SHAPE;
+  if (static_cast<long long>(B) * H > 65535) return PASA_ERR_SHAPE;  // grid.y
+  if (!aligned16(k) || !aligned16(k8) || !aligned16(kscale) || (means && !aligned16(means))) return PASA_ERR_ALIGN;
+  int rc = check_device();
+  if (rc != PASA_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return mode == PASA_MODE_SHIFT_FP8
+             ? launch_kshift<128, pasa::kShiftFp8>(k, k8, means, kscale, B, H, Sk, st, first_block, Sk_cap)
+             : launch_kshift<128, pasa::kRawFp8>(k, k8, means, kscale, B, H, Sk, st, first_block, Sk_cap);
 }
 
 int pasa_attn_fwd_ws(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,

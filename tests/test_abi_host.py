@@ -206,3 +206,34 @@ def test_decode_workspace_bytes(lib):
                  (1, 8, 1, 1, 5000, 128, 12), (2, 28, 4, 4, 3001, 128, 0), (1, 16, 2, 8, 2049, 64, 0)]:
         assert lib.pasa_attn_fwd_decode_workspace_bytes(*args) == expect(*args), args
     assert lib.pasa_attn_fwd_decode_workspace_bytes(1, 3, 2, 1, 100, 128, 0) == 0   # Hq % Hkv != 0
+
+
+def test_fp8_decode_entry_points_check_arguments(lib):
+    P = ctypes.c_void_p
+
+    # pasa_attn_fwd_decode_fp8(q, k8, means, kscale, v, o, lse, B, Hq, Hkv, Sq, Sk, Sk_cap, D, causal, scale,
+    #                          mode, splits, workspace, workspace_bytes, stream)
+    def dec8(means=FAKE, kscale=FAKE, Hq=8, Hkv=1, Sq=1, D=128, mode=5, cap=5000):
+        return lib.pasa_attn_fwd_decode_fp8(P(FAKE), P(FAKE), P(means) if means else None,
+                                            P(kscale) if kscale else None, P(FAKE), P(FAKE), P(FAKE), 1, Hq, Hkv, Sq,
+                                            5000, cap, D, 1, 0.0, mode, 0, None, 0, None)
+
+    assert dec8(mode=0) == -3 and dec8(mode=3) == -3     # fp16 modes: pasa_attn_fwd_decode
+    assert dec8(D=64) == -3                              # e4m3 keys: D = 128 only
+    assert dec8(Sq=5) == -3                              # 40 packed rows: beyond the decode kernel
+    assert dec8(kscale=0) == -1
+    assert dec8(means=0) == -1 and dec8(mode=6, means=0) != -1
+    assert dec8(kscale=FAKE_MIS) == -4
+    assert dec8(cap=4999) == -2
+    # the fp16 decode entry refuses the FP8 modes
+    assert lib.pasa_attn_fwd_decode(P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), 1, 8, 1, 1, 5000, 5000, 128,
+                                    1, 0.0, 5, 0, None, 0, None) == -3
+    # pasa_kprep_fp8_blocks(k, k8, means, kscale, B, H, Sk, Sk_cap, D, mode, first_block, stream)
+    kb = lib.pasa_kprep_fp8_blocks
+    assert kb(P(FAKE), P(FAKE), None, P(FAKE), 1, 1, 300, 300, 128, 5, 0, None) == -1   # mode 5 needs means
+    assert kb(P(FAKE), P(FAKE), None, None, 1, 1, 300, 300, 128, 6, 0, None) == -1
+    assert kb(P(FAKE), P(FAKE), P(FAKE), P(FAKE), 1, 1, 300, 300, 128, 5, 3, None) == -2
+    assert kb(P(FAKE), P(FAKE), P(FAKE), P(FAKE), 1, 1, 300, 299, 128, 5, 0, None) == -2
+    assert kb(P(FAKE), P(FAKE), P(FAKE), P(FAKE), 1, 1, 300, 300, 64, 5, 0, None) == -3
+    assert kb(P(FAKE), P(FAKE), P(FAKE), P(FAKE), 1, 1, 300, 300, 128, 1, 0, None) == -3
+    assert kb(P(FAKE_MIS), P(FAKE), P(FAKE), P(FAKE), 1, 1, 300, 300, 128, 6, 0, None) == -4
