@@ -50,7 +50,9 @@
 
 namespace pasa {
 
-constexpr int kDecThreads = 192;
+// Threads of a decode CTA with G softmax warpgroups: 4 G softmax warps, the TMA producer
+// and the TMEM-owning MMA warp.
+__host__ __device__ constexpr int dec_threads(int G) { return 32 * (4 * G + 2); }
 
 struct DecodeParams {
   __half* o;          // [planes][rows][128] fp16 (the [B, Hq, Sq, D] output)
@@ -69,7 +71,7 @@ struct DecodeParams {
   int kstride;
 };
 
-template <int NQ, int KST, int VST, bool FP8 = false>
+template <int NQ, int KST, int VST, bool FP8 = false, int G = 1>
 struct DecodeSmem {
   static constexpr int D = 128, BN = 128;
   static constexpr int kTile = BN * D * 2;            // one fp16 block of V (or K')
@@ -83,10 +85,11 @@ struct DecodeSmem {
   alignas(1024) uint8_t v[VST][kTile];
   alignas(1024) uint8_t q[kQTile];
   alignas(1024) uint8_t q8[FP8 ? NQ * 128 : 16];        // FP8: e4m3 codes of Q, one atom per row
-  alignas(1024) uint8_t pt[2][kPTile];                // P_j (rows = queries, K = keys), by block parity
+  alignas(1024) uint8_t pt[G][2][kPTile];             // per group: P_j (rows = queries, K = keys), 2 buffers
   alignas(1024) uint8_t m[2][kMTile];
-  alignas(16) float cv[2][kChunkBlocks][NQ];          // offsets q . m_j of a chunk, by chunk parity
-  alignas(16) float red[2][4][NQ];                    // per-warp column maxima, by block parity
+  alignas(16) float cv[G][2][kChunkBlocks][NQ];       // per group: offsets q . m_j of a chunk, by chunk parity
+  alignas(16) float red[G][2][4][NQ];                 // per group: per-warp column maxima, 2 buffers
+  float exm[NQ], exl[NQ];                             // G = 2: group 1's m (log2) and l for the merge
   float cm[NQ], cl[NQ];                               // cluster merge: this split's m (log2) and l
   float sqs[NQ];                                      // FP8: the e4m3 scale of each query row
   uint64_t q_full;
@@ -94,9 +97,9 @@ struct DecodeSmem {
   uint64_t k_full[KST], k_empty[KST];
   uint64_t v_full[VST], v_empty[VST];
   uint64_t m_full[2], m_empty[2];
-  uint64_t s_full[2], s_free[2];
-  uint64_t p_full[2], p_free[2];
-  uint64_t o_full, drain;
+  uint64_t s_full[G][2], s_free[G][2];
+  uint64_t p_full[G][2], p_free[G][2];
+  uint64_t o_full[G], drain;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -138,17 +141,20 @@ __device__ __forceinline__ float warp_reduce_scatter(float* v, int lane) {
   return v[0];
 }
 
-template <int NQ, bool F16ACC, bool SHIFT, bool F16PV, int KST, int VST, bool FP8 = false>
-__global__ void __launch_bounds__(kDecThreads, 1)
+template <int NQ, bool F16ACC, bool SHIFT, bool F16PV, int KST, int VST, bool FP8 = false, int G = 1>
+__global__ void __launch_bounds__(dec_threads(G), 1)
 decode_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                   const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapM,
                   const DecodeParams p) {
   static_assert(!F16PV || F16ACC, "fp16 PV accumulation is a variant of the fp16-score mode");
   static_assert(!FP8 || (!F16ACC && !F16PV), "FP8 scores accumulate in fp32");
-  using Smem = DecodeSmem<NQ, KST, VST, FP8>;
+  static_assert(G == 1 || G == 2, "softmax groups");
+  using Smem = DecodeSmem<NQ, KST, VST, FP8, G>;
   static_assert(sizeof(Smem) + 1024 <= 227 * 1024, "shared memory per CTA");
   constexpr int D = 128, BN = 128;
-  constexpr uint32_t kTmemCols = NQ == 16 ? 64 : 128;   // S_0, S_1, O: 3 * NQ columns
+  // per group: S_0, S_1 and O, NQ columns each, from column 3 NQ g
+  constexpr uint32_t kTmemCols = G * 3 * NQ <= 64 ? 64 : (G * 3 * NQ <= 128 ? 128 : 256);
+  constexpr int kProdWarp = 4 * G, kMmaWarp = 4 * G + 1;
   extern __shared__ uint8_t smem_raw[];
   Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -167,18 +173,20 @@ decode_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
     for (int i = 0; i < VST; ++i) { mbar_init(&s.v_full[i], 1); mbar_init(&s.v_empty[i], 1); }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.m_full[i], 1);
-      mbar_init(&s.m_empty[i], 4);
-      mbar_init(&s.s_full[i], 1);
-      mbar_init(&s.s_free[i], 4);
-      mbar_init(&s.p_full[i], 4);
-      mbar_init(&s.p_free[i], 1);
+      mbar_init(&s.m_empty[i], 4 * G);
+      for (int g = 0; g < G; ++g) {
+        mbar_init(&s.s_full[g][i], 1);
+        mbar_init(&s.s_free[g][i], 4);
+        mbar_init(&s.p_full[g][i], 4);
+        mbar_init(&s.p_free[g][i], 1);
+      }
     }
-    mbar_init(&s.o_full, 1);
+    for (int g = 0; g < G; ++g) mbar_init(&s.o_full[g], 1);
     mbar_init(&s.drain, 1);
     s.abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(&s.tmem_base, kTmemCols);
     tmem_relinquish();
   }
@@ -188,7 +196,7 @@ decode_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
   const uint32_t tmem = s.tmem_base;
   volatile int* abort_flag = &s.abort_flag;
 
-  if (warp == 4) {
+  if (warp == kProdWarp) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&mapQ);
@@ -228,9 +236,11 @@ decode_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
         v_issued = j + 1;
         return true;
       };
-      bool pok = nblk == 0 || load_k(0);
+      // K runs G blocks ahead of V, matching the MMA thread (QK(j + G) before PV(j))
+      bool pok = true;
+      for (int j = 0; pok && j < G && j < nblk; ++j) pok = load_k(j);
       for (int j = 0; pok && j < nblk; ++j) {
-        if (j + 1 < nblk && !load_k(j + 1)) break;
+        if (j + G < nblk && !load_k(j + G)) break;
         if (!load_v(j)) break;
       }
       if (*abort_flag) {
@@ -247,8 +257,10 @@ decode_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA thread
+    // Block j belongs to softmax group j mod G (its local index i = j / G picks the S and P
+    // buffers); QK(j + G) is issued before PV(j).
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_f16_ab(BN, NQ, !F16ACC, false, false);
       constexpr uint32_t id_o = idesc_f16_ab(D, NQ, !F16PV, true, false);
@@ -260,52 +272,54 @@ decode_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
       const uint32_t q8_lo = sdesc_lo(smem_u32(s.q8), 16);
       constexpr uint32_t id_s8 = idesc_e4m3(BN, NQ);
       constexpr uint32_t kKStride = sizeof(s.k[0]) >> 4, kVStride = sizeof(s.v[0]) >> 4;
-      constexpr uint32_t kPStride = sizeof(s.pt[0]) >> 4;
-      const uint32_t tO = tmem + 2 * NQ;
+      constexpr uint32_t kPStride = sizeof(s.pt[0][0]) >> 4;
       auto qk = [&](int j) -> bool {
-        const int ks = j % KST, sb = j & 1;
+        const int g = j % G, i = j / G;
+        const int ks = j % KST, sb = i & 1;
         if (!mbar_wait(&s.k_full[ks], (j / KST) & 1, abort_flag, 0x601)) return false;
-        if (j >= 2 && !mbar_wait(&s.s_free[sb], ((j >> 1) - 1) & 1, abort_flag, 0x602)) return false;
+        if (i >= 2 && !mbar_wait(&s.s_free[g][sb], ((i >> 1) - 1) & 1, abort_flag, 0x602)) return false;
+        const uint32_t tS = tmem + g * 3 * NQ + sb * NQ;
         tc_fence_after();
         const uint32_t k_lo = k_lo0 + ks * kKStride;
         if constexpr (FP8) {
           // e4m3 codes of K and Q, one 128-byte atom per row: four K-steps of 32 (32 bytes)
 #pragma unroll
           for (int kk = 0; kk < D / 32; ++kk)
-            mma_ss_f8_w(tmem + sb * NQ, k_lo + ((kk * 32) >> 4), hi, q8_lo + ((kk * 32) >> 4), hi, id_s8,
-                        kk > 0 ? 1u : 0u);
+            mma_ss_f8_w(tS, k_lo + ((kk * 32) >> 4), hi, q8_lo + ((kk * 32) >> 4), hi, id_s8, kk > 0 ? 1u : 0u);
         } else {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off_k = ((kk / 4) * Smem::kChunk + (kk % 4) * 32) >> 4;
             const uint32_t off_q = ((kk / 4) * Smem::kQChunk + (kk % 4) * 32) >> 4;
-            mma_ss_w(tmem + sb * NQ, k_lo + off_k, hi, q_lo + off_q, hi, id_s, kk > 0 ? 1u : 0u);
+            mma_ss_w(tS, k_lo + off_k, hi, q_lo + off_q, hi, id_s, kk > 0 ? 1u : 0u);
           }
         }
-        mma_commit(&s.s_full[sb]);
+        mma_commit(&s.s_full[g][sb]);
         mma_commit(&s.k_empty[ks]);
         return true;
       };
       auto pv = [&](int j) -> bool {
-        const int vs = j % VST, pb = j & 1;
+        const int g = j % G, i = j / G;
+        const int vs = j % VST, pb = i & 1;
         if (!mbar_wait(&s.v_full[vs], (j / VST) & 1, abort_flag, 0x603)) return false;
-        if (!mbar_wait(&s.p_full[pb], (j >> 1) & 1, abort_flag, 0x604)) return false;
+        if (!mbar_wait(&s.p_full[g][pb], (i >> 1) & 1, abort_flag, 0x604)) return false;
         tc_fence_after();
-        const uint32_t v_lo = v_lo0 + vs * kVStride, p_lo = p_lo0 + pb * kPStride;
+        const uint32_t v_lo = v_lo0 + vs * kVStride, p_lo = p_lo0 + (g * 2 + pb) * kPStride;
+        const uint32_t tO = tmem + g * 3 * NQ + 2 * NQ;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
           const uint32_t off_p = ((kk / 4) * Smem::kPChunk + (kk % 4) * 32) >> 4;
-          mma_ss_w(tO, v_lo + kk * (2048 >> 4), hi, p_lo + off_p, hi, id_o, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_ss_w(tO, v_lo + kk * (2048 >> 4), hi, p_lo + off_p, hi, id_o, (i > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&s.p_free[pb]);
+        mma_commit(&s.p_free[g][pb]);
         mma_commit(&s.v_empty[vs]);
-        if (j == nblk - 1) mma_commit(&s.o_full);
+        if (j + G >= nblk) mma_commit(&s.o_full[g]);   // the group's last block
         return true;
       };
       bool ok = mbar_wait(FP8 ? &s.q8_full : &s.q_full, 0, abort_flag, 0x600);
-      if (ok && nblk > 0) ok = qk(0);
+      for (int j = 0; ok && j < G && j < nblk; ++j) ok = qk(j);
       for (int j = 0; ok && j < nblk; ++j) {
-        if (j + 1 < nblk && !qk(j + 1)) break;
+        if (j + G < nblk && !qk(j + G)) break;
         if (!pv(j)) break;
       }
       // every MMA issued here completes before TMEM is released
@@ -317,8 +331,12 @@ decode_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
     __syncwarp();
   } else {
     // ------------------------------------------------------------------ softmax + epilogue
-    const int t = tid;   // TMEM lane: key t of a block, output dim t
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    // Group g takes blocks g, g + G, ...; with G = 2 the two groups' results are merged by
+    // group 0 at the end.
+    const int g = warp >> 2;
+    const int t = tid & 127;   // TMEM lane: key t of a block, output dim t
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tG = tmem + lane_base + g * 3 * NQ;   // this group's S_0, S_1, O
     const float sl2 = p.scale_log2;
     constexpr int kLaneShift = NQ == 16 ? 1 : 0;
     const int q_of_lane = lane >> kLaneShift;              // column held after a reduce-scatter
@@ -338,6 +356,7 @@ decode_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
     if (SHIFT || FP8) ok = warp_wait(&s.q_full, 0, abort_flag, 0x700);
     float sqv[FP8 ? NQ : 1];   // FP8: the e4m3 scale of each query row
     if constexpr (FP8) {
+      if (g == 0) {
       // quantise Q to e4m3, one scale per row: sq = fp32(a / 448), a = max |q_row|,
       // code = e4m3_rn_satfinite(fp32(q * fp32(448 / a))) (a = 0: both 1). TPR consecutive
       // threads share a row, EPT elements each; the row maximum is a shuffle reduction.
@@ -378,23 +397,25 @@ decode_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s.q8_full);
-      named_bar_sync(1, 128);   // every row's scale is in shared memory
+      }
+      named_bar_sync(3, 128 * G);   // every row's scale is in shared memory
 #pragma unroll
       for (int q = 0; q < NQ; ++q) sqv[q] = s.sqs[q];
     }
 
     // FP8: block scales, loaded one block ahead so the load is off the score path
     const float* kscale_row = FP8 ? p.kscale + static_cast<size_t>(plane) * p.kstride : nullptr;
-    float sk_next = (FP8 && nblk > 0) ? __ldg(kscale_row + jb0) : 1.0f;
-    for (int j = 0; j < nblk; ++j) {
-      const int sb = j & 1;
+    float sk_next = (FP8 && g < nblk) ? __ldg(kscale_row + jb0 + g) : 1.0f;
+    for (int j = g; j < nblk; j += G) {
+      const int i = j / G;   // the group's local block index
+      const int sb = i & 1;
       const int jg = jb0 + j;
       float sk = 1.0f;
       if constexpr (FP8) {
         sk = sk_next;
-        if (j + 1 < nblk) sk_next = __ldg(kscale_row + jg + 1);
+        if (j + G < nblk) sk_next = __ldg(kscale_row + jg + G);
       }
-      if (SHIFT && (j % kChunkBlocks) == 0) {
+      if (SHIFT && (j % kChunkBlocks) == g) {   // the group's first block of a chunk
         // offsets of the chunk's 16 blocks: thread t takes block t % 16 and the query rows
         // t / 16 + 8 e; fp32 dot products over the 128 dims (both tiles 128-byte swizzled)
         const int ci = j / kChunkBlocks;
@@ -426,19 +447,19 @@ decode_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
             }
           }
 #pragma unroll
-          for (int e = 0; e < NQ / 8; ++e) s.cv[ci & 1][blk][qg + 8 * e] = acc[e];
+          for (int e = 0; e < NQ / 8; ++e) s.cv[g][ci & 1][blk][qg + 8 * e] = acc[e];
         }
-        named_bar_sync(1, 128);
+        named_bar_sync(1 + g, 128);
         __syncwarp();
         if (lane == 0) mbar_arrive(&s.m_empty[ci & 1]);
       }
 
       // scores of block j: this thread's key against the NQ query columns
-      if (ok) ok = warp_wait(&s.s_full[sb], (j >> 1) & 1, abort_flag, 0x702);
+      if (ok) ok = warp_wait(&s.s_full[g][sb], (i >> 1) & 1, abort_flag, 0x702);
       tc_fence_after();
       float y[NQ];
       {
-        const uint32_t tS = tmem + lane_base + sb * NQ;
+        const uint32_t tS = tG + sb * NQ;
         if constexpr (F16ACC) {
           uint32_t h[NQ / 2];
 #pragma unroll
@@ -463,7 +484,7 @@ decode_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s.s_free[sb]);
+      if (lane == 0) mbar_arrive(&s.s_free[g][sb]);
 
       // recovered scores in log2 units, masked
       if constexpr (FP8) {   // dequantise: S = sq_q * sk_j * (codes product)
@@ -471,7 +492,7 @@ decode_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
         for (int q = 0; q < NQ; ++q) y[q] *= sqv[q] * sk;
       }
       if constexpr (SHIFT) {
-        const float4* cr = reinterpret_cast<const float4*>(s.cv[(j / kChunkBlocks) & 1][j % kChunkBlocks]);
+        const float4* cr = reinterpret_cast<const float4*>(s.cv[g][(j / kChunkBlocks) & 1][j % kChunkBlocks]);
 #pragma unroll
         for (int c4 = 0; c4 < NQ / 4; ++c4) {
           const float4 c = cr[c4];
@@ -499,13 +520,13 @@ decode_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
 #pragma unroll
         for (int q = 0; q < NQ; ++q) v[q] = y[q];
         const float mx = warp_reduce_scatter<NQ, true>(v, lane);
-        if (writer) s.red[sb][warp][q_of_lane] = mx;
+        if (writer) s.red[g][sb][warp & 3][q_of_lane] = mx;
       }
-      named_bar_sync(1, 128);
+      named_bar_sync(1 + g, 128);
       float alpha[NQ];
       bool resc = false;
       {
-        const float4* r4 = reinterpret_cast<const float4*>(s.red[sb]);
+        const float4* r4 = reinterpret_cast<const float4*>(s.red[g][sb]);
 #pragma unroll
         for (int c4 = 0; c4 < NQ / 4; ++c4) {
           const float4 a = r4[c4], b = r4[NQ / 4 + c4], c = r4[2 * (NQ / 4) + c4], d = r4[3 * (NQ / 4) + c4];
@@ -542,11 +563,11 @@ decode_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
         for (int q = 0; q < NQ; ++q) lsum[q] = (resc ? lsum[q] * alpha[q] : lsum[q]) + pe[q];
       }
       // P_(j-2) (same buffer) has been consumed by PV(j-2); a rescale of O needs PV(j-1) done
-      if (ok && j >= 2) ok = warp_wait(&s.p_free[sb], ((j >> 1) - 1) & 1, abort_flag, 0x703);
-      if (resc && j >= 1) {
-        if (ok) ok = warp_wait(&s.p_free[sb ^ 1], ((j - 1) >> 1) & 1, abort_flag, 0x704);
+      if (ok && i >= 2) ok = warp_wait(&s.p_free[g][sb], ((i >> 1) - 1) & 1, abort_flag, 0x703);
+      if (resc && i >= 1) {
+        if (ok) ok = warp_wait(&s.p_free[g][sb ^ 1], ((i - 1) >> 1) & 1, abort_flag, 0x704);
         tc_fence_after();
-        const uint32_t tO = tmem + lane_base + 2 * NQ;
+        const uint32_t tO = tG + 2 * NQ;
         if constexpr (F16PV) {
           uint32_t w[NQ / 2];
 #pragma unroll
@@ -572,7 +593,7 @@ decode_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
       }
       {
         // element (query q, key t) of the K-major, 128-byte swizzled P tile
-        uint8_t* prow = s.pt[sb] + (t >> 6) * Smem::kPChunk + (t & 7) * 2;
+        uint8_t* prow = s.pt[g][sb] + (t >> 6) * Smem::kPChunk + (t & 7) * 2;
         const int u = (t & 63) >> 3;
 #pragma unroll
         for (int e = 0; e < NQ / 2; ++e) {
@@ -586,11 +607,12 @@ decode_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s.p_full[sb]);
+      if (lane == 0) mbar_arrive(&s.p_full[g][sb]);
     }
 
     // ------------------------------------------------------------------ epilogue
-    if (ok && nblk > 0) ok = warp_wait(&s.o_full, 0, abort_flag, 0x705);
+    const int nmine = nblk > g ? (nblk - g + G - 1) / G : 0;   // this group's blocks
+    if (ok && nmine > 0) ok = warp_wait(&s.o_full[g], 0, abort_flag, 0x705);
     tc_fence_after();
     // row sums: the 128 threads' partial sums per column (F16PV: fp16 partials added in
     // fp32, the total rounded to fp16)
@@ -607,9 +629,9 @@ decode_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
         }
       }
       const float sum = warp_reduce_scatter<NQ, false>(v, lane);
-      if (writer) s.red[nblk & 1][warp][q_of_lane] = sum;
-      named_bar_sync(1, 128);
-      const float4* r4 = reinterpret_cast<const float4*>(s.red[nblk & 1]);
+      if (writer) s.red[g][nmine & 1][warp & 3][q_of_lane] = sum;
+      named_bar_sync(1 + g, 128);
+      const float4* r4 = reinterpret_cast<const float4*>(s.red[g][nmine & 1]);
 #pragma unroll
       for (int c4 = 0; c4 < NQ / 4; ++c4) {
         const float4 a = r4[c4], b = r4[NQ / 4 + c4], c = r4[2 * (NQ / 4) + c4], d = r4[3 * (NQ / 4) + c4];
@@ -624,9 +646,8 @@ decode_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
       }
     }
     // O^T lane t is output dim t of every query column
-    float ov[NQ];
-    if (ok && nblk > 0) {
-      const uint32_t tO = tmem + lane_base + 2 * NQ;
+    // O^T in TMEM (fp32, or fp16 with F16PV) -> NQ fp32 values of output dim t
+    auto load_o = [&](uint32_t tO, float* out) {
       if constexpr (F16PV) {
         uint32_t w[NQ / 2];
 #pragma unroll
@@ -636,8 +657,8 @@ decode_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
 #pragma unroll
         for (int e = 0; e < NQ / 2; ++e) {
           const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
-          ov[2 * e] = f.x;
-          ov[2 * e + 1] = f.y;
+          out[2 * e] = f.x;
+          out[2 * e + 1] = f.y;
         }
       } else {
         uint32_t w[NQ];
@@ -646,12 +667,56 @@ decode_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
         tmem_ld_wait();
         reg_fence<NQ>(w);
 #pragma unroll
-        for (int q = 0; q < NQ; ++q) ov[q] = __uint_as_float(w[q]);
+        for (int q = 0; q < NQ; ++q) out[q] = __uint_as_float(w[q]);
       }
+    };
+    float ov[NQ];
+    if (ok && nmine > 0) {
+      load_o(tG + 2 * NQ, ov);
     } else {
 #pragma unroll
       for (int q = 0; q < NQ; ++q) ov[q] = 0.0f;
     }
+    if constexpr (G == 2) {
+      // group 1 hands m and l to group 0, which merges the two partial results:
+      // O = a0 O0 + a1 O1, l = a0 l0 + a1 l1, a_x = 2^(m_x - M), M = max(m0, m1)
+      if (g == 1) {
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+          if (t == q) {
+            s.exm[q] = lt[q] > 0.0f ? m_run[q] : -INFINITY;
+            s.exl[q] = lt[q];
+          }
+        }
+      }
+      named_bar_sync(3, 256);
+      if (g == 0) {
+        const int n1 = nblk / 2;   // group 1's blocks
+        float o1[NQ];
+        if (ok && n1 > 0) ok = warp_wait(&s.o_full[1], 0, abort_flag, 0x706);
+        tc_fence_after();
+        if (ok && n1 > 0) {
+          load_o(tmem + lane_base + 3 * NQ + 2 * NQ, o1);
+        } else {
+#pragma unroll
+          for (int q = 0; q < NQ; ++q) o1[q] = 0.0f;
+        }
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+          const float m0 = lt[q] > 0.0f ? m_run[q] : -INFINITY;
+          const float m1 = s.exm[q], l1 = s.exl[q];
+          const float M = fmaxf(m0, m1);
+          if (M != -INFINITY) {
+            const float a0 = m0 == -INFINITY ? 0.0f : ex2_approx(m0 - M);
+            const float a1 = m1 == -INFINITY ? 0.0f : ex2_approx(m1 - M);
+            ov[q] = a0 * ov[q] + a1 * o1[q];
+            lt[q] = a0 * lt[q] + a1 * l1;
+            m_run[q] = M;
+          }
+        }
+      }
+    }
+    if (g == 0) {
     const size_t rows_total = static_cast<size_t>(gridDim.x) * p.rows;
     const size_t row0 = static_cast<size_t>(plane) * p.rows;
     if (p.cluster) {
@@ -683,6 +748,7 @@ decode_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
         }
       }
     }
+    }  // group 0
   }
 
   if (p.cluster) {
@@ -729,7 +795,7 @@ decode_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tmem, kTmemCols);
+  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace pasa
