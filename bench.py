@@ -53,9 +53,9 @@ TRAFFIC_MODE = 0
 TRAFFIC_BYTES = 4 * (75.631872e6 + 24.462592e6)
 TRAFFIC_KERNEL_SHA = "ae9385673b602f59"
 # The same for one decode-kernel launch on the decode workload (captured at full size:
-# 539.11 MB read + 3.06 MB written); profiles/decode_fwd_kbias10_t3_b8h28g4_q1_s32768_full.md.
-DECODE_TRAFFIC_BYTES = 539113984 + 3058688
-DECODE_TRAFFIC_SHA = "7554aed3cf7c75ba"
+# 539.11 MB read + 3.17 MB written); profiles/decode_fwd_kbias10_t3_b8h28g4_q1_s32768_full.md.
+DECODE_TRAFFIC_BYTES = 539113472 + 3172608
+DECODE_TRAFFIC_SHA = "ca888b56aee96d33"
 
 
 def _source_sha(name):
@@ -403,6 +403,37 @@ def bench_decode(args, w: wl.Workload, local_rank: int, sampler=None):
     }
 
 
+def bench_stats(args, w: wl.Workload, local_rank: int):
+    """The overflow diagnostic (pasa_attn_fwd_stats with per-key-block maxima): one step is the
+    shift, the zeroing of the block maxima and the diagnostic variant of the attention kernel,
+    which also tracks each block's score minimum and reduces both magnitudes per block."""
+    import torch
+
+    import precision_flashattention_numerics_gb300 as pasa
+
+    dev = torch.device("cuda", local_rank)
+    q, k, v = wl.make_inputs(w)
+    qt, kt, vt = (torch.from_numpy(x).to(dev) for x in (q, k, v))
+    mode = args.mode if args.mode in (0, 1, 2, 3, 4) else 0
+    for _ in range(3):
+        pasa.attn_fwd_stats(qt, kt, vt, causal=w.causal, mode=mode, block_stats=True)
+    torch.cuda.synchronize()
+    pasa.check_device_error()
+    n = max(3, min(args.steps, 10))
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for i in range(n):
+        ev[i][0].record(stream)
+        pasa.attn_fwd_stats(qt, kt, vt, causal=w.causal, mode=mode, block_stats=True)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    pasa.check_device_error()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    return {"workload": w.name, "mode": MODE_NAMES[mode], "ms_per_step": round(ms, 4),
+            "tflops": round(w.flops() / (ms * 1e-3) / 1e12, 1), "steps": n,
+            "step": "kshift + zeroing of the block maxima + diagnostic attention kernel"}
+
+
 def decode_main(args, rank: int, world: int, local_rank: int):
     """`--decode`: one JSON line for the decode step alone (tokens/s; roofline against HBM)."""
     w = wl.WORKLOADS[DECODE_WORKLOAD]
@@ -506,6 +537,8 @@ def main():
                           "attn_ms": round(ra["attn_ms"], 4), "kshift_ms": round(ra["kshift_ms"], 4),
                           "finite": ra["finite"]}
         also[DECODE_WORKLOAD] = bench_decode(args, wl.WORKLOADS[DECODE_WORKLOAD], local_rank)
+        if args.mode not in FP8_MODES:
+            also["overflow_diagnostic"] = bench_stats(args, w, local_rank)
 
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))  # fp16 dense = bf16 dense rate
     peak_note = f"{peak_src} bf16 dense burst (fp16 dense has the same nominal rate)"
