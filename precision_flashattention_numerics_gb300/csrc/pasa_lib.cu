@@ -11,6 +11,7 @@
 
 #include "../../include/pasa.h"
 #include "attn_fwd.cuh"
+#include "attn_fwd2s.cuh"
 #include "decode_fwd.cuh"
 #include "kshift.cuh"
 #include "ptx.cuh"
@@ -183,6 +184,38 @@ int validate(const void* q, const void* k, const void* v, const void* o, const f
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (lse && !aligned16(lse)))
     return PASA_ERR_ALIGN;
   return PASA_OK;
+}
+
+// D = 64 prefill, modes 0-3: two softmax warp sets on alternate key blocks.
+template <bool F16ACC, bool SHIFT, bool CAUSAL>
+int launch_2set(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mo,
+                const CUtensorMap& mm, const pasa::AttnParams& p, cudaStream_t st) {
+  constexpr int KST = 4, VST = 4;
+  auto kern = pasa::twoset::attn_fwd_2set_kernel<64, 128, F16ACC, SHIFT, CAUSAL, KST, VST, false>;
+  const int smem = static_cast<int>(sizeof(pasa::twoset::AttnSmem<64, 128, KST, VST>)) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const long long ctas = static_cast<long long>(p.n_qblk) * p.Hq * p.B;
+  kern<<<static_cast<unsigned>(ctas), pasa::twoset::kAttnThreads, smem, st>>>(mq, mk, mv, mo, mm, p);
+  e = cudaGetLastError();
+  return e == cudaSuccess ? PASA_OK : cuda_fail(e);
+}
+
+int twoset_dispatch(int mode, int causal, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                    const CUtensorMap& mo, const CUtensorMap& mm, const pasa::AttnParams& p, cudaStream_t st) {
+#define PASA_2S_CASE(MODE, F16, SH)                                                   \
+  case MODE:                                                                          \
+    return causal ? launch_2set<F16, SH, true>(mq, mk, mv, mo, mm, p, st)             \
+                  : launch_2set<F16, SH, false>(mq, mk, mv, mo, mm, p, st);
+  switch (mode) {
+    PASA_2S_CASE(PASA_MODE_SHIFT_F16ACC, true, true)
+    PASA_2S_CASE(PASA_MODE_SHIFT_F32ACC, false, true)
+    PASA_2S_CASE(PASA_MODE_NAIVE_F16ACC, true, false)
+    PASA_2S_CASE(PASA_MODE_NOSHIFT_F32ACC, false, false)
+    default:
+      return PASA_ERR_UNSUPPORTED;
+  }
+#undef PASA_2S_CASE
 }
 
 // The swapped-operand decode kernel (D = 128, at most 32 packed query rows per kv head).
@@ -374,6 +407,8 @@ static int attn_launch(const void* q, const void* kk, const void* mm, const void
   if (stats)
     return D == 64 ? attn_dispatch<64, true>(mode, causal, mq, mk, mv, mo, mmeans, p, st)
                    : attn_dispatch<128, true>(mode, causal, mq, mk, mv, mo, mmeans, p, st);
+  if (D == 64 && mode <= PASA_MODE_NOSHIFT_F32ACC)
+    return twoset_dispatch(mode, causal, mq, mk, mv, mo, mmeans, p, st);
   return D == 64 ? attn_dispatch<64, false>(mode, causal, mq, mk, mv, mo, mmeans, p, st)
                  : attn_dispatch<128, false>(mode, causal, mq, mk, mv, mo, mmeans, p, st);
 }
