@@ -239,10 +239,11 @@ int pasa_kshift_blocks(const void* k, void* k_shifted, void* means, int B, int H
                        int first_block, void* stream);
 
 /*
- * Bytes of workspace pasa_attn_fwd_decode needs for these sizes and `splits` (0 = the
- * automatic choice): 0 when the call runs unsplit, else splits * B * Hq * Sq * (D + 1)
- * fp32 values (partial outputs and log-sum-exps, each part 256-byte aligned). Returns 0 for
- * invalid sizes as well.
+ * Bytes of workspace pasa_attn_fwd_decode(_fp8) needs for these sizes and `splits` (0 =
+ * the automatic choice): 0 when the call runs unsplit or merges its splits inside a
+ * thread-block cluster (D = 128, g * Sq <= 32, 2 to 8 splits), else splits * B * Hq * Sq *
+ * (D + 1) fp32 values (partial outputs and log-sum-exps, each part 256-byte aligned).
+ * Returns 0 for invalid sizes as well.
  */
 size_t pasa_attn_fwd_decode_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D, int splits);
 
@@ -262,9 +263,11 @@ size_t pasa_attn_fwd_decode_workspace_bytes(int B, int Hq, int Hkv, int Sq, int 
  *    (padded to 16 or 32) on its N side; otherwise the attention kernel runs on the
  *    packed rows as one 128-row tile;
  *  - the key blocks are split across `splits` CTAs per kv head (0 = automatic: at most one
- *    CTA per SM, at least eight key blocks per split). Each split writes its O / l (fp32)
- *    and m + log2 l to the workspace; a second kernel merges them:
- *    O = sum_s w_s O_s / sum_s w_s, w_s = 2^(lse_s - max lse), and writes o (fp16) and lse.
+ *    CTA per SM, at least eight key blocks per split), merged by their log-sum-exps:
+ *    O = sum_s w_s O_s / sum_s w_s, w_s = 2^(lse_s - max lse). On the swapped-operand
+ *    kernel with up to 8 splits the splits of a kv head run as one thread-block cluster and
+ *    merge through distributed shared memory (no workspace); otherwise each split writes
+ *    its O / l (fp32) and m + log2 l to the workspace and a second kernel merges them.
  * The causal mask is bottom-right aligned per head, as in pasa_attn_fwd. q, o: fp16
  * [B, Hq, Sq, D]; the cache holds Sk valid keys of Sk_cap allocated rows per head
  * (Sk_cap >= Sk, else PASA_ERR_SHAPE; pass Sk for dense tensors): k_shifted, v fp16
