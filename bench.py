@@ -286,18 +286,19 @@ def bench_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int, also
     if also:
         return res
 
-    # end to end through pasa_attn_fwd with host buffers (copies inside the timed region)
+    # end to end through pasa_attn_fwd_host: q, k, v from pinned host memory, o and lse back
+    # to it, every copy inside the timed region (overlapped with the kernels piece by piece)
     qh, kh, vh = (torch.from_numpy(x).pin_memory() for x in (q, k, v))
     oh = torch.empty(qt.shape, dtype=torch.float16).pin_memory()
     lh = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    B, Hq, Sq, D = qt.shape
+    Hkv, Sk = kt.shape[1], kt.shape[2]
+    hbuf = torch.empty(pasa.host_device_bytes(B, Hq, Hkv, Sq, Sk, D, args.mode, args.host_chunks),
+                       dtype=torch.uint8, device=qt.device)
 
     def e2e_step():
-        qt.copy_(qh, non_blocking=True)
-        kt.copy_(kh, non_blocking=True)
-        vt.copy_(vh, non_blocking=True)
-        pasa.attn_fwd_alloc(qt, kt, vt, causal=w.causal, mode=args.mode, out=o, lse=lse)
-        oh.copy_(o, non_blocking=True)
-        lh.copy_(lse, non_blocking=True)
+        pasa.attn_fwd_host(qh, kh, vh, causal=w.causal, mode=args.mode, out=oh, lse=lh, chunks=args.host_chunks,
+                           device_buffer=hbuf, sync=False)
 
     for _ in range(2):
         e2e_step()
@@ -479,6 +480,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-also", action="store_true")
+    ap.add_argument("--host-chunks", type=int, default=0,
+                    help="pieces of the host-buffer (e2e) call; 0 = the library's automatic count")
     ap.add_argument("--decode", action="store_true",
                     help="time only the decode step (refresh the cache's last block + attend) on the decode workload")
     args = ap.parse_args()

@@ -110,6 +110,46 @@ int pasa_attn_fwd(const void* q, const void* k, const void* v, void* o, float* l
 int pasa_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
                           int Hkv, int Sq, int Sk, int D, int causal, float scale, int mode, void* stream);
 
+/*
+ * pasa_attn_fwd on HOST buffers: the PASA forward pass ("Online Pseudo-average Shifting
+ * Attention (PASA) for Robust Low-precision LLM Inference", Abstract) computed exactly as
+ * pasa_attn_fwd computes it, for inputs and outputs in host memory. (The paper has no
+ * counterpart: this is a library convenience. It is the one entry point whose tensors are
+ * host pointers.)
+ *   q, k, v   HOST fp16 inputs in the layout above; o HOST fp16 [B, Hq, Sq, D]; lse HOST
+ *             fp32 [B, Hq, Sq] or NULL. No alignment is required. For the copies to
+ *             overlap with the kernels they must be page-locked (cudaHostAlloc /
+ *             cudaHostRegister); pageable memory gives the same results, slower.
+ *   chunks    0 = automatic, else the number of pieces the B * Hkv (batch, kv head) units
+ *             are cut into, clamped to [1, min(B * Hkv, 64)]; negative is an error. The
+ *             automatic count is the largest one <= min(B * Hkv, 8) that leaves every
+ *             piece at least 256 query tiles of 128 rows.
+ *   device_buffer, device_buffer_bytes
+ *             device memory of at least pasa_attn_fwd_host_device_bytes(...) bytes, 256-byte
+ *             aligned: it stages the whole problem (q, k, v, o, lse) and one piece's shift
+ *             workspace. NULL: the call takes it from the stream-ordered allocator on
+ *             `stream` and frees it there.
+ *   stream    the stream the kernels run on. The call only enqueues: o and lse hold the
+ *             result once `stream` has reached the end of this call's work (synchronize
+ *             it, or record an event after the call). Work queued on `stream` earlier is
+ *             finished before any copy of this call starts.
+ * Per piece: its q, k and v go host->device on a side stream, its shift and attention
+ * kernels run on `stream` when they have landed, and its o and lse go device->host on a
+ * second side stream when the kernels are done. Each piece is a problem of n (batch, kv
+ * head) units with one kv head, so the results are bit-identical to pasa_attn_fwd on the
+ * same inputs. The two side streams are non-blocking streams the library creates once per
+ * device and keeps. Errors: as pasa_attn_fwd (shapes and mode), PASA_ERR_WORKSPACE when the
+ * buffer is too small, PASA_ERR_ALIGN when it is not 256-byte aligned; a failure after
+ * enqueueing began still orders `stream` after every copy already queued.
+ */
+int pasa_attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                       int Sq, int Sk, int D, int causal, float scale, int mode, int chunks, void* device_buffer,
+                       size_t device_buffer_bytes, void* stream);
+
+/* Device bytes pasa_attn_fwd_host needs for these sizes, mode and chunk request (0 when the
+ * arguments are invalid). */
+size_t pasa_attn_fwd_host_device_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D, int mode, int chunks);
+
 /* Workspace bytes pasa_attn_fwd_ws needs for these sizes and mode (0 for modes 2 and 3, and
  * for the FP8 modes with D != 128). */
 size_t pasa_attn_fwd_workspace_bytes(int B, int Hkv, int Sk, int D, int mode);

@@ -57,6 +57,8 @@ SIGNATURES = {
     "pasa_attn_fwd_decode_fp8": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P],
                                  _I),
     "pasa_kprep_fp8_blocks": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P], _I),
+    "pasa_attn_fwd_host": ([_P, _P, _P, _P, _P] + [_I] * 7 + [_F, _I, _I, _P, _SZ, _P], _I),
+    "pasa_attn_fwd_host_device_bytes": ([_I] * 8, _SZ),
     "pasa_check_device_error": ([_P, ctypes.POINTER(ctypes.c_ulonglong)], _I),
     "pasa_strerror": ([_I], ctypes.c_char_p),
     "pasa_last_cuda_error": ([], _I),
@@ -161,6 +163,45 @@ def attn_fwd_alloc(q, k, v, causal: bool = False, scale: float | None = None, mo
                            int(bool(causal)), float(scale) if scale is not None else 0.0, int(mode), _stream())
     if rc != 0:
         raise PasaError(rc, "pasa_attn_fwd")
+    return out, lse
+
+
+def _check_host(x: torch.Tensor, name: str, dtype=torch.float16):
+    if not isinstance(x, torch.Tensor) or x.is_cuda or x.dtype != dtype or not x.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous host (CPU) {dtype} tensor")
+
+
+def host_device_bytes(B: int, Hq: int, Hkv: int, Sq: int, Sk: int, D: int, mode: int, chunks: int = 0) -> int:
+    return int(library().pasa_attn_fwd_host_device_bytes(B, Hq, Hkv, Sq, Sk, D, mode, chunks))
+
+
+def attn_fwd_host(q, k, v, causal: bool = False, scale: float | None = None, mode: int = MODE_SHIFT_F16ACC,
+                  out=None, lse=None, chunks: int = 0, device_buffer=None, sync: bool = True):
+    """pasa_attn_fwd_host: q, k, v and the outputs are HOST fp16/fp32 tensors (pin them for
+    the copies to overlap the kernels); the library stages them on the current device in
+    pieces of (batch, kv head) units. With sync=False the call only enqueues on the current
+    stream and out/lse are complete once that stream has been synchronized."""
+    lib = library()
+    _check_host(q, "q"), _check_host(k, "k"), _check_host(v, "v")
+    B, Hq, Sq, D = q.shape
+    _, Hkv, Sk, _ = k.shape
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float16, pin_memory=True)
+    if lse is None:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, pin_memory=True)
+    _check_host(out, "out"), _check_host(lse, "lse", torch.float32)
+    nbytes = 0
+    if device_buffer is not None:
+        if not device_buffer.is_cuda or not device_buffer.is_contiguous():
+            raise TypeError("device_buffer must be a contiguous CUDA tensor")
+        nbytes = device_buffer.numel() * device_buffer.element_size()
+    rc = lib.pasa_attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Sk, D,
+                                int(bool(causal)), float(scale) if scale is not None else 0.0, int(mode),
+                                int(chunks), _ptr(device_buffer), nbytes, _stream())
+    if rc != 0:
+        raise PasaError(rc, "pasa_attn_fwd_host")
+    if sync:
+        torch.cuda.current_stream().synchronize()
     return out, lse
 
 

@@ -169,9 +169,7 @@ int attn_dispatch(int mode, int causal, const CUtensorMap& mq, const CUtensorMap
 #undef PASA_CASE
 }
 
-int validate(const void* q, const void* k, const void* v, const void* o, const float* lse, int B, int Hq, int Hkv,
-             int Sq, int Sk, int D, int mode) {
-  if (!q || !k || !v || !o) return PASA_ERR_NULLPTR;
+int validate_shape(int B, int Hq, int Hkv, int Sq, int Sk, int D, int mode) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Sk <= 0 || Hq % Hkv != 0) return PASA_ERR_SHAPE;
   if (D != 64 && D != 128) return PASA_ERR_UNSUPPORTED;
   if (mode < PASA_MODE_SHIFT_F16ACC || mode > PASA_MODE_NAIVE_FP8) return PASA_ERR_UNSUPPORTED;
@@ -181,6 +179,14 @@ int validate(const void* q, const void* k, const void* v, const void* o, const f
   if (n_qblk * Hq * B > 0x7fffffffLL) return PASA_ERR_SHAPE;
   if (static_cast<long long>(B) * Hq > 0x7fffffffLL || static_cast<long long>(B) * Hkv > 0x7fffffffLL)
     return PASA_ERR_SHAPE;
+  return PASA_OK;
+}
+
+int validate(const void* q, const void* k, const void* v, const void* o, const float* lse, int B, int Hq, int Hkv,
+             int Sq, int Sk, int D, int mode) {
+  if (!q || !k || !v || !o) return PASA_ERR_NULLPTR;
+  const int rc = validate_shape(B, Hq, Hkv, Sq, Sk, D, mode);
+  if (rc != PASA_OK) return rc;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (lse && !aligned16(lse)))
     return PASA_ERR_ALIGN;
   return PASA_OK;
@@ -777,4 +783,208 @@ extern "C" int pasa_attn_fwd_noalloc(const void* q, const void* k, const void* v
   }
   return pasa_attn_fwd_ws(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, mode, ws,
                           need > 0 ? kNoAllocScratchBytes : 0, stream);
+}
+
+// ---------------------------------------------------------------------------------------
+// Host-buffer forward: q, k, v in host memory, o and lse back to host memory, with the
+// copies overlapped with the attention kernels.
+//
+// The (batch, kv head) pairs are the units of work: a unit's query heads, keys, values and
+// outputs are contiguous in the [B, H, S, D] layouts, and a run of consecutive units is
+// itself a problem of n units with one kv head, n = u1 - u0 standing in for B. The units
+// are cut into chunks; chunk i's host->device copies run on one side stream, its shift and
+// attention kernels on the caller's stream once they have landed, and its device->host
+// copies on a second side stream once they have finished. Copy engines and SMs then work
+// at the same time, and only the first chunk's inputs and the last chunk's outputs are
+// not hidden behind computation.
+// ---------------------------------------------------------------------------------------
+namespace {
+
+constexpr int kHostMaxChunks = 64;
+constexpr long long kHostMinChunkTiles = 256;  // query tiles of 128 rows a chunk keeps
+
+struct HostPlan {
+  int units = 0;
+  int chunks = 0;
+  int max_units = 0;         // units in the largest chunk
+  size_t chunk_stride = 0;   // bytes of one unit's q, k, v, o and lse slots together
+  size_t q_bytes = 0, kv_bytes = 0, lse_bytes = 0;  // per unit
+  size_t ws_off = 0, ws_bytes = 0, total = 0;
+};
+
+int host_chunk_begin(const HostPlan& hp, int i) {
+  return static_cast<int>(static_cast<long long>(i) * hp.units / hp.chunks);
+}
+
+// Chunk count: the requested one clamped to [1, min(units, 64)]; 0 asks for as many as
+// keep every chunk at >= 256 query tiles (a few waves of the 152 SMs), at most 8.
+HostPlan host_plan(int B, int Hq, int Hkv, int Sq, int Sk, int D, int mode, int chunks) {
+  HostPlan hp;
+  hp.units = B * Hkv;
+  const int g = Hq / Hkv;
+  const int cap = hp.units < kHostMaxChunks ? hp.units : kHostMaxChunks;
+  if (chunks <= 0) {
+    const long long tiles = static_cast<long long>(g) * ((static_cast<long long>(Sq) + 127) / 128);
+    int c = cap < 8 ? cap : 8;
+    while (c > 1 && (hp.units / c) * tiles < kHostMinChunkTiles) --c;
+    chunks = c;
+  }
+  hp.chunks = chunks < cap ? chunks : cap;
+  hp.max_units = 0;
+  for (int i = 0; i < hp.chunks; ++i) {
+    const int n = host_chunk_begin(hp, i + 1) - host_chunk_begin(hp, i);
+    if (n > hp.max_units) hp.max_units = n;
+  }
+  hp.q_bytes = static_cast<size_t>(g) * Sq * D * 2;
+  hp.kv_bytes = static_cast<size_t>(Sk) * D * 2;
+  hp.lse_bytes = static_cast<size_t>(g) * Sq * 4;
+  // chunk slots: q, k, v, o, lse of the whole problem, each slot of each chunk 256-aligned
+  size_t off = 0;
+  for (int i = 0; i < hp.chunks; ++i) {
+    const size_t n = static_cast<size_t>(host_chunk_begin(hp, i + 1) - host_chunk_begin(hp, i));
+    off += 2 * align_up(n * hp.q_bytes, 256) + 2 * align_up(n * hp.kv_bytes, 256) + align_up(n * hp.lse_bytes, 256);
+  }
+  hp.ws_off = off;
+  hp.ws_bytes = pasa_attn_fwd_workspace_bytes(hp.max_units, 1, Sk, D, mode);
+  hp.total = align_up(off + hp.ws_bytes, 256);
+  return hp;
+}
+
+// One pair of non-blocking copy streams per device, created on first use and kept for the
+// life of the process. Calls from several host threads may share them: every wait a call
+// enqueues refers to work that call has already enqueued, so the order stays acyclic.
+std::mutex g_copy_mutex;
+cudaStream_t g_copy_streams[kNoAllocMaxDevices][2] = {};
+
+int copy_streams(cudaStream_t* h2d, cudaStream_t* d2h) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return PASA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_copy_mutex);
+  for (int j = 0; j < 2; ++j) {
+    if (g_copy_streams[dev][j] == nullptr) {
+      e = cudaStreamCreateWithFlags(&g_copy_streams[dev][j], cudaStreamNonBlocking);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+  }
+  *h2d = g_copy_streams[dev][0];
+  *d2h = g_copy_streams[dev][1];
+  return PASA_OK;
+}
+
+}  // namespace
+
+extern "C" size_t pasa_attn_fwd_host_device_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D, int mode,
+                                                   int chunks) {
+  if (chunks < 0 || validate_shape(B, Hq, Hkv, Sq, Sk, D, mode) != PASA_OK) return 0;
+  return host_plan(B, Hq, Hkv, Sq, Sk, D, mode, chunks).total;
+}
+
+extern "C" int pasa_attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                                  int Hkv, int Sq, int Sk, int D, int causal, float scale, int mode, int chunks,
+                                  void* device_buffer, size_t device_buffer_bytes, void* stream) {
+  if (!q || !k || !v || !o) return PASA_ERR_NULLPTR;
+  int rc = validate_shape(B, Hq, Hkv, Sq, Sk, D, mode);
+  if (rc != PASA_OK) return rc;
+  if (chunks < 0) return PASA_ERR_SHAPE;
+  const HostPlan hp = host_plan(B, Hq, Hkv, Sq, Sk, D, mode, chunks);
+  if (device_buffer) {
+    if (device_buffer_bytes < hp.total) return PASA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(device_buffer) & 255u) != 0) return PASA_ERR_ALIGN;
+  }
+  rc = check_device();
+  if (rc != PASA_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaStream_t s_in = nullptr, s_out = nullptr;
+  rc = copy_streams(&s_in, &s_out);
+  if (rc != PASA_OK) return rc;
+
+  // events: [0] start on st, [1] h2d stream done, [2] d2h stream done,
+  // [3 + i] chunk i's inputs landed, [3 + chunks + i] chunk i's kernels finished
+  const int n_ev = 3 + 2 * hp.chunks;
+  cudaEvent_t ev[3 + 2 * kHostMaxChunks] = {};
+  cudaError_t e = cudaSuccess;
+  int made = 0;
+  for (; made < n_ev; ++made) {
+    e = cudaEventCreateWithFlags(&ev[made], cudaEventDisableTiming);
+    if (e != cudaSuccess) break;
+  }
+  uint8_t* buf = static_cast<uint8_t*>(device_buffer);
+  bool owned = false;
+  if (e == cudaSuccess && !buf) {
+    e = cudaMallocAsync(reinterpret_cast<void**>(&buf), hp.total, st);
+    owned = e == cudaSuccess;
+  }
+  if (e != cudaSuccess) {
+    for (int j = 0; j < made; ++j) cudaEventDestroy(ev[j]);
+    return cuda_fail(e);
+  }
+
+  // Everything below is enqueued on st, s_in or s_out; on the first failure the rest is
+  // skipped, but the side streams are still joined back to st before the buffer is freed.
+  auto step = [&](cudaError_t err) {
+    if (e == cudaSuccess && err != cudaSuccess) e = err;
+    return e == cudaSuccess;
+  };
+  const uint8_t* qh = static_cast<const uint8_t*>(q);
+  const uint8_t* kh = static_cast<const uint8_t*>(k);
+  const uint8_t* vh = static_cast<const uint8_t*>(v);
+  uint8_t* oh = static_cast<uint8_t*>(o);
+  uint8_t* lh = reinterpret_cast<uint8_t*>(lse);
+  struct Slot { uint8_t *q, *k, *v, *o, *lse; size_t n; int u0; };
+  Slot slot[kHostMaxChunks];
+  size_t off = 0;
+  for (int i = 0; i < hp.chunks; ++i) {
+    Slot& s = slot[i];
+    s.u0 = host_chunk_begin(hp, i);
+    s.n = static_cast<size_t>(host_chunk_begin(hp, i + 1) - s.u0);
+    s.q = buf + off;  off += align_up(s.n * hp.q_bytes, 256);
+    s.k = buf + off;  off += align_up(s.n * hp.kv_bytes, 256);
+    s.v = buf + off;  off += align_up(s.n * hp.kv_bytes, 256);
+    s.o = buf + off;  off += align_up(s.n * hp.q_bytes, 256);
+    s.lse = buf + off; off += align_up(s.n * hp.lse_bytes, 256);
+  }
+  // the buffer may still be in use by work the caller queued on st before this call
+  step(cudaEventRecord(ev[0], st));
+  step(cudaStreamWaitEvent(s_in, ev[0], 0));
+  step(cudaStreamWaitEvent(s_out, ev[0], 0));
+  for (int i = 0; i < hp.chunks && e == cudaSuccess; ++i) {
+    const Slot& s = slot[i];
+    step(cudaMemcpyAsync(s.k, kh + s.u0 * hp.kv_bytes, s.n * hp.kv_bytes, cudaMemcpyHostToDevice, s_in));
+    step(cudaMemcpyAsync(s.v, vh + s.u0 * hp.kv_bytes, s.n * hp.kv_bytes, cudaMemcpyHostToDevice, s_in));
+    step(cudaMemcpyAsync(s.q, qh + s.u0 * hp.q_bytes, s.n * hp.q_bytes, cudaMemcpyHostToDevice, s_in));
+    step(cudaEventRecord(ev[3 + i], s_in));
+  }
+  const int g = Hq / Hkv;
+  for (int i = 0; i < hp.chunks && e == cudaSuccess; ++i) {
+    const Slot& s = slot[i];
+    if (!step(cudaStreamWaitEvent(st, ev[3 + i], 0))) break;
+    const int krc = pasa_attn_fwd_ws(s.q, s.k, s.v, s.o, lse ? reinterpret_cast<float*>(s.lse) : nullptr,
+                                     static_cast<int>(s.n), g, 1, Sq, Sk, D, causal, scale, mode,
+                                     hp.ws_bytes ? buf + hp.ws_off : nullptr, hp.ws_bytes, st);
+    if (krc != PASA_OK) {
+      rc = krc;
+      break;
+    }
+    step(cudaEventRecord(ev[3 + hp.chunks + i], st));
+    step(cudaStreamWaitEvent(s_out, ev[3 + hp.chunks + i], 0));
+    step(cudaMemcpyAsync(oh + s.u0 * hp.q_bytes, s.o, s.n * hp.q_bytes, cudaMemcpyDeviceToHost, s_out));
+    if (lse) step(cudaMemcpyAsync(lh + s.u0 * hp.lse_bytes, s.lse, s.n * hp.lse_bytes, cudaMemcpyDeviceToHost, s_out));
+  }
+  // join: st continues only after both side streams have drained this call's copies
+  cudaError_t je = cudaEventRecord(ev[1], s_in);
+  if (je == cudaSuccess) je = cudaStreamWaitEvent(st, ev[1], 0);
+  if (je == cudaSuccess) je = cudaEventRecord(ev[2], s_out);
+  if (je == cudaSuccess) je = cudaStreamWaitEvent(st, ev[2], 0);
+  if (je != cudaSuccess) {
+    // st cannot be ordered after the side streams: wait for them here before freeing
+    cudaStreamSynchronize(s_in);
+    cudaStreamSynchronize(s_out);
+    step(je);
+  }
+  if (owned) step(cudaFreeAsync(buf, st));
+  for (int j = 0; j < n_ev; ++j) cudaEventDestroy(ev[j]);
+  if (rc != PASA_OK) return rc;
+  return e == cudaSuccess ? PASA_OK : cuda_fail(e);
 }

@@ -237,3 +237,45 @@ def test_fp8_decode_entry_points_check_arguments(lib):
     assert kb(P(FAKE), P(FAKE), P(FAKE), P(FAKE), 1, 1, 300, 300, 64, 5, 0, None) == -3
     assert kb(P(FAKE), P(FAKE), P(FAKE), P(FAKE), 1, 1, 300, 300, 128, 1, 0, None) == -3
     assert kb(P(FAKE_MIS), P(FAKE), P(FAKE), P(FAKE), 1, 1, 300, 300, 128, 6, 0, None) == -4
+
+
+def test_host_buffer_entry_checks_arguments(lib):
+    P = ctypes.c_void_p
+    # pasa_attn_fwd_host(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, mode, chunks, buf, buf_bytes, stream)
+    def host(q=FAKE, o=FAKE, B=1, Hq=8, Hkv=2, Sq=300, Sk=300, D=128, mode=0, chunks=0, buf=FAKE, nbytes=None):
+        if nbytes is None:
+            nbytes = lib.pasa_attn_fwd_host_device_bytes(B, Hq, Hkv, Sq, Sk, D, mode, chunks)
+        return lib.pasa_attn_fwd_host(P(q) if q else None, P(FAKE), P(FAKE), P(o) if o else None, None, B, Hq, Hkv,
+                                      Sq, Sk, D, 1, 0.0, mode, chunks, P(buf) if buf else None, nbytes, None)
+
+    assert host(q=0) == -1 and host(o=0) == -1
+    assert host(Hq=7) == -2 and host(Sk=0) == -2 and host(chunks=-1) == -2
+    assert host(D=96) == -3 and host(mode=9) == -3 and host(D=64, mode=5) == -3
+    nbytes = lib.pasa_attn_fwd_host_device_bytes(1, 8, 2, 300, 300, 128, 0, 0)
+    assert host(nbytes=nbytes - 1) == -7                 # buffer too small
+    assert host(buf=FAKE + 128, nbytes=nbytes) == -4     # buffer not 256-byte aligned
+    # host pointers need no alignment: a misaligned q gets past argument checks to the
+    # device query, which fails here (no GPU) instead of reporting PASA_ERR_ALIGN
+    assert host(q=FAKE_MIS) != -4
+
+
+def test_host_buffer_device_bytes(lib):
+    nb = lib.pasa_attn_fwd_host_device_bytes
+    assert nb(1, 8, 2, 300, 300, 128, 0, -1) == 0 and nb(1, 7, 2, 300, 300, 128, 0, 0) == 0
+    for (B, Hq, Hkv, Sq, Sk, D) in [(1, 28, 4, 32768, 32768, 128), (2, 5, 5, 9216, 9216, 64), (8, 28, 4, 1, 4096, 128),
+                                    (3, 6, 3, 129, 257, 64)]:
+        units = B * Hkv
+        problem = 2 * B * Hq * Sq * D * 2 + 2 * B * Hkv * Sk * D * 2 + B * Hq * Sq * 4
+        for mode in (0, 2, 5):
+            if mode == 5 and D != 128:
+                continue
+            for chunks in (1, 2, 3, units, units + 5):
+                n = min(chunks, units)
+                biggest = -(-units // n)
+                got = nb(B, Hq, Hkv, Sq, Sk, D, mode, chunks)
+                # whole problem staged + one piece's workspace, slots 256-byte aligned
+                ws = lib.pasa_attn_fwd_workspace_bytes(biggest, 1, Sk, D, mode)
+                assert problem + ws <= got <= problem + ws + 5 * 256 * n + 256, (B, Hq, Hkv, Sq, Sk, D, mode, chunks)
+                assert got % 256 == 0
+            # automatic chunking stages the same problem
+            assert nb(B, Hq, Hkv, Sq, Sk, D, mode, 0) >= problem

@@ -1,0 +1,137 @@
+"""GPU tests of pasa_attn_fwd_host: the PASA forward pass ("Online Pseudo-average Shifting
+Attention (PASA) for Robust Low-precision LLM Inference", Abstract) on host buffers, staged
+to the device in pieces of (batch, kv head) units with the copies overlapped.
+
+Each piece is the same computation on a sub-problem with one kv head, so the host-buffer
+call must agree BIT FOR BIT with pasa_attn_fwd on device copies of the same inputs, for
+every mode, piece count and memory kind (pinned or pageable). One small case is also
+checked against the fp64 oracle directly, with the bounds of the attention parity tests.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from gpu_helpers import lse_tolerance, rel_errors, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def pasa():
+    import precision_flashattention_numerics_gb300 as p
+
+    return p
+
+
+def make(B, Hq, Hkv, Sq, Sk, D, kind, seed, **params):
+    w = wl.Workload("host", B, Hq, Hkv, Sq, Sk, D, False, kind, seed, tuple(sorted(params.items())))
+    return wl.make_inputs(w)
+
+
+def host_tensors(q, k, v, pinned=True):
+    ts = [torch.from_numpy(np.ascontiguousarray(x)) for x in (q, k, v)]
+    return [t.pin_memory() for t in ts] if pinned else ts
+
+
+def device_result(q, k, v, causal, mode):
+    p = pasa()
+    qt, kt, vt = to_dev(q, k, v)
+    o, lse = p.attn_fwd_alloc(qt, kt, vt, causal=causal, mode=mode)
+    torch.cuda.synchronize()
+    return o.cpu(), lse.cpu()
+
+
+CASES = [
+    # (B, Hq, Hkv, Sq, Sk, D, causal, kind, params)
+    (2, 8, 4, 520, 520, 128, True, "iid", {}),
+    (3, 6, 3, 300, 700, 64, True, "kbias", {"bias_std": 20.0}),
+    (1, 4, 4, 257, 1000, 128, False, "kbias_t3", {"bias_std": 10.0, "t_dof": 3, "t_scale": 4.0}),
+    (4, 8, 2, 1, 900, 128, True, "iid", {}),      # one query row per head
+]
+
+
+@pytest.mark.parametrize("case", range(len(CASES)))
+@pytest.mark.parametrize("mode", [0, 1, 2, 3, 4, 5, 6])
+def test_host_matches_device(case, mode):
+    B, Hq, Hkv, Sq, Sk, D, causal, kind, params = CASES[case]
+    if mode >= 5 and D != 128:
+        pytest.skip("FP8 modes: D = 128")
+    p = pasa()
+    q, k, v = make(B, Hq, Hkv, Sq, Sk, D, kind, 700 + case, **params)
+    o_ref, lse_ref = device_result(q, k, v, causal, mode)
+    qh, kh, vh = host_tensors(q, k, v)
+    units = B * Hkv
+    for chunks in sorted({0, 1, 2, 3, units, units + 3}):
+        o, lse = p.attn_fwd_host(qh, kh, vh, causal=causal, mode=mode, chunks=chunks)
+        p.check_device_error()
+        assert torch.equal(o, o_ref), (mode, chunks)
+        assert torch.equal(lse, lse_ref), (mode, chunks)
+
+
+def test_host_pageable_and_own_buffer():
+    p = pasa()
+    B, Hq, Hkv, Sq, Sk, D = 2, 8, 4, 520, 520, 128
+    q, k, v = make(B, Hq, Hkv, Sq, Sk, D, "kbias", 731, bias_std=20.0)
+    o_ref, lse_ref = device_result(q, k, v, True, 0)
+    qh, kh, vh = host_tensors(q, k, v, pinned=False)
+    out = torch.empty(q.shape, dtype=torch.float16)
+    lse = torch.empty((B, Hq, Sq), dtype=torch.float32)
+    nbytes = p.host_device_bytes(B, Hq, Hkv, Sq, Sk, D, 0, 3)
+    buf = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    p.attn_fwd_host(qh, kh, vh, causal=True, mode=0, out=out, lse=lse, chunks=3, device_buffer=buf)
+    assert torch.equal(out, o_ref) and torch.equal(lse, lse_ref)
+    # a buffer one byte short is refused before anything is enqueued
+    with pytest.raises(p.PasaError):
+        p.attn_fwd_host(qh, kh, vh, causal=True, mode=0, out=out, lse=lse, chunks=3, device_buffer=buf[:-1])
+
+
+def test_host_without_lse():
+    p = pasa()
+    lib = p.library()
+    B, Hq, Hkv, Sq, Sk, D = 1, 4, 2, 300, 300, 64
+    q, k, v = make(B, Hq, Hkv, Sq, Sk, D, "iid", 732)
+    o_ref, _ = device_result(q, k, v, False, 1)
+    qh, kh, vh = host_tensors(q, k, v)
+    out = torch.empty(q.shape, dtype=torch.float16).pin_memory()
+    P = ctypes.c_void_p
+    rc = lib.pasa_attn_fwd_host(P(qh.data_ptr()), P(kh.data_ptr()), P(vh.data_ptr()), P(out.data_ptr()), None, B, Hq,
+                                Hkv, Sq, Sk, D, 0, 0.0, 1, 2, None, 0,
+                                P(torch.cuda.current_stream().cuda_stream))
+    assert rc == 0
+    torch.cuda.current_stream().synchronize()
+    assert torch.equal(out, o_ref)
+
+
+def test_host_calls_queue_in_order_on_one_buffer():
+    """Back-to-back calls without a host synchronisation, sharing one device buffer: each
+    call's copies wait for the work queued before it, so neither result is overwritten."""
+    p = pasa()
+    B, Hq, Hkv, Sq, Sk, D = 2, 8, 4, 1030, 1030, 128
+    ins = [make(B, Hq, Hkv, Sq, Sk, D, "kbias", 740 + i, bias_std=10.0) for i in range(3)]
+    refs = [device_result(*x, True, 0) for x in ins]
+    buf = torch.empty(p.host_device_bytes(B, Hq, Hkv, Sq, Sk, D, 0, 4), dtype=torch.uint8, device="cuda")
+    outs = []
+    for x in ins:
+        qh, kh, vh = host_tensors(*x)
+        outs.append(p.attn_fwd_host(qh, kh, vh, causal=True, mode=0, chunks=4, device_buffer=buf, sync=False))
+    torch.cuda.current_stream().synchronize()
+    p.check_device_error()
+    for (o, lse), (o_ref, lse_ref) in zip(outs, refs):
+        assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
+
+
+def test_host_against_oracle():
+    p = pasa()
+    B, Hq, Hkv, Sq, Sk, D = 2, 4, 2, 333, 333, 128
+    q, k, v = make(B, Hq, Hkv, Sq, Sk, D, "kbias", 733, bias_std=20.0)
+    qh, kh, vh = host_tensors(q, k, v)
+    o, lse = p.attn_fwd_host(qh, kh, vh, causal=True, mode=0, chunks=0)
+    o_ref, lse_ref = oracle.attention(q, k, v, causal=True)
+    rmse, _ = rel_errors(o.double().numpy(), o_ref)
+    assert rmse <= 5e-3
+    assert np.all(np.isfinite(o.float().numpy()))
+    tol = lse_tolerance(q, k, True, 0, D)
+    assert np.max(np.abs(lse.double().numpy() - lse_ref)) <= tol
