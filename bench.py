@@ -293,7 +293,7 @@ def bench_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int, also
     lh = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
     B, Hq, Sq, D = qt.shape
     Hkv, Sk = kt.shape[1], kt.shape[2]
-    hbuf = torch.empty(pasa.host_device_bytes(B, Hq, Hkv, Sq, Sk, D, args.mode, args.host_chunks),
+    hbuf = torch.empty(pasa.host_device_bytes(B, Hq, Hkv, Sq, Sk, D, w.causal, args.mode, args.host_chunks),
                        dtype=torch.uint8, device=qt.device)
 
     def e2e_step():

@@ -122,33 +122,52 @@ int pasa_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, 
  *             cudaHostRegister); pageable memory gives the same results, slower.
  *   chunks    0 = automatic, else the number of pieces the B * Hkv (batch, kv head) units
  *             are cut into, clamped to [1, min(B * Hkv, 64)]; negative is an error. The
- *             automatic count is the largest one <= min(B * Hkv, 8) that leaves every
- *             piece at least 256 query tiles of 128 rows.
+ *             automatic plan takes the largest count <= min(B * Hkv, 8) that leaves every
+ *             piece at least 256 query tiles of 128 rows, and also cuts the first and the
+ *             last unit along the query rows into pieces that halve towards the ends
+ *             (Sq/2, Sq/4, Sq/8 rows; the smallest keeps >= 128 query tiles), so that
+ *             little of the copying waits on, or is waited on by, the kernels. Row pieces
+ *             start on 128-row tiles and, under the causal mask, see a key prefix ending
+ *             on a 128-key block; they are used only where that holds (not causal, or
+ *             Sk >= Sq with Sk - Sq a multiple of 128).
  *   device_buffer, device_buffer_bytes
  *             device memory of at least pasa_attn_fwd_host_device_bytes(...) bytes, 256-byte
- *             aligned: it stages the whole problem (q, k, v, o, lse) and one piece's shift
- *             workspace. NULL: the call takes it from the stream-ordered allocator on
- *             `stream` and frees it there.
+ *             aligned: it stages the whole problem (q, k, v, o, lse) and two shift
+ *             workspaces, one per compute stream. Its contents on entry do not matter.
+ *             NULL: the call takes it from the stream-ordered allocator on `stream` and
+ *             frees it there.
  *   stream    the stream the kernels run on. The call only enqueues: o and lse hold the
  *             result once `stream` has reached the end of this call's work (synchronize
  *             it, or record an event after the call). Work queued on `stream` earlier is
  *             finished before any copy of this call starts.
- * Per piece: its q, k and v go host->device on a side stream, its shift and attention
- * kernels run on `stream` when they have landed, and its o and lse go device->host on a
- * second side stream when the kernels are done. Each piece is a problem of n (batch, kv
- * head) units with one kv head, so the results are bit-identical to pasa_attn_fwd on the
- * same inputs. The two side streams are non-blocking streams the library creates once per
- * device and keeps. Errors: as pasa_attn_fwd (shapes and mode), PASA_ERR_WORKSPACE when the
- * buffer is too small, PASA_ERR_ALIGN when it is not 256-byte aligned; a failure after
- * enqueueing began still orders `stream` after every copy already queued.
+ * Per piece: its q, k and v go host->device on a side stream; its shift and attention
+ * kernels run once they have landed, pieces alternating between `stream` and a second
+ * compute stream so that one piece's last tiles overlap the next piece's first; its o and
+ * lse go device->host on another side stream once the kernels are done. A piece is a
+ * problem of n (batch, kv head) units with one kv head, or query rows [r0, r1) of one unit
+ * with the keys they see, and every query tile meets the same key blocks and
+ * pseudo-averages as in one call: the results are bit-identical to pasa_attn_fwd on the
+ * same inputs. The three side streams are non-blocking streams the library creates once
+ * per device and keeps. Errors: as pasa_attn_fwd (shapes and mode), PASA_ERR_WORKSPACE
+ * when the buffer is too small, PASA_ERR_ALIGN when it is not 256-byte aligned; a failure
+ * after enqueueing began still orders `stream` after all work already queued.
  */
 int pasa_attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                        int Sq, int Sk, int D, int causal, float scale, int mode, int chunks, void* device_buffer,
                        size_t device_buffer_bytes, void* stream);
 
-/* Device bytes pasa_attn_fwd_host needs for these sizes, mode and chunk request (0 when the
- * arguments are invalid). */
-size_t pasa_attn_fwd_host_device_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D, int mode, int chunks);
+/* The pieces pasa_attn_fwd_host runs for these arguments, in order: writes min(count,
+ * max_pieces) records of six ints (u0, n, r0, r1, k0, k1) to `pieces` (host memory) and
+ * returns the count, or a negative status (argument errors as pasa_attn_fwd_host; NULL
+ * pieces with max_pieces > 0 is PASA_ERR_NULLPTR). A record stands for query rows [r0, r1)
+ * of the units [u0, u0 + n) attending keys [0, k1); its copy-in adds keys [k0, k1). */
+int pasa_attn_fwd_host_plan(int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, int mode, int chunks,
+                            int* pieces, int max_pieces);
+
+/* Device bytes pasa_attn_fwd_host needs for these sizes, masking, mode and chunk request (0
+ * when the arguments are invalid). */
+size_t pasa_attn_fwd_host_device_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, int mode,
+                                       int chunks);
 
 /* Workspace bytes pasa_attn_fwd_ws needs for these sizes and mode (0 for modes 2 and 3, and
  * for the FP8 modes with D != 128). */

@@ -58,7 +58,8 @@ SIGNATURES = {
                                  _I),
     "pasa_kprep_fp8_blocks": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P], _I),
     "pasa_attn_fwd_host": ([_P, _P, _P, _P, _P] + [_I] * 7 + [_F, _I, _I, _P, _SZ, _P], _I),
-    "pasa_attn_fwd_host_device_bytes": ([_I] * 8, _SZ),
+    "pasa_attn_fwd_host_device_bytes": ([_I] * 9, _SZ),
+    "pasa_attn_fwd_host_plan": ([_I] * 9 + [_P, _I], _I),
     "pasa_check_device_error": ([_P, ctypes.POINTER(ctypes.c_ulonglong)], _I),
     "pasa_strerror": ([_I], ctypes.c_char_p),
     "pasa_last_cuda_error": ([], _I),
@@ -171,8 +172,21 @@ def _check_host(x: torch.Tensor, name: str, dtype=torch.float16):
         raise TypeError(f"{name} must be a contiguous host (CPU) {dtype} tensor")
 
 
-def host_device_bytes(B: int, Hq: int, Hkv: int, Sq: int, Sk: int, D: int, mode: int, chunks: int = 0) -> int:
-    return int(library().pasa_attn_fwd_host_device_bytes(B, Hq, Hkv, Sq, Sk, D, mode, chunks))
+def host_device_bytes(B: int, Hq: int, Hkv: int, Sq: int, Sk: int, D: int, causal: bool, mode: int,
+                      chunks: int = 0) -> int:
+    return int(library().pasa_attn_fwd_host_device_bytes(B, Hq, Hkv, Sq, Sk, D, int(bool(causal)), mode, chunks))
+
+
+def host_plan(B: int, Hq: int, Hkv: int, Sq: int, Sk: int, D: int, causal: bool, mode: int, chunks: int = 0):
+    """The pieces attn_fwd_host runs: a list of (u0, n, r0, r1, k0, k1)."""
+    lib = library()
+    args = (B, Hq, Hkv, Sq, Sk, D, int(bool(causal)), int(mode), int(chunks))
+    count = lib.pasa_attn_fwd_host_plan(*args, None, 0)
+    if count < 0:
+        raise PasaError(count, "pasa_attn_fwd_host_plan")
+    rec = (ctypes.c_int * (6 * max(count, 1)))()
+    lib.pasa_attn_fwd_host_plan(*args, ctypes.cast(rec, ctypes.c_void_p), count)
+    return [tuple(rec[6 * i:6 * i + 6]) for i in range(count)]
 
 
 def attn_fwd_host(q, k, v, causal: bool = False, scale: float | None = None, mode: int = MODE_SHIFT_F16ACC,

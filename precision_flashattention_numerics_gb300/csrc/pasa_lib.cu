@@ -791,94 +791,199 @@ extern "C" int pasa_attn_fwd_noalloc(const void* q, const void* k, const void* v
 //
 // The (batch, kv head) pairs are the units of work: a unit's query heads, keys, values and
 // outputs are contiguous in the [B, H, S, D] layouts, and a run of consecutive units is
-// itself a problem of n units with one kv head, n = u1 - u0 standing in for B. The units
-// are cut into chunks; chunk i's host->device copies run on one side stream, its shift and
-// attention kernels on the caller's stream once they have landed, and its device->host
-// copies on a second side stream once they have finished. Copy engines and SMs then work
-// at the same time, and only the first chunk's inputs and the last chunk's outputs are
-// not hidden behind computation.
+// itself a problem of n units with one kv head, n standing in for B. The work is cut into
+// pieces; piece i's host->device copies run on one side stream, its shift and attention
+// kernels on the caller's stream once they have landed, and its device->host copies on a
+// second side stream once they have finished. Copy engines and SMs then work at the same
+// time, and only the first piece's inputs and the last piece's outputs are not hidden
+// behind computation.
+//
+// To keep those two small, the automatic plan also cuts the first and the last unit along
+// the query rows, in pieces that halve towards the ends ([0, Sq/8), [Sq/8, Sq/4),
+// [Sq/4, Sq/2), ... for the first unit, mirrored for the last). A row piece [r0, r1) is the
+// problem with Sq' = r1 - r0 query rows and, under the causal mask, the key prefix
+// Sk' = r1 + Sk - Sq it can see: row r0 + i' sees key j iff j <= i' + Sk' - Sq', the same
+// keys as before. With r0 on a 128-row tile boundary and Sk' on a 128-key block boundary
+// (or Sk' = Sk) every query tile meets the same key blocks with the same pseudo-averages,
+// so the results stay bit-identical to the single call. The unit's keys are copied once,
+// in the slices each row piece adds.
 // ---------------------------------------------------------------------------------------
+#include <vector>
+
 namespace {
 
 constexpr int kHostMaxChunks = 64;
-constexpr long long kHostMinChunkTiles = 256;  // query tiles of 128 rows a chunk keeps
+constexpr long long kHostMinChunkTiles = 256;  // query tiles of 128 rows a unit chunk keeps
+constexpr long long kHostMinRowTiles = 128;    // ... and the smallest row piece keeps
+constexpr int kHostMaxHalvings = 3;
+
+struct HostPiece {
+  int u0 = 0, n = 0;    // units [u0, u0 + n)
+  int r0 = 0, r1 = 0;   // query rows [r0, r1) of each unit
+  int k0 = 0, k1 = 0;   // keys this piece copies in; it attends keys [0, k1)
+  size_t q_off = 0, kv_off = 0, o_off = 0, lse_off = 0;  // slots in the device buffer
+};
 
 struct HostPlan {
-  int units = 0;
-  int chunks = 0;
-  int max_units = 0;         // units in the largest chunk
-  size_t chunk_stride = 0;   // bytes of one unit's q, k, v, o and lse slots together
-  size_t q_bytes = 0, kv_bytes = 0, lse_bytes = 0;  // per unit
+  std::vector<HostPiece> pieces;
+  int max_units = 0;  // units in the largest piece
   size_t ws_off = 0, ws_bytes = 0, total = 0;
 };
 
-int host_chunk_begin(const HostPlan& hp, int i) {
-  return static_cast<int>(static_cast<long long>(i) * hp.units / hp.chunks);
+// Row boundaries for one unit: halving pieces at the front and/or the back, on 128-row
+// tiles, the smallest with at least kHostMinRowTiles tiles over the unit's g heads.
+std::vector<int> host_row_cuts(int Sq, int g, bool front, bool back) {
+  std::vector<int> cuts{0};
+  int halvings = 0;
+  while (halvings < kHostMaxHalvings) {
+    const long long rows = (static_cast<long long>(Sq) >> (halvings + 1)) / 128 * 128;
+    if (rows <= 0 || static_cast<long long>(g) * (rows / 128) < kHostMinRowTiles) break;
+    ++halvings;
+  }
+  if (halvings == 0 || (!front && !back)) {
+    cuts.push_back(Sq);
+    return cuts;
+  }
+  auto tile = [](long long r) { return static_cast<int>(r / 128 * 128); };
+  if (front)
+    for (int h = halvings; h >= 1; --h) cuts.push_back(tile(static_cast<long long>(Sq) >> h));
+  else
+    cuts.push_back(tile(static_cast<long long>(Sq) >> 1));
+  if (back)
+    for (int h = 2; h <= halvings; ++h) cuts.push_back(tile(Sq - (static_cast<long long>(Sq) >> h)));
+  cuts.push_back(Sq);
+  std::vector<int> out{0};
+  for (size_t i = 1; i < cuts.size(); ++i)
+    if (cuts[i] > out.back()) out.push_back(cuts[i]);
+  return out;
 }
 
-// Chunk count: the requested one clamped to [1, min(units, 64)]; 0 asks for as many as
-// keep every chunk at >= 256 query tiles (a few waves of the 152 SMs), at most 8.
-HostPlan host_plan(int B, int Hq, int Hkv, int Sq, int Sk, int D, int mode, int chunks) {
+// Pieces: the units cut into chunks (the requested count clamped to [1, min(units, 64)];
+// 0 asks for as many as keep every chunk at >= 256 query tiles, at most 8). Only the
+// automatic plan cuts the first and last unit into row pieces, and only where the row
+// pieces keep the computation tile-for-tile the same (see above).
+HostPlan host_plan(int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, int mode, int chunks) {
   HostPlan hp;
-  hp.units = B * Hkv;
+  const int units = B * Hkv;
   const int g = Hq / Hkv;
-  const int cap = hp.units < kHostMaxChunks ? hp.units : kHostMaxChunks;
-  if (chunks <= 0) {
+  const int cap = units < kHostMaxChunks ? units : kHostMaxChunks;
+  const bool automatic = chunks <= 0;
+  if (automatic) {
     const long long tiles = static_cast<long long>(g) * ((static_cast<long long>(Sq) + 127) / 128);
     int c = cap < 8 ? cap : 8;
-    while (c > 1 && (hp.units / c) * tiles < kHostMinChunkTiles) --c;
+    while (c > 1 && (units / c) * tiles < kHostMinChunkTiles) --c;
     chunks = c;
   }
-  hp.chunks = chunks < cap ? chunks : cap;
-  hp.max_units = 0;
-  for (int i = 0; i < hp.chunks; ++i) {
-    const int n = host_chunk_begin(hp, i + 1) - host_chunk_begin(hp, i);
-    if (n > hp.max_units) hp.max_units = n;
+  chunks = chunks < cap ? chunks : cap;
+  const bool rows_ok = automatic && (!causal || (Sk >= Sq && (Sk - Sq) % 128 == 0));
+  for (int c = 0; c < chunks; ++c) {
+    const int a = static_cast<int>(static_cast<long long>(c) * units / chunks);
+    const int b = static_cast<int>(static_cast<long long>(c + 1) * units / chunks);
+    for (int u = a; u < b;) {
+      const bool first = u == 0, last = u == units - 1;
+      std::vector<int> cuts{0, Sq};
+      if (rows_ok && (first || last)) cuts = host_row_cuts(Sq, g, first, last);
+      if (cuts.size() > 2) {
+        int kprev = 0;
+        for (size_t i = 0; i + 1 < cuts.size(); ++i) {
+          HostPiece pc;
+          pc.u0 = u, pc.n = 1, pc.r0 = cuts[i], pc.r1 = cuts[i + 1];
+          pc.k1 = causal ? pc.r1 + (Sk - Sq) : Sk;
+          pc.k0 = kprev;
+          kprev = pc.k1;
+          hp.pieces.push_back(pc);
+        }
+        ++u;
+        continue;
+      }
+      // a run of whole units up to the chunk's end or the next unit that is cut into rows
+      int e = u + 1;
+      while (e < b && !(rows_ok && e == units - 1 && host_row_cuts(Sq, g, false, true).size() > 2)) ++e;
+      HostPiece pc;
+      pc.u0 = u, pc.n = e - u, pc.r0 = 0, pc.r1 = Sq, pc.k0 = 0, pc.k1 = Sk;
+      hp.pieces.push_back(pc);
+      u = e;
+    }
   }
-  hp.q_bytes = static_cast<size_t>(g) * Sq * D * 2;
-  hp.kv_bytes = static_cast<size_t>(Sk) * D * 2;
-  hp.lse_bytes = static_cast<size_t>(g) * Sq * 4;
-  // chunk slots: q, k, v, o, lse of the whole problem, each slot of each chunk 256-aligned
-  size_t off = 0;
-  for (int i = 0; i < hp.chunks; ++i) {
-    const size_t n = static_cast<size_t>(host_chunk_begin(hp, i + 1) - host_chunk_begin(hp, i));
-    off += 2 * align_up(n * hp.q_bytes, 256) + 2 * align_up(n * hp.kv_bytes, 256) + align_up(n * hp.lse_bytes, 256);
+  // slots: q and o [n, g, rows, D], lse [n, g, rows], and the keys/values [n, Sk, D] of a
+  // unit once (row pieces after the first of a unit reuse it); each 256-byte aligned
+  const size_t row_bytes = static_cast<size_t>(D) * 2;
+  size_t off = 0, kv_last = 0;
+  int kv_unit = -1;
+  for (HostPiece& pc : hp.pieces) {
+    const size_t nrows = static_cast<size_t>(pc.n) * g * (pc.r1 - pc.r0);
+    pc.q_off = off;   off += align_up(nrows * row_bytes, 256);
+    pc.o_off = off;   off += align_up(nrows * row_bytes, 256);
+    pc.lse_off = off; off += align_up(nrows * 4, 256);
+    if (pc.n == 1 && pc.k0 > 0 && kv_unit == pc.u0) {
+      pc.kv_off = kv_last;
+    } else {
+      pc.kv_off = kv_last = off;
+      kv_unit = pc.n == 1 ? pc.u0 : -1;
+      off += 2 * align_up(static_cast<size_t>(pc.n) * Sk * row_bytes, 256);
+    }
+    if (pc.n > hp.max_units) hp.max_units = pc.n;
   }
+  // one shift workspace per compute stream (pieces alternate between two)
   hp.ws_off = off;
-  hp.ws_bytes = pasa_attn_fwd_workspace_bytes(hp.max_units, 1, Sk, D, mode);
-  hp.total = align_up(off + hp.ws_bytes, 256);
+  hp.ws_bytes = align_up(pasa_attn_fwd_workspace_bytes(hp.max_units, 1, Sk, D, mode), 256);
+  hp.total = off + (hp.pieces.size() > 1 ? 2 : 1) * hp.ws_bytes;
   return hp;
 }
 
-// One pair of non-blocking copy streams per device, created on first use and kept for the
-// life of the process. Calls from several host threads may share them: every wait a call
-// enqueues refers to work that call has already enqueued, so the order stays acyclic.
-std::mutex g_copy_mutex;
-cudaStream_t g_copy_streams[kNoAllocMaxDevices][2] = {};
+// Three non-blocking side streams per device (host->device copies, device->host copies, a
+// second compute stream), created on first use and kept for the life of the process. Calls
+// from several host threads may share them: every wait a call enqueues refers to work that
+// call has already enqueued, so the order stays acyclic.
+std::mutex g_side_mutex;
+cudaStream_t g_side_streams[kNoAllocMaxDevices][3] = {};
 
-int copy_streams(cudaStream_t* h2d, cudaStream_t* d2h) {
+int side_streams(cudaStream_t* out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
   if (dev < 0 || dev >= kNoAllocMaxDevices) return PASA_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_copy_mutex);
-  for (int j = 0; j < 2; ++j) {
-    if (g_copy_streams[dev][j] == nullptr) {
-      e = cudaStreamCreateWithFlags(&g_copy_streams[dev][j], cudaStreamNonBlocking);
+  std::lock_guard<std::mutex> lock(g_side_mutex);
+  for (int j = 0; j < 3; ++j) {
+    if (g_side_streams[dev][j] == nullptr) {
+      e = cudaStreamCreateWithFlags(&g_side_streams[dev][j], cudaStreamNonBlocking);
       if (e != cudaSuccess) return cuda_fail(e);
     }
+    out[j] = g_side_streams[dev][j];
   }
-  *h2d = g_copy_streams[dev][0];
-  *d2h = g_copy_streams[dev][1];
   return PASA_OK;
+}
+
+// `height` rows of `width` bytes between pitched buffers; one plain copy when both sides
+// are contiguous.
+cudaError_t copy_rows(void* dst, size_t dpitch, const void* src, size_t spitch, size_t width, size_t height,
+                      cudaMemcpyKind kind, cudaStream_t st) {
+  if (width == 0 || height == 0) return cudaSuccess;
+  if (dpitch == width && spitch == width) return cudaMemcpyAsync(dst, src, width * height, kind, st);
+  return cudaMemcpy2DAsync(dst, dpitch, src, spitch, width, height, kind, st);
 }
 
 }  // namespace
 
-extern "C" size_t pasa_attn_fwd_host_device_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D, int mode,
-                                                   int chunks) {
+extern "C" size_t pasa_attn_fwd_host_device_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal,
+                                                   int mode, int chunks) {
   if (chunks < 0 || validate_shape(B, Hq, Hkv, Sq, Sk, D, mode) != PASA_OK) return 0;
-  return host_plan(B, Hq, Hkv, Sq, Sk, D, mode, chunks).total;
+  return host_plan(B, Hq, Hkv, Sq, Sk, D, causal, mode, chunks).total;
+}
+
+extern "C" int pasa_attn_fwd_host_plan(int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, int mode,
+                                       int chunks, int* pieces, int max_pieces) {
+  if (chunks < 0 || max_pieces < 0 || (max_pieces > 0 && !pieces)) return chunks < 0 ? PASA_ERR_SHAPE : PASA_ERR_NULLPTR;
+  const int rc = validate_shape(B, Hq, Hkv, Sq, Sk, D, mode);
+  if (rc != PASA_OK) return rc;
+  const HostPlan hp = host_plan(B, Hq, Hkv, Sq, Sk, D, causal, mode, chunks);
+  const int np = static_cast<int>(hp.pieces.size());
+  for (int i = 0; i < np && i < max_pieces; ++i) {
+    const HostPiece& pc = hp.pieces[i];
+    int* r = pieces + 6 * static_cast<size_t>(i);
+    r[0] = pc.u0, r[1] = pc.n, r[2] = pc.r0, r[3] = pc.r1, r[4] = pc.k0, r[5] = pc.k1;
+  }
+  return np;
 }
 
 extern "C" int pasa_attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
@@ -888,7 +993,7 @@ extern "C" int pasa_attn_fwd_host(const void* q, const void* k, const void* v, v
   int rc = validate_shape(B, Hq, Hkv, Sq, Sk, D, mode);
   if (rc != PASA_OK) return rc;
   if (chunks < 0) return PASA_ERR_SHAPE;
-  const HostPlan hp = host_plan(B, Hq, Hkv, Sq, Sk, D, mode, chunks);
+  const HostPlan hp = host_plan(B, Hq, Hkv, Sq, Sk, D, causal, mode, chunks);
   if (device_buffer) {
     if (device_buffer_bytes < hp.total) return PASA_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(device_buffer) & 255u) != 0) return PASA_ERR_ALIGN;
@@ -896,17 +1001,19 @@ extern "C" int pasa_attn_fwd_host(const void* q, const void* k, const void* v, v
   rc = check_device();
   if (rc != PASA_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaStream_t s_in = nullptr, s_out = nullptr;
-  rc = copy_streams(&s_in, &s_out);
+  cudaStream_t side[3] = {};
+  rc = side_streams(side);
   if (rc != PASA_OK) return rc;
+  cudaStream_t s_in = side[0], s_out = side[1];
+  cudaStream_t s_run[2] = {st, side[2]};  // piece i computes on s_run[i % 2]
 
-  // events: [0] start on st, [1] h2d stream done, [2] d2h stream done,
-  // [3 + i] chunk i's inputs landed, [3 + chunks + i] chunk i's kernels finished
-  const int n_ev = 3 + 2 * hp.chunks;
-  cudaEvent_t ev[3 + 2 * kHostMaxChunks] = {};
+  // events: [0] start on st, [1] h2d stream done, [2] d2h stream done, [3] second compute
+  // stream done, [4 + i] piece i's inputs landed, [4 + np + i] piece i's kernels finished
+  const int np = static_cast<int>(hp.pieces.size());
+  std::vector<cudaEvent_t> ev(4 + 2 * static_cast<size_t>(np), nullptr);
   cudaError_t e = cudaSuccess;
-  int made = 0;
-  for (; made < n_ev; ++made) {
+  size_t made = 0;
+  for (; made < ev.size(); ++made) {
     e = cudaEventCreateWithFlags(&ev[made], cudaEventDisableTiming);
     if (e != cudaSuccess) break;
   }
@@ -917,7 +1024,7 @@ extern "C" int pasa_attn_fwd_host(const void* q, const void* k, const void* v, v
     owned = e == cudaSuccess;
   }
   if (e != cudaSuccess) {
-    for (int j = 0; j < made; ++j) cudaEventDestroy(ev[j]);
+    for (size_t j = 0; j < made; ++j) cudaEventDestroy(ev[j]);
     return cuda_fail(e);
   }
 
@@ -927,64 +1034,76 @@ extern "C" int pasa_attn_fwd_host(const void* q, const void* k, const void* v, v
     if (e == cudaSuccess && err != cudaSuccess) e = err;
     return e == cudaSuccess;
   };
+  const int g = Hq / Hkv;
+  const size_t row_bytes = static_cast<size_t>(D) * 2;
+  const size_t q_unit = static_cast<size_t>(g) * Sq * row_bytes;  // bytes of one unit's q (and o)
+  const size_t kv_unit = static_cast<size_t>(Sk) * row_bytes;
+  const size_t lse_unit = static_cast<size_t>(g) * Sq * 4;
   const uint8_t* qh = static_cast<const uint8_t*>(q);
   const uint8_t* kh = static_cast<const uint8_t*>(k);
   const uint8_t* vh = static_cast<const uint8_t*>(v);
   uint8_t* oh = static_cast<uint8_t*>(o);
   uint8_t* lh = reinterpret_cast<uint8_t*>(lse);
-  struct Slot { uint8_t *q, *k, *v, *o, *lse; size_t n; int u0; };
-  Slot slot[kHostMaxChunks];
-  size_t off = 0;
-  for (int i = 0; i < hp.chunks; ++i) {
-    Slot& s = slot[i];
-    s.u0 = host_chunk_begin(hp, i);
-    s.n = static_cast<size_t>(host_chunk_begin(hp, i + 1) - s.u0);
-    s.q = buf + off;  off += align_up(s.n * hp.q_bytes, 256);
-    s.k = buf + off;  off += align_up(s.n * hp.kv_bytes, 256);
-    s.v = buf + off;  off += align_up(s.n * hp.kv_bytes, 256);
-    s.o = buf + off;  off += align_up(s.n * hp.q_bytes, 256);
-    s.lse = buf + off; off += align_up(s.n * hp.lse_bytes, 256);
-  }
+
   // the buffer may still be in use by work the caller queued on st before this call
   step(cudaEventRecord(ev[0], st));
   step(cudaStreamWaitEvent(s_in, ev[0], 0));
   step(cudaStreamWaitEvent(s_out, ev[0], 0));
-  for (int i = 0; i < hp.chunks && e == cudaSuccess; ++i) {
-    const Slot& s = slot[i];
-    step(cudaMemcpyAsync(s.k, kh + s.u0 * hp.kv_bytes, s.n * hp.kv_bytes, cudaMemcpyHostToDevice, s_in));
-    step(cudaMemcpyAsync(s.v, vh + s.u0 * hp.kv_bytes, s.n * hp.kv_bytes, cudaMemcpyHostToDevice, s_in));
-    step(cudaMemcpyAsync(s.q, qh + s.u0 * hp.q_bytes, s.n * hp.q_bytes, cudaMemcpyHostToDevice, s_in));
-    step(cudaEventRecord(ev[3 + i], s_in));
+  step(cudaStreamWaitEvent(s_run[1], ev[0], 0));
+  for (int i = 0; i < np && e == cudaSuccess; ++i) {
+    const HostPiece& pc = hp.pieces[i];
+    const size_t kv_bytes = align_up(static_cast<size_t>(pc.n) * kv_unit, 256);
+    uint8_t* kd = buf + pc.kv_off;
+    uint8_t* vd = kd + kv_bytes;
+    // whole units: all their keys; a row piece: the keys [k0, k1) its rows newly see
+    const size_t kb0 = static_cast<size_t>(pc.k0) * row_bytes;
+    const size_t nb = pc.n == 1 ? static_cast<size_t>(pc.k1 - pc.k0) * row_bytes : pc.n * kv_unit;
+    step(copy_rows(kd + kb0, nb, kh + pc.u0 * kv_unit + kb0, nb, nb, 1, cudaMemcpyHostToDevice, s_in));
+    step(copy_rows(vd + kb0, nb, vh + pc.u0 * kv_unit + kb0, nb, nb, 1, cudaMemcpyHostToDevice, s_in));
+    const size_t w = static_cast<size_t>(pc.r1 - pc.r0) * row_bytes;
+    step(copy_rows(buf + pc.q_off, w, qh + pc.u0 * q_unit + pc.r0 * row_bytes, static_cast<size_t>(Sq) * row_bytes,
+                   w, static_cast<size_t>(pc.n) * g, cudaMemcpyHostToDevice, s_in));
+    step(cudaEventRecord(ev[4 + i], s_in));
   }
-  const int g = Hq / Hkv;
-  for (int i = 0; i < hp.chunks && e == cudaSuccess; ++i) {
-    const Slot& s = slot[i];
-    if (!step(cudaStreamWaitEvent(st, ev[3 + i], 0))) break;
-    const int krc = pasa_attn_fwd_ws(s.q, s.k, s.v, s.o, lse ? reinterpret_cast<float*>(s.lse) : nullptr,
-                                     static_cast<int>(s.n), g, 1, Sq, Sk, D, causal, scale, mode,
-                                     hp.ws_bytes ? buf + hp.ws_off : nullptr, hp.ws_bytes, st);
+  for (int i = 0; i < np && e == cudaSuccess; ++i) {
+    const HostPiece& pc = hp.pieces[i];
+    const size_t kv_bytes = align_up(static_cast<size_t>(pc.n) * kv_unit, 256);
+    const int rows = pc.r1 - pc.r0;
+    cudaStream_t run = s_run[i & 1];
+    if (!step(cudaStreamWaitEvent(run, ev[4 + i], 0))) break;
+    const int krc = pasa_attn_fwd_ws(buf + pc.q_off, buf + pc.kv_off, buf + pc.kv_off + kv_bytes, buf + pc.o_off,
+                                     lse ? reinterpret_cast<float*>(buf + pc.lse_off) : nullptr, pc.n, g, 1, rows,
+                                     pc.k1, D, causal, scale, mode,
+                                     hp.ws_bytes ? buf + hp.ws_off + (i & 1) * hp.ws_bytes : nullptr, hp.ws_bytes,
+                                     run);
     if (krc != PASA_OK) {
       rc = krc;
       break;
     }
-    step(cudaEventRecord(ev[3 + hp.chunks + i], st));
-    step(cudaStreamWaitEvent(s_out, ev[3 + hp.chunks + i], 0));
-    step(cudaMemcpyAsync(oh + s.u0 * hp.q_bytes, s.o, s.n * hp.q_bytes, cudaMemcpyDeviceToHost, s_out));
-    if (lse) step(cudaMemcpyAsync(lh + s.u0 * hp.lse_bytes, s.lse, s.n * hp.lse_bytes, cudaMemcpyDeviceToHost, s_out));
+    step(cudaEventRecord(ev[4 + np + i], run));
+    step(cudaStreamWaitEvent(s_out, ev[4 + np + i], 0));
+    const size_t w = static_cast<size_t>(rows) * row_bytes;
+    const size_t h = static_cast<size_t>(pc.n) * g;
+    step(copy_rows(oh + pc.u0 * q_unit + pc.r0 * row_bytes, static_cast<size_t>(Sq) * row_bytes, buf + pc.o_off, w,
+                   w, h, cudaMemcpyDeviceToHost, s_out));
+    if (lse)
+      step(copy_rows(lh + pc.u0 * lse_unit + static_cast<size_t>(pc.r0) * 4, static_cast<size_t>(Sq) * 4,
+                     buf + pc.lse_off, static_cast<size_t>(rows) * 4, static_cast<size_t>(rows) * 4, h,
+                     cudaMemcpyDeviceToHost, s_out));
   }
-  // join: st continues only after both side streams have drained this call's copies
-  cudaError_t je = cudaEventRecord(ev[1], s_in);
-  if (je == cudaSuccess) je = cudaStreamWaitEvent(st, ev[1], 0);
-  if (je == cudaSuccess) je = cudaEventRecord(ev[2], s_out);
-  if (je == cudaSuccess) je = cudaStreamWaitEvent(st, ev[2], 0);
+  // join: st continues only after the side streams have drained this call's work
+  cudaError_t je = cudaSuccess;
+  for (int j = 0; j < 3 && je == cudaSuccess; ++j) {
+    je = cudaEventRecord(ev[1 + j], side[j]);
+    if (je == cudaSuccess) je = cudaStreamWaitEvent(st, ev[1 + j], 0);
+  }
   if (je != cudaSuccess) {
     // st cannot be ordered after the side streams: wait for them here before freeing
-    cudaStreamSynchronize(s_in);
-    cudaStreamSynchronize(s_out);
+    for (int j = 0; j < 3; ++j) cudaStreamSynchronize(side[j]);
     step(je);
   }
   if (owned) step(cudaFreeAsync(buf, st));
-  for (int j = 0; j < n_ev; ++j) cudaEventDestroy(ev[j]);
+  for (cudaEvent_t x : ev) cudaEventDestroy(x);
   if (rc != PASA_OK) return rc;
   return e == cudaSuccess ? PASA_OK : cuda_fail(e);
 }

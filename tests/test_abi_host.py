@@ -244,14 +244,14 @@ def test_host_buffer_entry_checks_arguments(lib):
     # pasa_attn_fwd_host(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, mode, chunks, buf, buf_bytes, stream)
     def host(q=FAKE, o=FAKE, B=1, Hq=8, Hkv=2, Sq=300, Sk=300, D=128, mode=0, chunks=0, buf=FAKE, nbytes=None):
         if nbytes is None:
-            nbytes = lib.pasa_attn_fwd_host_device_bytes(B, Hq, Hkv, Sq, Sk, D, mode, chunks)
+            nbytes = lib.pasa_attn_fwd_host_device_bytes(B, Hq, Hkv, Sq, Sk, D, 1, mode, chunks)
         return lib.pasa_attn_fwd_host(P(q) if q else None, P(FAKE), P(FAKE), P(o) if o else None, None, B, Hq, Hkv,
                                       Sq, Sk, D, 1, 0.0, mode, chunks, P(buf) if buf else None, nbytes, None)
 
     assert host(q=0) == -1 and host(o=0) == -1
     assert host(Hq=7) == -2 and host(Sk=0) == -2 and host(chunks=-1) == -2
     assert host(D=96) == -3 and host(mode=9) == -3 and host(D=64, mode=5) == -3
-    nbytes = lib.pasa_attn_fwd_host_device_bytes(1, 8, 2, 300, 300, 128, 0, 0)
+    nbytes = lib.pasa_attn_fwd_host_device_bytes(1, 8, 2, 300, 300, 128, 1, 0, 0)
     assert host(nbytes=nbytes - 1) == -7                 # buffer too small
     assert host(buf=FAKE + 128, nbytes=nbytes) == -4     # buffer not 256-byte aligned
     # host pointers need no alignment: a misaligned q gets past argument checks to the
@@ -261,21 +261,84 @@ def test_host_buffer_entry_checks_arguments(lib):
 
 def test_host_buffer_device_bytes(lib):
     nb = lib.pasa_attn_fwd_host_device_bytes
-    assert nb(1, 8, 2, 300, 300, 128, 0, -1) == 0 and nb(1, 7, 2, 300, 300, 128, 0, 0) == 0
+    assert nb(1, 8, 2, 300, 300, 128, 1, 0, -1) == 0 and nb(1, 7, 2, 300, 300, 128, 1, 0, 0) == 0
     for (B, Hq, Hkv, Sq, Sk, D) in [(1, 28, 4, 32768, 32768, 128), (2, 5, 5, 9216, 9216, 64), (8, 28, 4, 1, 4096, 128),
-                                    (3, 6, 3, 129, 257, 64)]:
+                                    (3, 6, 3, 129, 257, 64), (1, 64, 1, 2048, 2048, 128)]:
         units = B * Hkv
         problem = 2 * B * Hq * Sq * D * 2 + 2 * B * Hkv * Sk * D * 2 + B * Hq * Sq * 4
         for mode in (0, 2, 5):
             if mode == 5 and D != 128:
                 continue
-            for chunks in (1, 2, 3, units, units + 5):
-                n = min(chunks, units)
-                biggest = -(-units // n)
-                got = nb(B, Hq, Hkv, Sq, Sk, D, mode, chunks)
-                # whole problem staged + one piece's workspace, slots 256-byte aligned
-                ws = lib.pasa_attn_fwd_workspace_bytes(biggest, 1, Sk, D, mode)
-                assert problem + ws <= got <= problem + ws + 5 * 256 * n + 256, (B, Hq, Hkv, Sq, Sk, D, mode, chunks)
-                assert got % 256 == 0
-            # automatic chunking stages the same problem
-            assert nb(B, Hq, Hkv, Sq, Sk, D, mode, 0) >= problem
+            for causal in (0, 1):
+                for chunks in (1, 2, 3, units, units + 5):
+                    n = min(chunks, units)
+                    biggest = -(-units // n)
+                    got = nb(B, Hq, Hkv, Sq, Sk, D, causal, mode, chunks)
+                    # whole problem staged + a workspace for each of the two compute streams
+                    # (one when there is one piece), slots 256-byte aligned
+                    ws = -(-lib.pasa_attn_fwd_workspace_bytes(biggest, 1, Sk, D, mode) // 256) * 256
+                    ws *= 2 if n > 1 else 1
+                    assert problem + ws <= got <= problem + ws + 5 * 256 * n, (B, Hq, Sq, mode, chunks)
+                    assert got % 256 == 0
+                # the automatic plan (row pieces included) stages the same problem, once
+                auto = nb(B, Hq, Hkv, Sq, Sk, D, causal, mode, 0)
+                ws1 = lib.pasa_attn_fwd_workspace_bytes(1, 1, Sk, D, mode)
+                assert problem + ws1 <= auto <= problem + 2 * lib.pasa_attn_fwd_workspace_bytes(units, 1, Sk, D, mode) \
+                    + 5 * 256 * (units + 8) + 512
+
+
+def host_plan_checks(B, Hq, Hkv, Sq, Sk, D, causal, chunks):
+    """Every (unit, query row) in exactly one piece, in unit order; each unit's keys copied
+    once, in order, up to what its rows see; row pieces on 128-row tiles with their key
+    prefix ending on a 128-key block or at Sk (the conditions for tile-for-tile equality)."""
+    import precision_flashattention_numerics_gb300 as pasa
+
+    plan = pasa.host_plan(B, Hq, Hkv, Sq, Sk, D, causal, 0, chunks)
+    units = B * Hkv
+    covered = {}
+    keys = {}
+    for (u0, n, r0, r1, k0, k1) in plan:
+        assert n >= 1 and 0 <= r0 < r1 <= Sq
+        if n > 1 or (r0 == 0 and r1 == Sq):
+            assert (r0, r1, k0, k1) == (0, Sq, 0, Sk)
+        else:
+            assert r0 % 128 == 0
+            assert k1 == (r1 + Sk - Sq if causal else Sk)
+            assert k1 == Sk or k1 % 128 == 0
+        for u in range(u0, u0 + n):
+            covered.setdefault(u, []).append((r0, r1))
+            assert k0 == keys.get(u, 0), "keys copied in order, once"
+            keys[u] = k1
+    assert sorted(covered) == list(range(units))
+    for u, spans in covered.items():
+        assert spans[0][0] == 0 and spans[-1][1] == Sq
+        assert all(a[1] == b[0] for a, b in zip(spans, spans[1:]))
+        assert keys[u] == Sk
+    order = [(u0, r0) for (u0, n, r0, r1, k0, k1) in plan]
+    assert order == sorted(order)
+    return plan
+
+
+def test_host_buffer_plan(lib):
+    # explicit chunk counts: whole units only
+    plan = host_plan_checks(3, 6, 3, 300, 700, 64, True, 4)
+    assert [p[1] for p in plan] == [2, 2, 2, 3] and all((p[2], p[3]) == (0, 300) for p in plan)
+    assert [p[1] for p in host_plan_checks(2, 8, 4, 520, 520, 128, True, 3)] == [2, 3, 3]
+    # automatic: the 32K workload, 4 units; the first and last unit in halving row pieces
+    plan = host_plan_checks(1, 28, 4, 32768, 32768, 128, True, 0)
+    assert [(p[0], p[2], p[3]) for p in plan] == [
+        (0, 0, 4096), (0, 4096, 8192), (0, 8192, 16384), (0, 16384, 32768), (1, 0, 32768), (2, 0, 32768),
+        (3, 0, 16384), (3, 16384, 24576), (3, 24576, 28672), (3, 28672, 32768)]
+    # one unit cut at both ends; Sk > Sq by whole blocks; not causal with a ragged Sk
+    assert len(host_plan_checks(1, 64, 1, 2048, 2048, 128, True, 0)) == 6
+    assert len(host_plan_checks(1, 64, 1, 2048, 2048 + 256, 128, True, 0)) == 6
+    assert len(host_plan_checks(1, 64, 1, 2048, 2000, 64, False, 0)) == 6
+    # causal offsets that are not whole blocks, or rows that see no key: no row pieces
+    assert len(host_plan_checks(1, 64, 1, 2048, 2048 + 100, 128, True, 0)) == 1
+    assert len(host_plan_checks(1, 64, 1, 2048, 1024, 128, True, 0)) == 1
+    # small problems stay one piece
+    assert len(host_plan_checks(1, 8, 1, 300, 300, 128, True, 0)) == 1
+    assert len(host_plan_checks(8, 28, 4, 1, 4096, 128, True, 0)) == 1
+    for shape in [(4, 32, 8, 8192, 8192, 128, True), (2, 5, 5, 9216, 9216, 64, False), (3, 48, 3, 4096, 4224, 64, True)]:
+        host_plan_checks(*shape, 0)
+        host_plan_checks(*shape, 5)

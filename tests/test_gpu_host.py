@@ -1,10 +1,11 @@
 """GPU tests of pasa_attn_fwd_host: the PASA forward pass ("Online Pseudo-average Shifting
 Attention (PASA) for Robust Low-precision LLM Inference", Abstract) on host buffers, staged
-to the device in pieces of (batch, kv head) units with the copies overlapped.
+to the device in pieces (runs of (batch, kv head) units, or query-row ranges of one unit)
+with the copies overlapped.
 
-Each piece is the same computation on a sub-problem with one kv head, so the host-buffer
+Each piece meets the same key blocks and pseudo-averages tile for tile, so the host-buffer
 call must agree BIT FOR BIT with pasa_attn_fwd on device copies of the same inputs, for
-every mode, piece count and memory kind (pinned or pageable). One small case is also
+every mode, piece plan and memory kind (pinned or pageable). One small case is also
 checked against the fp64 oracle directly, with the bounds of the attention parity tests.
 """
 import ctypes
@@ -71,6 +72,34 @@ def test_host_matches_device(case, mode):
         assert torch.equal(lse, lse_ref), (mode, chunks)
 
 
+ROW_CASES = [
+    # shapes whose automatic plan cuts the first and last unit into query-row pieces
+    # (B, Hq, Hkv, Sq, Sk, D, causal, kind, params)
+    (1, 64, 1, 2048, 2048, 128, True, "kbias", {"bias_std": 20.0}),       # 6 row pieces
+    (1, 64, 1, 2048, 2048 + 256, 64, True, "iid", {}),                    # Sk > Sq by whole blocks
+    (1, 64, 1, 2048, 2000, 64, False, "kbias", {"bias_std": 10.0}),       # ragged Sk, no mask
+    (2, 32, 2, 2048, 2048, 128, True, "kbias_t3", {"bias_std": 10.0, "t_dof": 3, "t_scale": 4.0}),
+]
+
+
+@pytest.mark.parametrize("case", range(len(ROW_CASES)))
+@pytest.mark.parametrize("mode", [0, 1, 2, 3, 4, 5, 6])
+def test_host_row_pieces_match_device(case, mode):
+    B, Hq, Hkv, Sq, Sk, D, causal, kind, params = ROW_CASES[case]
+    if mode >= 5 and D != 128:
+        pytest.skip("FP8 modes: D = 128")
+    p = pasa()
+    plan = p.host_plan(B, Hq, Hkv, Sq, Sk, D, causal, mode, 0)
+    assert any(r1 - r0 < Sq for (_, _, r0, r1, _, _) in plan), "the plan has row pieces"
+    q, k, v = make(B, Hq, Hkv, Sq, Sk, D, kind, 760 + case, **params)
+    o_ref, lse_ref = device_result(q, k, v, causal, mode)
+    qh, kh, vh = host_tensors(q, k, v)
+    o, lse = p.attn_fwd_host(qh, kh, vh, causal=causal, mode=mode, chunks=0)
+    p.check_device_error()
+    assert torch.equal(o, o_ref), plan
+    assert torch.equal(lse, lse_ref), plan
+
+
 def test_host_pageable_and_own_buffer():
     p = pasa()
     B, Hq, Hkv, Sq, Sk, D = 2, 8, 4, 520, 520, 128
@@ -79,7 +108,7 @@ def test_host_pageable_and_own_buffer():
     qh, kh, vh = host_tensors(q, k, v, pinned=False)
     out = torch.empty(q.shape, dtype=torch.float16)
     lse = torch.empty((B, Hq, Sq), dtype=torch.float32)
-    nbytes = p.host_device_bytes(B, Hq, Hkv, Sq, Sk, D, 0, 3)
+    nbytes = p.host_device_bytes(B, Hq, Hkv, Sq, Sk, D, True, 0, 3)
     buf = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
     p.attn_fwd_host(qh, kh, vh, causal=True, mode=0, out=out, lse=lse, chunks=3, device_buffer=buf)
     assert torch.equal(out, o_ref) and torch.equal(lse, lse_ref)
@@ -112,13 +141,25 @@ def test_host_calls_queue_in_order_on_one_buffer():
     B, Hq, Hkv, Sq, Sk, D = 2, 8, 4, 1030, 1030, 128
     ins = [make(B, Hq, Hkv, Sq, Sk, D, "kbias", 740 + i, bias_std=10.0) for i in range(3)]
     refs = [device_result(*x, True, 0) for x in ins]
-    buf = torch.empty(p.host_device_bytes(B, Hq, Hkv, Sq, Sk, D, 0, 4), dtype=torch.uint8, device="cuda")
+    buf = torch.empty(p.host_device_bytes(B, Hq, Hkv, Sq, Sk, D, True, 0, 4), dtype=torch.uint8, device="cuda")
     outs = []
     for x in ins:
         qh, kh, vh = host_tensors(*x)
         outs.append(p.attn_fwd_host(qh, kh, vh, causal=True, mode=0, chunks=4, device_buffer=buf, sync=False))
     torch.cuda.current_stream().synchronize()
     p.check_device_error()
+    for (o, lse), (o_ref, lse_ref) in zip(outs, refs):
+        assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
+    # the same with row pieces sharing a unit's key slot
+    B, Hq, Hkv, Sq, Sk, D = 1, 64, 1, 2048, 2048, 128
+    ins = [make(B, Hq, Hkv, Sq, Sk, D, "kbias", 750 + i, bias_std=10.0) for i in range(2)]
+    refs = [device_result(*x, True, 1) for x in ins]
+    buf = torch.empty(p.host_device_bytes(B, Hq, Hkv, Sq, Sk, D, True, 1, 0), dtype=torch.uint8, device="cuda")
+    outs = []
+    for x in ins:
+        qh, kh, vh = host_tensors(*x)
+        outs.append(p.attn_fwd_host(qh, kh, vh, causal=True, mode=1, device_buffer=buf, sync=False))
+    torch.cuda.current_stream().synchronize()
     for (o, lse), (o_ref, lse_ref) in zip(outs, refs):
         assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
 
