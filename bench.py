@@ -4,8 +4,9 @@ One step = the whole hot path on one batch of synthetic input already resident i
 the pseudo-average shift of K (kshift kernel) followed by the attention kernel, both
 through the C ABI (pasa_kshift, pasa_attn_fwd_shifted). FLOPs follow the FlashAttention
 convention (4 * B * Hq * visible (query, key) pairs * D). The e2e figure goes through
-pasa_attn_fwd with host buffers: pinned host -> device copies of q, k, v, the call, and
-device -> host copies of o and lse, all inside the timed region.
+pasa_attn_fwd_host with pinned host buffers: every byte of q, k, v copied in and of o and
+lse copied out lies inside the timed region, the copies overlapping the kernels piece by
+piece.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--mode M]
   python bench.py --impl reference ...   # the fp64 CPU oracle on this host's cores

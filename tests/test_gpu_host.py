@@ -176,3 +176,20 @@ def test_host_against_oracle():
     assert np.all(np.isfinite(o.float().numpy()))
     tol = lse_tolerance(q, k, True, 0, D)
     assert np.max(np.abs(lse.double().numpy() - lse_ref)) <= tol
+
+
+def test_host_full_size_32k_matches_device():
+    """The call the end-to-end benchmark times, at full size (32K biased causal workload,
+    B1 Hq28/Hkv4 D128, mode 0, automatic plan with row pieces): bit-identical to the
+    device-resident call."""
+    p = pasa()
+    w = wl.WORKLOADS["kbias10_t3_b1h28g4_s32768_d128_causal"]
+    q, k, v = wl.make_inputs(w)
+    plan = p.host_plan(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, w.causal, 0, 0)
+    assert len(plan) == 10
+    o_ref, lse_ref = device_result(q, k, v, w.causal, 0)
+    qh, kh, vh = host_tensors(q, k, v)
+    o, lse = p.attn_fwd_host(qh, kh, vh, causal=w.causal, mode=0)
+    p.check_device_error()
+    assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
+    assert bool(torch.isfinite(o).all())
