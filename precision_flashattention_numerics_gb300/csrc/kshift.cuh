@@ -27,15 +27,21 @@
 // inv = fp32(448 / a), code = e4m3_rn_satfinite(fp32(K' * inv)), scale = fp32(a / 448)
 // (a = 0: inv = scale = 1). 448 is the largest finite e4m3 value.
 //
-// Kernel shape: one CTA of 256 threads per (batch*kv-head, key block). Each thread owns one
-// 16-byte unit (8 channels) of up to ceil(block rows / row groups) rows and keeps them in
-// registers; the per-channel max and integer sums are reduced with warp shuffles and a
-// small shared-memory exchange across the 8 warps; the block is read from HBM once and
-// K' written once (HBM-bound: 2 * rows * D * 2 bytes per block).
+// Kernel shape: one CTA of 256 threads per (batch*kv-head, key block). A block's rows are
+// contiguous, so one thread stages the whole block into shared memory with a single
+// untiled bulk copy (cp.async.bulk, completing on an mbarrier); each thread owns one 16-byte
+// unit (8 channels) of up to ceil(block rows / row groups) rows and reads them from shared
+// memory in each pass. The per-channel max and integer sums are reduced with warp shuffles
+// and a small shared-memory exchange across the 8 warps. Keeping the block in shared
+// memory instead of registers leaves room for several CTAs per SM, so one CTA's loads
+// overlap another's reductions and stores. The block is read from HBM once and K' written
+// once (HBM-bound: 2 * rows * D * 2 bytes per block).
 #pragma once
 
 #include <cstdint>
 #include <cuda_fp16.h>
+
+#include "ptx.cuh"
 
 namespace pasa {
 
@@ -78,10 +84,13 @@ kshift_kernel(const __half* __restrict__ k, void* __restrict__ kshift, __half* _
   static_assert(32 % U == 0 || U % 32 == 0, "unit layout");
   static_assert(U <= 32, "D <= 256");
 
+  __shared__ __align__(128) uint4 sh_blk[BN * U];   // the block, row-major, rows >= n zeroed
+  __shared__ uint64_t sh_bar;
+  __shared__ int sh_abort;
   __shared__ uint32_t sh_max[NW][U][4];
   __shared__ uint32_t sh_nf[NW][U][4];
   static_assert(!PLAIN || OUT == kShiftF16, "the plain-mean reading has the fp16 output only");
-  __shared__ int sh_sum[NW][U][8];
+  __shared__ int sh_sum[PLAIN ? 1 : NW][U][8];
   __shared__ long long sh_sum64[PLAIN ? NW : 1][U][8];
   __shared__ uint32_t sh_amax[NW];
 
@@ -96,22 +105,39 @@ kshift_kernel(const __half* __restrict__ k, void* __restrict__ kshift, __half* _
   const int row0 = j * BN;
   const int n = min(BN, Sk - row0);
 
-  const uint4* src = reinterpret_cast<const uint4*>(k + (static_cast<size_t>(bh) * cap + row0) * D) + u;
   uint4* dst = reinterpret_cast<uint4*>(static_cast<__half*>(kshift) + (static_cast<size_t>(bh) * cap + row0) * D) + u;
 
-  uint4 x[RPT];
-#pragma unroll
-  for (int i = 0; i < RPT; ++i) {
-    const int r = rg + i * R;
-    if (r < n) x[i] = __ldg(src + static_cast<size_t>(r) * U);
-    else x[i] = make_uint4(0, 0, 0, 0);
+  // 0. stage the block: n contiguous rows of D fp16 (n * D * 2 bytes, a multiple of 16)
+  if (tid == 0) {
+    sh_abort = 0;
+    mbar_init(&sh_bar, 1);
+    fence_mbar_init();
   }
+  for (int r = n + tid / U; r < BN; r += R) sh_blk[r * U + u] = make_uint4(0, 0, 0, 0);
+  __syncthreads();
+  // One thread waits for the copy (256 polling threads per CTA would crowd the shared-memory
+  // pipe that the other resident CTAs' passes use); the rest wait at the CTA barrier.
+  if (tid == 0) {
+    const uint32_t bytes = static_cast<uint32_t>(n) * D * 2;
+    mbar_arrive_expect_tx(&sh_bar, bytes);
+    bulk_load_1d(sh_blk, k + (static_cast<size_t>(bh) * cap + row0) * D, bytes, &sh_bar);
+    if (!mbar_wait(&sh_bar, 0, &sh_abort, 0x4B530000u | static_cast<uint32_t>(blockIdx.y & 0xFFFF))) {
+      // give the copy in flight a last bounded chance to land before the CTA leaves
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(&sh_bar, 0) && globaltimer_ns() - t0 < kWaitTimeoutNs) {
+      }
+    }
+  }
+  __syncthreads();
+  if (sh_abort) return;
+  const uint4* blk = sh_blk + u;
 
   // 1. per-channel max |K| over finite values, and a non-finite flag (16-bit lanes)
   uint32_t mx[4] = {0, 0, 0, 0}, nf[4] = {0, 0, 0, 0};
 #pragma unroll
   for (int i = 0; i < RPT; ++i) {
-    const uint32_t w[4] = {x[i].x, x[i].y, x[i].z, x[i].w};
+    const uint4 xi = blk[(rg + i * R) * U];
+    const uint32_t w[4] = {xi.x, xi.y, xi.z, xi.w};
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       const uint32_t a = w[c] & 0x7FFF7FFFu;
@@ -165,7 +191,8 @@ kshift_kernel(const __half* __restrict__ k, void* __restrict__ kshift, __half* _
     long long sum[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
-      const __half* hv = reinterpret_cast<const __half*>(&x[i]);
+      const uint4 xi = blk[(rg + i * R) * U];
+      const __half* hv = reinterpret_cast<const __half*>(&xi);
 #pragma unroll
       for (int h = 0; h < 8; ++h) {
         const float f = __half2float(hv[h]);
@@ -182,16 +209,24 @@ kshift_kernel(const __half* __restrict__ k, void* __restrict__ kshift, __half* _
       for (int h = 0; h < 8; ++h) sh_sum64[warp][u][h] = sum[h];
     }
   } else {
-    int sum[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    // t = K / g is exact (a power-of-two scale) and |t| < 2^11 in every channel that is not
+    // guarded (|K| <= M < 2^11 g), so fp32(t + 1.5 * 2^23) is rint_even(t) + 1.5 * 2^23
+    // exactly and its bit pattern minus that of 1.5 * 2^23 is rint_even(t): one FFMA and one
+    // integer add per element. Rows >= n hold zeros. A guarded channel (non-finite values, or
+    // M >= 2^15) gets a meaningless sum that is discarded below; the sums are unsigned so
+    // that it wraps harmlessly.
+    constexpr float kRound = 12582912.0f;      // 1.5 * 2^23
+    constexpr uint32_t kRoundBits = 0x4B400000u;
+    uint32_t sum[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
-      const __half* hv = reinterpret_cast<const __half*>(&x[i]);
+      const uint4 xi = blk[(rg + i * R) * U];
+      const __half2* hv = reinterpret_cast<const __half2*>(&xi);
 #pragma unroll
-      for (int h = 0; h < 8; ++h) {
-        const float f = __half2float(hv[h]);
-        // rows >= n hold zeros; non-finite values only occur in guarded channels
-        const float t = isfinite(f) ? f * inv_g[h] : 0.0f;  // exact: power-of-two scale
-        sum[h] += __float2int_rn(t);
+      for (int c = 0; c < 4; ++c) {
+        const float2 f = __half22float2(hv[c]);
+        sum[2 * c] += __float_as_uint(__fmaf_rn(f.x, inv_g[2 * c], kRound)) - kRoundBits;
+        sum[2 * c + 1] += __float_as_uint(__fmaf_rn(f.y, inv_g[2 * c + 1], kRound)) - kRoundBits;
       }
     }
 #pragma unroll
@@ -201,7 +236,7 @@ kshift_kernel(const __half* __restrict__ k, void* __restrict__ kshift, __half* _
     }
     if ((tid % 32) < U) {
 #pragma unroll
-      for (int h = 0; h < 8; ++h) sh_sum[warp][u][h] = sum[h];
+      for (int h = 0; h < 8; ++h) sh_sum[warp][u][h] = static_cast<int>(sum[h]);
     }
   }
   __syncthreads();
@@ -218,10 +253,11 @@ kshift_kernel(const __half* __restrict__ k, void* __restrict__ kshift, __half* _
       mh[h] = guard[h] ? __float2half_rn(0.0f) : __double2half(static_cast<double>(s) / n * 0x1p-24);
       mf[h] = __half2float(mh[h]);
     } else {
-      int s = 0;
+      uint32_t su = 0;
 #pragma unroll
-      for (int w = 0; w < NW; ++w) s += sh_sum[w][u][h];
-      const int mu = rne_div(s, n);
+      for (int w = 0; w < NW; ++w) su += static_cast<uint32_t>(sh_sum[w][u][h]);
+      const int s = static_cast<int>(su);  // |s| < 128 * 2^11 wherever it is used
+      const int mu = guard[h] ? 0 : rne_div(s, n);
       mf[h] = (guard[h] || OUT == kRawFp8) ? 0.0f : static_cast<float>(mu) * g[h];  // exact, an fp16 value
       mh[h] = __float2half_rn(mf[h]);
     }
@@ -239,25 +275,32 @@ kshift_kernel(const __half* __restrict__ k, void* __restrict__ kshift, __half* _
       const int r = rg + i * R;
       if (r < n) {
         uint4 o;
-        const __half* hv = reinterpret_cast<const __half*>(&x[i]);
-        __half* op = reinterpret_cast<__half*>(&o);
+        const uint4 xi = blk[r * U];
+        const __half2* hv = reinterpret_cast<const __half2*>(&xi);
+        __half2* op = reinterpret_cast<__half2*>(&o);
 #pragma unroll
-        for (int h = 0; h < 8; ++h) op[h] = __float2half_rn(__half2float(hv[h]) - mf[h]);
+        for (int c = 0; c < 4; ++c) {
+          const float2 f = __half22float2(hv[c]);
+          op[c] = __floats2half2_rn(f.x - mf[2 * c], f.y - mf[2 * c + 1]);  // each rounded once, RN
+        }
         dst[static_cast<size_t>(r) * U] = o;
       }
     }
   } else {
-    // K' (rounded to fp16, as the fp16 modes use it) in place, and its block maximum
+    // K' (rounded to fp16, as the fp16 modes use it) over the block's own shared-memory
+    // copy (each thread rewrites only the units it reads), and its block maximum
     uint32_t amax = 0;
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
       const int r = rg + i * R;
-      __half* hv = reinterpret_cast<__half*>(&x[i]);
+      uint4 xi = blk[r * U];
+      __half* hv = reinterpret_cast<__half*>(&xi);
 #pragma unroll
       for (int h = 0; h < 8; ++h) {
         hv[h] = r < n ? __float2half_rn(__half2float(hv[h]) - mf[h]) : __ushort_as_half(0);
         amax = max(amax, static_cast<uint32_t>(__half_as_ushort(hv[h]) & 0x7FFFu));
       }
+      sh_blk[r * U + u] = xi;
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, off));
@@ -274,7 +317,8 @@ kshift_kernel(const __half* __restrict__ k, void* __restrict__ kshift, __half* _
     for (int i = 0; i < RPT; ++i) {
       const int r = rg + i * R;
       if (r < n) {
-        const __half* hv = reinterpret_cast<const __half*>(&x[i]);
+        const uint4 xi = blk[r * U];
+        const __half* hv = reinterpret_cast<const __half*>(&xi);
         uint16_t c[4];
 #pragma unroll
         for (int h = 0; h < 4; ++h)
