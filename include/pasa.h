@@ -384,6 +384,22 @@ int pasa_last_cuda_error(void);
 /* 1 if `device` can run this library (compute capability 10.3), else 0. */
 int pasa_device_supported(int device);
 
+/*
+ * Exercises the failure-detection path without a fault. (The paper has no counterpart: this
+ * is a library test hook.) It launches one CTA whose thread 0 waits, through the same
+ * bounded mbarrier wait every kernel of the library uses, on a barrier that nothing arrives
+ * on. After the library's wait limit (2 s of %globaltimer) the wait gives up and records a
+ * timeout in the device error word, with site tag 0x5E1F7E57 as the low 32 bits of the
+ * info word, and the kernel returns. It holds no TMA copy and no tensor memory, so the GPU
+ * context stays usable: pasa_check_device_error(stream, &info) then returns
+ * PASA_ERR_TIMEOUT with that tag and clears the word. Any error already latched in the word
+ * makes the wait give up at once instead, keeping the first error's info.
+ *   stream  where the CTA runs. Returns PASA_OK once launched; errors as for every entry
+ *           point (no supported device: PASA_ERR_UNSUPPORTED; a failed launch:
+ *           PASA_ERR_CUDA).
+ */
+int pasa_selftest_wait_timeout(void* stream);
+
 #ifdef __cplusplus
 }
 #endif

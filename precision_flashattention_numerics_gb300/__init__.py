@@ -61,6 +61,7 @@ SIGNATURES = {
     "pasa_attn_fwd_host_device_bytes": ([_I] * 9, _SZ),
     "pasa_attn_fwd_host_plan": ([_I] * 9 + [_P, _I], _I),
     "pasa_check_device_error": ([_P, ctypes.POINTER(ctypes.c_ulonglong)], _I),
+    "pasa_selftest_wait_timeout": ([_P], _I),
     "pasa_strerror": ([_I], ctypes.c_char_p),
     "pasa_last_cuda_error": ([], _I),
     "pasa_device_supported": ([_I], _I),
@@ -406,6 +407,15 @@ def attn_fwd_decode_fp8(q, k8, means, kscale, v, causal: bool = False, scale: fl
     if rc != 0:
         raise PasaError(rc, "pasa_attn_fwd_decode_fp8")
     return out, lse
+
+
+def selftest_wait_timeout():
+    """Launch the failure-detection self-test on the current stream (pasa_selftest_wait_timeout):
+    one CTA waits on a barrier nothing arrives on until the library's wait limit (2 s) and
+    records a timeout in the device error word. check_device_error() then raises it."""
+    rc = library().pasa_selftest_wait_timeout(_stream())
+    if rc != 0:
+        raise PasaError(rc, "pasa_selftest_wait_timeout")
 
 
 def check_device_error():

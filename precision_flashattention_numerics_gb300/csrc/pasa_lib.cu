@@ -16,6 +16,28 @@
 #include "kshift.cuh"
 #include "ptx.cuh"
 
+namespace pasa {
+
+// Site tag the self-test below records in the device error word.
+constexpr uint32_t kSelftestSite = 0x5E1F7E57u;
+
+// The failure-detection path without a fault: thread 0 waits, through the bounded mbarrier
+// wait every kernel of this library uses, on a barrier that nothing arrives on. The wait
+// gives up after kWaitTimeoutNs, records the timeout in the device error word and returns;
+// the CTA holds no TMA copy and no tensor memory, so it simply ends.
+__global__ void wait_selftest_kernel() {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    (void)mbar_wait(&bar, 0, &abort_flag, kSelftestSite);
+  }
+}
+
+}  // namespace pasa
+
 namespace {
 
 thread_local int t_last_cuda_error = 0;
@@ -703,6 +725,14 @@ int pasa_attn_fwd(const void* q, const void* k, const void* v, void* o, float* l
     if (rc == PASA_OK && e != cudaSuccess) rc = cuda_fail(e);
   }
   return rc;
+}
+
+int pasa_selftest_wait_timeout(void* stream) {
+  int rc = check_device();
+  if (rc != PASA_OK) return rc;
+  pasa::wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>();
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? PASA_OK : cuda_fail(e);
 }
 
 int pasa_check_device_error(void* stream, unsigned long long* info) {

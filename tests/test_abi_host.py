@@ -126,6 +126,8 @@ def test_no_device_here_is_reported_not_launched(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert lib.pasa_device_supported(0) == 0
+    # the failure-detection self-test launches nothing without a supported device
+    assert lib.pasa_selftest_wait_timeout(None) in (-3, -5)
 
 
 def test_fp8_entry_points_check_arguments(lib):
