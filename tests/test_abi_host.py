@@ -344,3 +344,26 @@ def test_host_buffer_plan(lib):
     for shape in [(4, 32, 8, 8192, 8192, 128, True), (2, 5, 5, 9216, 9216, 64, False), (3, 48, 3, 4096, 4224, 64, True)]:
         host_plan_checks(*shape, 0)
         host_plan_checks(*shape, 5)
+
+
+def test_host_buffer_plan_properties(lib):
+    """Random shapes, masks and chunk requests: every plan covers each (unit, query row)
+    once, copies each key once and in order, keeps row pieces tile- and block-aligned, and
+    the staging size holds at least the whole problem."""
+    hypothesis = pytest.importorskip("hypothesis")
+    st = hypothesis.strategies
+
+    @hypothesis.settings(max_examples=300, deadline=None, derandomize=True)
+    @hypothesis.given(B=st.integers(1, 6), Hkv=st.integers(1, 8), g=st.sampled_from([1, 2, 4, 7, 8, 16, 64]),
+                      Sq=st.integers(1, 40000), dk=st.integers(-2000, 3000), D=st.sampled_from([64, 128]),
+                      causal=st.booleans(), chunks=st.integers(0, 70))
+    def check(B, Hkv, g, Sq, dk, D, causal, chunks):
+        Sk = max(1, Sq + dk)
+        plan = host_plan_checks(B, Hkv * g, Hkv, Sq, Sk, D, causal, chunks)
+        units = B * Hkv
+        assert len(plan) >= min(max(chunks, 1), units, 64) if chunks else len(plan) >= 1
+        nbytes = lib.pasa_attn_fwd_host_device_bytes(B, Hkv * g, Hkv, Sq, Sk, D, int(causal), 0, chunks)
+        problem = 2 * B * Hkv * g * Sq * D * 2 + 2 * units * Sk * D * 2 + B * Hkv * g * Sq * 4
+        assert nbytes >= problem and nbytes % 256 == 0
+
+    check()
