@@ -36,8 +36,17 @@ import numpy as np  # noqa: E402
 
 import workloads as wl  # noqa: E402
 
+METRIC = "PASA attn fwd TFLOP/s at 1 GB300; fraction of fp16 tensor peak; RMSE vs fp64"
 DEFAULT_WORKLOAD = "kbias10_t3_b1h28g4_s32768_d128_causal"
-ALSO_WORKLOADS = ["iid_b4h32g8_s8192_d128_causal"]
+# Each extra (workload, mode) of the default run: its TFLOP/s, fraction of the peak and
+# relRMSE against the fp64 oracle. None = the mode of the headline line.
+ALSO_RUNS = [
+    ("kbias20_b1h28g4_s4096_d128_causal", None),
+    ("resonance_a30_b2h5_s9216_d64", None),
+    ("iid_b4h32g8_s8192_d128_causal", None),
+    ("kbias10_t3_b1h28g4_s32768_d128_causal", 1),
+    ("resonance_a30_b2h5_s9216_d64", 1),
+]
 DECODE_WORKLOAD = "kbias10_t3_b8h28g4_q1_s32768_d128_decode"
 MODE_NAMES = {0: "shift_f16acc", 1: "shift_f32acc", 2: "naive_f16acc", 3: "noshift_f32acc", 4: "shift_f16all",
               5: "shift_fp8", 6: "naive_fp8"}
@@ -45,17 +54,15 @@ SHIFT_MODES = (0, 1, 4)     # a pseudo-average shift kernel (fp16 K') runs befor
 FP8_MODES = (5, 6)          # an e4m3 key-preparation kernel runs before it
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one attention-kernel launch,
-# from an ncu capture of a quarter of the 32K workload (7 of 28 query heads, 1 of 4 kv heads:
-# 75.63 MB read + 24.46 MB written) scaled x4 to a full launch; the traffic is per head, so it
-# grows in proportion. Summary and command: profiles/attn_fwd_kbias10_t3_b1h7g1_s32768_full.md.
-# Reported only while the kernel source is the one the counters were taken on.
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one attention-kernel launch
+# on the 32K workload in mode 0, from an ncu capture of one full-size launch. Reported only
+# while the kernel sources are the ones the counters were taken on.
 TRAFFIC_WORKLOAD = "kbias10_t3_b1h28g4_s32768_d128_causal"
 TRAFFIC_MODE = 0
-TRAFFIC_BYTES = 4 * (75.631872e6 + 24.462592e6)
-TRAFFIC_KERNEL_SHA = "ae9385673b602f59"
-# The same for one decode-kernel launch on the decode workload (captured at full size:
-# 539.11 MB read + 3.17 MB written); profiles/decode_fwd_kbias10_t3_b8h28g4_q1_s32768_full.md.
+TRAFFIC_BYTES = None
+TRAFFIC_KERNEL_SHA = None
+# The same for one decode-kernel launch on the decode workload (an ncu capture at full
+# size: 539.11 MB read + 3.17 MB written).
 DECODE_TRAFFIC_BYTES = 539113472 + 3172608
 DECODE_TRAFFIC_SHA = "ca888b56aee96d33"
 
@@ -71,7 +78,8 @@ def _source_sha(name):
 
 
 def measured_traffic(w, mode):
-    if w.name != TRAFFIC_WORKLOAD or mode != TRAFFIC_MODE or _source_sha("attn_fwd.cuh") != TRAFFIC_KERNEL_SHA:
+    if TRAFFIC_BYTES is None or w.name != TRAFFIC_WORKLOAD or mode != TRAFFIC_MODE or \
+            _source_sha("attn_fwd.cuh") != TRAFFIC_KERNEL_SHA:
         return None
     return round(TRAFFIC_BYTES)
 
@@ -174,8 +182,9 @@ def visible_pairs_rows(w: wl.Workload, rows: np.ndarray) -> np.ndarray:
     return np.clip(i + w.Sk - w.Sq + 1, 0, w.Sk)
 
 
-def cpu_oracle_sample(w: wl.Workload, q, k, v, budget_s: float, seed: int = 0):
-    """Time the fp64 oracle on random rows of the workload for about `budget_s` seconds."""
+def cpu_oracle_sample(w: wl.Workload, q, k, v, budget_s: float, seed: int = 0, keep: list | None = None):
+    """Time the fp64 oracle on random rows of the workload for about `budget_s` seconds.
+    With `keep`, the (rows, O_ref) pairs it computed are appended to it."""
     import oracle
 
     rng = np.random.default_rng(seed)
@@ -185,8 +194,10 @@ def cpu_oracle_sample(w: wl.Workload, q, k, v, budget_s: float, seed: int = 0):
     while elapsed < budget_s:
         rows = np.sort(rng.integers(0, total_rows, n)).astype(np.int64)
         t0 = time.perf_counter()
-        oracle.attention(q, k, v, causal=w.causal, rows=rows)
+        o_ref, _ = oracle.attention(q, k, v, causal=w.causal, rows=rows)
         dt = time.perf_counter() - t0
+        if keep is not None:
+            keep.append((rows, o_ref))
         elapsed += dt
         flops += float(4.0 * w.D * visible_pairs_rows(w, rows).sum())
         rows_done += n
@@ -204,10 +215,29 @@ def cpu_oracle_sample(w: wl.Workload, q, k, v, budget_s: float, seed: int = 0):
     }
 
 
-def bench_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int, also: bool = False):
+def rmse_vs_oracle(o, pairs):
+    """relRMSE / relMax (output scale) of device output `o` [B, H, S, D] against fp64 oracle
+    rows: `pairs` is a list of (flat row indices, O_ref rows)."""
+    import torch
+
+    rows = np.concatenate([r for r, _ in pairs])
+    ref = np.concatenate([x for _, x in pairs]).astype(np.float64)
+    flat = o.reshape(-1, o.shape[-1])
+    got = flat.index_select(0, torch.as_tensor(rows, device=o.device, dtype=torch.long)).double().cpu().numpy()
+    if not np.isfinite(got).all():
+        return {"rel_rmse": None, "rel_max": None, "rows": int(len(rows)), "nonfinite_rows": True}
+    d = got - ref
+    return {"rel_rmse": float(np.sqrt(np.mean(d * d)) / np.sqrt(np.mean(ref * ref))),
+            "rel_max": float(np.abs(d).max() / np.abs(ref).max()), "rows": int(len(rows)),
+            "vs": "fp64 oracle (plain attention) on the same fp16 inputs"}
+
+
+def bench_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int, also: bool = False, mode=None):
     import torch
 
     import precision_flashattention_numerics_gb300 as pasa
+
+    mode = args.mode if mode is None else mode
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
@@ -216,8 +246,8 @@ def bench_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int, also
     o = torch.empty_like(qt)
     lse = torch.empty((w.B, w.Hq, w.Sq), device=dev, dtype=torch.float32)
     nb = (w.Sk + pasa.block_rows(w.D) - 1) // pasa.block_rows(w.D)
-    shift = args.mode in SHIFT_MODES
-    fp8 = args.mode in FP8_MODES
+    shift = mode in SHIFT_MODES
+    fp8 = mode in FP8_MODES
     ks = torch.empty_like(kt) if shift else kt
     means = torch.empty((w.B, w.Hkv, nb, w.D), device=dev, dtype=torch.float16) if shift else None
     stream = torch.cuda.current_stream()
@@ -227,14 +257,14 @@ def bench_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int, also
         if shift:
             pasa.kshift(kt, out=ks, means=means)
         elif fp8:
-            prep["k8"], prep["means"], prep["kscale"] = pasa.kprep_fp8(kt, mode=args.mode)
+            prep["k8"], prep["means"], prep["kscale"] = pasa.kprep_fp8(kt, mode=mode)
 
     def attention():
         if fp8:
-            pasa.attn_fwd_fp8(qt, prep["k8"], prep["means"], prep["kscale"], vt, causal=w.causal, mode=args.mode,
+            pasa.attn_fwd_fp8(qt, prep["k8"], prep["means"], prep["kscale"], vt, causal=w.causal, mode=mode,
                               out=o, lse=lse)
         else:
-            pasa.attn_fwd_shifted(qt, ks, means, vt, causal=w.causal, mode=args.mode, out=o, lse=lse)
+            pasa.attn_fwd_shifted(qt, ks, means, vt, causal=w.causal, mode=mode, out=o, lse=lse)
 
     def step():
         prep_keys()
@@ -284,6 +314,7 @@ def bench_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int, also
         "finite": finite,
         "clocks": sampler.summary() if sampler else None,
         "host": (q, k, v),
+        "o": o,
     }
     if also:
         return res
@@ -295,17 +326,17 @@ def bench_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int, also
     lh = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
     B, Hq, Sq, D = qt.shape
     Hkv, Sk = kt.shape[1], kt.shape[2]
-    hbuf = torch.empty(pasa.host_device_bytes(B, Hq, Hkv, Sq, Sk, D, w.causal, args.mode, args.host_chunks),
+    hbuf = torch.empty(pasa.host_device_bytes(B, Hq, Hkv, Sq, Sk, D, w.causal, mode, args.host_chunks),
                        dtype=torch.uint8, device=qt.device)
 
     def e2e_step():
-        pasa.attn_fwd_host(qh, kh, vh, causal=w.causal, mode=args.mode, out=oh, lse=lh, chunks=args.host_chunks,
+        pasa.attn_fwd_host(qh, kh, vh, causal=w.causal, mode=mode, out=oh, lse=lh, chunks=args.host_chunks,
                            device_buffer=hbuf, sync=False)
 
-    for _ in range(2):
+    for _ in range(max(3, args.warmup)):
         e2e_step()
     torch.cuda.synchronize()
-    n_e2e = max(2, min(n, 5))
+    n_e2e = n
     barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
@@ -513,7 +544,7 @@ def main():
                 steps.append(r)
         val = statistics.mean(r["value"] for r in steps)
         out = {
-            "impl": "reference", "metric": "PASA attn fwd TFLOP/s (fp64 CPU oracle)", "value": val,
+            "impl": "reference", "metric": METRIC, "value": val,
             "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": None, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic", "config": config,
@@ -530,29 +561,46 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
 
+    def peak_for(mode):
+        peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))  # fp16 dense = bf16 dense rate
+        note = f"{peak_src} bf16 dense burst (fp16 dense has the same nominal rate)"
+        if mode in FP8_MODES:
+            # half the FLOPs (QK) at the e4m3 rate, nominally 2x the 16-bit one, half (PV) at
+            # fp16: the time at peak is 3/4 of the all-fp16 time
+            peak = peak * 4.0 / 3.0
+            note = (f"{peak_src} bf16 dense burst x 4/3: QK at the e4m3 rate (nominally 2x the 16-bit rate), "
+                    "PV at the fp16 rate")
+        return peak, note
+
     res = bench_gpu(args, w, rank, world, local_rank)
     also = {}
     if not args.no_also and world == 1:
-        for name in ALSO_WORKLOADS:
-            if name == w.name:
+        for name, amode in ALSO_RUNS:
+            amode = args.mode if amode is None else amode
+            if name == w.name and amode == args.mode:
                 continue
             wa = wl.WORKLOADS[name]
-            ra = bench_gpu(args, wa, rank, world, local_rank, also=True)
-            also[name] = {"tflops": round(ra["tflops"], 1), "ms_per_step": round(ra["ms_per_step"], 4),
-                          "attn_ms": round(ra["attn_ms"], 4), "kshift_ms": round(ra["kshift_ms"], 4),
-                          "finite": ra["finite"]}
+            ra = bench_gpu(args, wa, rank, world, local_rank, also=True, mode=amode)
+            aq, ak, av = ra["host"]
+            rows = wl.sample_rows(wa, 128)
+            import oracle
+
+            o_ref, _ = oracle.attention(aq, ak, av, causal=wa.causal, rows=rows)
+            apeak, _ = peak_for(amode)
+            attn_tf = ra["flops"] / (ra["attn_ms"] * 1e-3) / 1e12
+            also[f"{name}/{MODE_NAMES[amode]}"] = {
+                "workload": name, "mode": MODE_NAMES[amode], "tflops": round(ra["tflops"], 1),
+                "ms_per_step": round(ra["ms_per_step"], 4), "attn_ms": round(ra["attn_ms"], 4),
+                "attn_tflops": round(attn_tf, 1), "attn_frac": round(attn_tf / apeak, 4),
+                "kshift_ms": round(ra["kshift_ms"], 4), "finite": ra["finite"],
+                "rmse": rmse_vs_oracle(ra["o"], [(rows, o_ref)]), "steps": args.steps,
+                "warmup": max(3, args.warmup)}
+            del ra
         also[DECODE_WORKLOAD] = bench_decode(args, wl.WORKLOADS[DECODE_WORKLOAD], local_rank)
         if args.mode not in FP8_MODES:
             also["overflow_diagnostic"] = bench_stats(args, w, local_rank)
 
-    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))  # fp16 dense = bf16 dense rate
-    peak_note = f"{peak_src} bf16 dense burst (fp16 dense has the same nominal rate)"
-    if args.mode in FP8_MODES:
-        # half the FLOPs (QK) at the e4m3 rate, nominally 2x the 16-bit one, half (PV) at fp16:
-        # the time at peak is 3/4 of the all-fp16 time
-        peak = peak * 4.0 / 3.0
-        peak_note = (f"{peak_src} bf16 dense burst x 4/3: QK at the e4m3 rate (nominally 2x the 16-bit rate), "
-                     "PV at the fp16 rate")
+    peak, peak_note = peak_for(args.mode)
     traffic = measured_traffic(w, args.mode)
     attn_achieved = res["flops"] / (res["attn_ms"] * 1e-3) / 1e12
     roofline = {
@@ -583,21 +631,31 @@ def main():
                            "frac": round(dec["attn_gbs"] / hbm, 4),
                            "traffic": measured_decode_traffic(args.mode), "peak_source": f"{peak_src} copy bandwidth"}
 
+    # accuracy of the timed steps' output: the oracle's rows from the cpu_baseline leg (or,
+    # without it, a fixed sample of rows)
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    pairs = []
+    if rank == 0:
         q, k, v = res["host"]
-        cpu = cpu_oracle_sample(w, q, k, v, budget_s=args.cpu_budget)
+        if world == 1 and not args.no_cpu_baseline:
+            cpu = cpu_oracle_sample(w, q, k, v, budget_s=args.cpu_budget, keep=pairs)
+        else:
+            import oracle
+
+            rows = wl.sample_rows(w, 128)
+            pairs = [(rows, oracle.attention(q, k, v, causal=w.causal, rows=rows)[0])]
+    rmse = rmse_vs_oracle(res["o"], pairs) if rank == 0 else None
 
     if rank == 0:
         out = {
-            "metric": "PASA attn fwd TFLOP/s at 1 GB300 (fraction of dense fp16 tensor peak in roofline)",
+            "metric": METRIC,
             "value": round(res["tflops"], 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": max(3, args.warmup), "ms_per_step": round(res["ms_per_step"], 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3+f16" if args.mode in FP8_MODES else "f16",
             "data": "synthetic", "config": config,
             "roofline": roofline, "kshift": kshift_kernel, "cpu_baseline": cpu, "e2e": res["e2e"],
             "gpu_launches": args.steps * (2 if (args.mode in SHIFT_MODES or args.mode in FP8_MODES) else 1), "clocks": res["clocks"],
-            "finite_output": res["finite"], "also": also,
+            "finite_output": res["finite"], "rmse": rmse, "also": also,
         }
         print(json.dumps(out))
     if world > 1:

@@ -20,7 +20,10 @@
  *     asynchronously: a PASA_OK return means "validated and launched", like a CUDA kernel
  *     launch. Argument errors are detected on the host before anything is enqueued.
  *   - Device-side failures (a pipeline wait that timed out) are latched in a device error
- *     word and reported by pasa_check_device_error().
+ *     word and reported by pasa_check_device_error(). No entry point reads that word by
+ *     itself: the launch that timed out returned PASA_OK, and its outputs are invalid. A
+ *     timeout ends only the launch it happened in (its other CTAs stop waiting too); later
+ *     launches run normally, whether or not the word has been read.
  *   - Supported: D in {64, 128}; B, Hq, Hkv, Sq, Sk >= 1; Hq % Hkv == 0; a GPU of compute
  *     capability 10.3 (sm_103a). Anything else returns an error and launches nothing.
  *   - Causal masking is bottom-right aligned: key j is visible to query i iff
@@ -392,8 +395,8 @@ int pasa_device_supported(int device);
  * timeout in the device error word, with site tag 0x5E1F7E57 as the low 32 bits of the
  * info word, and the kernel returns. It holds no TMA copy and no tensor memory, so the GPU
  * context stays usable: pasa_check_device_error(stream, &info) then returns
- * PASA_ERR_TIMEOUT with that tag and clears the word. Any error already latched in the word
- * makes the wait give up at once instead, keeping the first error's info.
+ * PASA_ERR_TIMEOUT with that tag and clears the word. If the word already holds an unread
+ * error, the wait still runs to its limit and the word keeps the first error's info.
  *   stream  where the CTA runs. Returns PASA_OK once launched; errors as for every entry
  *           point (no supported device: PASA_ERR_UNSUPPORTED; a failed launch:
  *           PASA_ERR_CUDA).

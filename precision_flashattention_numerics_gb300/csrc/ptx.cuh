@@ -2,9 +2,10 @@
 // tcgen05 (TMEM alloc, MMA, commit, ld/st, fences) and shared-memory matrix descriptors.
 //
 // Every mbarrier wait in this library is bounded: it polls with try_wait, gives up after
-// kWaitTimeoutNs of %globaltimer time (or as soon as another CTA has recorded an error),
-// records PASA_DEVICE_ERR_TIMEOUT in the device error word and returns false, so a
-// broken pipeline ends the kernel instead of hanging the GPU.
+// kWaitTimeoutNs of %globaltimer time (or as soon as another CTA of the same launch has
+// given up), records a timeout in the device error word and returns false, so a broken
+// pipeline ends the kernel instead of hanging the GPU. The early abort is scoped to one
+// launch: a timeout nobody has read yet does not make later launches give up.
 #pragma once
 
 #include <cstdint>
@@ -22,9 +23,13 @@ enum : int {
 };
 
 // Defined here: the library is compiled as a single translation unit that includes this
-// header once.
+// header once. g_device_error and g_device_error_info latch the first timeout until the host
+// reads them (pasa_check_device_error). g_abort_grid holds the grid id (%gridid, a number the
+// driver gives each launch in a context) of the launch that last timed out: the other CTAs of
+// that launch see it and stop waiting, while CTAs of any other launch ignore it.
 __device__ int g_device_error = 0;
 __device__ unsigned long long g_device_error_info = 0;
+__device__ unsigned long long g_abort_grid = 0;
 
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s per wait
 
@@ -86,27 +91,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Record a timeout (first one wins) with a caller-supplied site tag, and raise the CTA's
-// abort flag.
+__device__ __forceinline__ unsigned long long grid_id() {
+  unsigned long long g;
+  asm volatile("mov.u64 %0, %%gridid;" : "=l"(g));
+  return g;
+}
+
+// Record a timeout (first one wins) with a caller-supplied site tag, raise the CTA's abort
+// flag and publish this launch's grid id to its other CTAs.
 __device__ __forceinline__ void record_timeout(volatile int* abort_flag, uint32_t site) {
   *abort_flag = 1;
+  atomicExch(&g_abort_grid, grid_id());
   if (atomicCAS(&g_device_error, kDeviceOk, kDeviceErrTimeout) == kDeviceOk) {
     g_device_error_info = (static_cast<unsigned long long>(blockIdx.x) << 32) | site;
   }
 }
 
-// Bounded wait for phase `parity` of `bar`. Returns false if this CTA (or any CTA, via the
-// device error word) has given up.
+// Bounded wait for phase `parity` of `bar`. Returns false if this CTA, or another CTA of the
+// same launch, has given up.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           uint32_t site) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
+  const unsigned long long gid = grid_id();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (*reinterpret_cast<volatile int*>(&g_device_error) != kDeviceOk) {
+    if (*reinterpret_cast<volatile unsigned long long*>(&g_abort_grid) == gid) {
       *abort_flag = 1;
       return false;
     }

@@ -25,6 +25,9 @@ def test_reference_arm_json_line():
     assert len(lines) == 1
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["higher_is_better"] is True
+    import bench
+
+    assert d["metric"] == bench.METRIC     # the GPU arm prints the same metric, so the two compare
     assert d["value"] > 0 and d["steps"] == 2 and d["warmup"] == 1
     assert d["config"]["workload"] == "iid_b1h1_s128_d64"
     cb = d["cpu_baseline"]

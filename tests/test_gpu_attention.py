@@ -5,7 +5,10 @@
 fp16 scores from overflowing (65504) under large sequence-dimension bias and Q/K
 resonance, and is judged by RMSE against high-precision attention. Tolerances (output
 scale): relRMSE <= 2e-3 and relMax <= 1e-2 on unbiased data; no inf/NaN and relRMSE <= 5e-3
-on biased and resonance data. LSE is compared in absolute terms.
+on biased and resonance data, except where the scores are accumulated in fp16 at
+magnitudes where that cannot hold (resonance keys: shifted scores near 1e4, fp16 spacing
+8-16): there the gate is 2x the relRMSE that an fp16 accumulator's rounding predicts
+(gpu_helpers.f16_score_rmse_model). LSE is compared in absolute terms.
 """
 import json
 import math
@@ -17,7 +20,8 @@ import torch
 
 import oracle
 import workloads as wl
-from gpu_helpers import f16all_bound, gather_rows, lse_tolerance, rel_errors, to_dev
+from gpu_helpers import (f16_score_rmse_gate, f16_score_rmse_model, f16all_bound, gather_rows, lse_tolerance,
+                         rel_errors, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -179,16 +183,26 @@ def full_inputs(name):
     return _inputs_cache[name]
 
 
-# (relRMSE, relMax) gates per (workload kind, mode); None = reported, only finiteness checked
-def gate(w, mode):
+# (relRMSE, relMax) gates per (workload, mode). The fp16-accumulated score modes on biased
+# and resonance inputs, and mode 4 everywhere, are gated on the fp16-accumulation error
+# model of gpu_helpers.f16_score_rmse_model (a relRMSE bound, no relMax): on resonance keys
+# the shifted scores stay near 1e4 (fp16 spacing 8-16), where no fixed 5e-3 holds for an
+# fp16 accumulator, but a kernel that loses accuracy beyond its accumulator still fails.
+_model_cache = {}
+
+
+def gate(name, w, mode):
     unbiased = w.kind == "iid"
-    if mode == 2:
-        return (2e-3, 1e-2) if unbiased else None
-    if mode == 0 and w.kind == "resonance":
-        return None   # fp16 accumulation of resonance scores (|S'| ~ 1e4, ulp 8): reported only
-    if mode == 4:
-        return None   # fp16 PV and row sum over up to 256 blocks: the bound is loose, reported only
-    return (2e-3, 1e-2) if unbiased else (5e-3, None)
+    if mode in (0, 2, 4) and (not unbiased or mode == 4):
+        if (name, mode) not in _model_cache:
+            _, (q, k, v), _, rows, _, _ = full_inputs(name)
+            _model_cache[(name, mode)] = f16_score_rmse_model(q, k, v, w.causal, mode, rows)
+        pred = _model_cache[(name, mode)]
+        g = f16_score_rmse_gate(pred)
+        if mode == 0 and w.kind != "resonance":
+            g = min(g, 5e-3)    # PASA on biased keys also keeps the contract's 5e-3
+        return g, None, pred
+    return ((2e-3, 1e-2) if unbiased else (5e-3, None)) + (None,)
 
 
 FULL_CASES = [(n, m) for n in FULL for m in MODES + [4]]
@@ -210,11 +224,13 @@ def test_full_size_sampled_rows(name, mode):
         assert n_bad > 0, "the naive fp16 kernel is expected to overflow on this input"
         return
     assert n_bad == 0
-    g = gate(w, mode)
-    if g is not None:
-        assert rmse <= g[0], rmse
-        if g[1] is not None:
-            assert rmax <= g[1], rmax
+    g_rmse, g_rmax, pred = gate(name, w, mode)
+    if pred is not None:
+        print(f"fp16-score model: predicted relRMSE {pred:.3e}, gate {g_rmse:.3e}, measured/predicted "
+              f"{rmse / pred:.2f}")
+    assert rmse <= g_rmse, (rmse, g_rmse)
+    if g_rmax is not None:
+        assert rmax <= g_rmax, (rmax, g_rmax)
 
 
 # ---------------------------------------------------------------------------------------
@@ -286,3 +302,53 @@ def test_f16all_differs_from_f32_accumulation():
     o0, _ = run(q, k, v, False, 0)
     o4, _ = run(q, k, v, False, 4)
     assert not torch.equal(o0, o4)
+
+
+# ---------------------------------------------------------------------------------------
+# pasa_attn_fwd itself (the contract's signature: the library takes its shift workspace
+# from the stream-ordered allocator), called through ctypes and compared with the oracle
+# ---------------------------------------------------------------------------------------
+def _attn_fwd_c_abi(q, k, v, causal, mode):
+    import ctypes
+
+    lib = pasa().library()
+    B, Hq, Sq, D = q.shape
+    _, Hkv, Sk, _ = k.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, Sq), device=q.device, dtype=torch.float32)
+    P = ctypes.c_void_p
+    rc = lib.pasa_attn_fwd(P(q.data_ptr()), P(k.data_ptr()), P(v.data_ptr()), P(o.data_ptr()), P(lse.data_ptr()),
+                           B, Hq, Hkv, Sq, Sk, D, int(causal), 0.0, mode, P(torch.cuda.current_stream().cuda_stream))
+    assert rc == 0, lib.pasa_strerror(rc)
+    pasa().check_device_error()
+    return o, lse
+
+
+C_ABI_CASES = [
+    # (B, Hq, Hkv, Sq, Sk, D, causal, kind, params): K bias 20 non-causal; causal GQA with a ragged tail
+    (1, 4, 4, 640, 700, 128, False, "kbias", {"bias_std": 20.0}),
+    (2, 6, 2, 333, 333, 64, True, "iid", {}),
+    (1, 8, 2, 1000, 1000, 128, True, "kbias_t3", {"bias_std": 10.0, "t_dof": 3, "t_scale": 4.0}),
+]
+
+
+@pytest.mark.parametrize("mode", [0, 1], ids=[MODE_NAMES[m] for m in (0, 1)])
+@pytest.mark.parametrize("case", range(len(C_ABI_CASES)))
+def test_pasa_attn_fwd_c_abi_against_oracle(case, mode):
+    B, Hq, Hkv, Sq, Sk, D, causal, kind, params = C_ABI_CASES[case]
+    q, k, v = small_case(B, Hq, Hkv, Sq, Sk, D, kind, 400 + case, **params)
+    qt, kt, vt = to_dev(q, k, v)
+    o, lse = _attn_fwd_c_abi(qt, kt, vt, causal, mode)
+    o_ref, lse_ref = oracle.attention(q, k, v, causal=causal)
+    og = o.double().cpu().numpy()
+    lg = lse.double().cpu().numpy()
+    assert np.isfinite(og).all()
+    rmse, rmax = rel_errors(og, o_ref)
+    tol = (5e-3, 5e-2) if kind != "iid" else (2e-3, 1e-2)
+    assert rmse <= tol[0] and rmax <= tol[1], (rmse, rmax)
+    fin = np.isfinite(lse_ref)
+    assert np.all(np.isneginf(lg[~fin]))
+    assert np.max(np.abs(lg[fin] - lse_ref[fin])) <= lse_tolerance(q, k, causal, mode, D)
+    # and the same bytes as the workspace entry point the other tests use
+    o_ws, lse_ws = pasa().attn_fwd(qt, kt, vt, causal=causal, mode=mode)
+    assert torch.equal(o, o_ws) and torch.equal(lse, lse_ws)

@@ -4,7 +4,8 @@ Every wait in the library's kernels is bounded: after a limit it records a timeo
 device error word and the kernel returns, so the host can read the error and the context
 stays usable. pasa_selftest_wait_timeout runs that wait on a barrier nothing arrives on;
 this test checks the status the host reads, the site tag, that the word is cleared, and
-that the next attention call is correct (checked against the fp64 oracle).
+that the next attention call is correct (checked against the fp64 oracle). A timeout ends
+only its own launch: a later launch is correct even while the timeout is still unread.
 """
 import ctypes
 import time
@@ -61,3 +62,28 @@ def test_python_check_raises_the_timeout():
         p.check_device_error()
     assert exc.value.status == PASA_ERR_TIMEOUT
     p.check_device_error()   # cleared
+
+
+def test_unread_timeout_does_not_abort_later_launches():
+    # The error word latches the timeout until it is read, but the abort that lets the other
+    # CTAs of a failed launch stop early is keyed to that launch: the attention call queued
+    # behind an unread timeout must still be correct, and the timeout must still be reported.
+    import precision_flashattention_numerics_gb300 as p
+
+    lib = p.library()
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    info = ctypes.c_ulonglong(0)
+    assert lib.pasa_check_device_error(stream, ctypes.byref(info)) == 0, "an error was already pending"
+    p.selftest_wait_timeout()
+    w = wl.Workload("behind_timeout", 1, 8, 2, 1000, 1000, 128, True, "kbias", 791, (("bias_std", 20.0),))
+    q, k, v = wl.make_inputs(w)
+    qt, kt, vt = to_dev(q, k, v)
+    o, lse = p.attn_fwd(qt, kt, vt, causal=True, mode=0)      # queued behind the timed-out kernel
+    torch.cuda.synchronize()
+    rc = lib.pasa_check_device_error(stream, ctypes.byref(info))
+    assert rc == PASA_ERR_TIMEOUT and info.value & 0xFFFFFFFF == SELFTEST_SITE
+    o_ref, lse_ref = oracle.attention(q, k, v, causal=True)
+    rmse, rmax = rel_errors(o.double().cpu().numpy(), o_ref)
+    assert rmse <= 5e-3 and rmax <= 5e-2, (rmse, rmax)
+    assert np.abs(lse.double().cpu().numpy() - lse_ref).max() <= 1e-2
+    assert lib.pasa_check_device_error(stream, ctypes.byref(info)) == 0
