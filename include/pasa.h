@@ -22,8 +22,8 @@
  *   - Device-side failures (a pipeline wait that timed out) are latched in a device error
  *     word and reported by pasa_check_device_error(). No entry point reads that word by
  *     itself: the launch that timed out returned PASA_OK, and its outputs are invalid. A
- *     timeout ends only the launch it happened in (its other CTAs stop waiting too); later
- *     launches run normally, whether or not the word has been read.
+ *     timeout ends only the CTA it happened in (each CTA of a broken launch gives up at its
+ *     own 2 s limit); other launches run normally, whether or not the word has been read.
  *   - Supported: D in {64, 128}; B, Hq, Hkv, Sq, Sk >= 1; Hq % Hkv == 0; a GPU of compute
  *     capability 10.3 (sm_103a). Anything else returns an error and launches nothing.
  *   - Causal masking is bottom-right aligned: key j is visible to query i iff
@@ -402,6 +402,21 @@ int pasa_device_supported(int device);
  *           PASA_ERR_CUDA).
  */
 int pasa_selftest_wait_timeout(void* stream);
+
+/*
+ * Evaluates the two exponentials the attention kernels' softmax uses, for testing. (The paper
+ * has no counterpart: the softmax's exp2 is an implementation detail of this library.) For
+ * each of the n fp32 values x[i] (device pointers, n >= 1):
+ *   poly[i] = 2^x[i] on the FMA pipe: Cody-Waite split x = rint(x) + f, f in [-1/2, 1/2],
+ *             a cubic fitted to 2^f (max relative error 7.5e-5) times 2^rint(x) built in the
+ *             exponent field; x <= -126 (or -inf) gives a value in [0, 2^-125]; NaN gives
+ *             NaN; x must be <= 127 (+inf gives NaN).
+ *   mufu[i] = ex2.approx.ftz.f32 of x[i] (the MUFU exponential).
+ * The kernels compute a fixed share of each key block's probabilities with the first and
+ * the rest with the second. Errors: PASA_ERR_NULLPTR, PASA_ERR_SHAPE (n <= 0),
+ * PASA_ERR_UNSUPPORTED (device), PASA_ERR_CUDA (launch). Asynchronous on `stream`.
+ */
+int pasa_selftest_exp2(const float* x, float* poly, float* mufu, int n, void* stream);
 
 #ifdef __cplusplus
 }

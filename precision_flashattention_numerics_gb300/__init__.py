@@ -62,6 +62,7 @@ SIGNATURES = {
     "pasa_attn_fwd_host_plan": ([_I] * 9 + [_P, _I], _I),
     "pasa_check_device_error": ([_P, ctypes.POINTER(ctypes.c_ulonglong)], _I),
     "pasa_selftest_wait_timeout": ([_P], _I),
+    "pasa_selftest_exp2": ([_P, _P, _P, _I, _P], _I),
     "pasa_strerror": ([_I], ctypes.c_char_p),
     "pasa_last_cuda_error": ([], _I),
     "pasa_device_supported": ([_I], _I),
@@ -416,6 +417,19 @@ def selftest_wait_timeout():
     rc = library().pasa_selftest_wait_timeout(_stream())
     if rc != 0:
         raise PasaError(rc, "pasa_selftest_wait_timeout")
+
+
+def selftest_exp2(x):
+    """(poly, mufu): the softmax's two exponentials 2^x of a CUDA fp32 tensor
+    (pasa_selftest_exp2): the FMA-pipe polynomial and MUFU ex2.approx."""
+    if not isinstance(x, torch.Tensor) or not x.is_cuda or x.dtype != torch.float32 or not x.is_contiguous():
+        raise TypeError("x must be a contiguous CUDA fp32 tensor")
+    poly = torch.empty_like(x)
+    mufu = torch.empty_like(x)
+    rc = library().pasa_selftest_exp2(_ptr(x), _ptr(poly), _ptr(mufu), x.numel(), _stream())
+    if rc != 0:
+        raise PasaError(rc, "pasa_selftest_exp2")
+    return poly, mufu
 
 
 def check_device_error():

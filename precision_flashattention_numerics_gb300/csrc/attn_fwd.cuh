@@ -62,6 +62,27 @@ constexpr int kChunkBlocks = 16;     // key blocks per offsets MMA (its N)
 constexpr int kAttnThreads = 224;
 constexpr float kRescaleLog2 = 8.0f;
 
+// The softmax's exponentials of a block: pair c (two scores) runs on the FMA pipe
+// (exp2_fma2) when bit (c mod 16) of kPolyMask is set and on MUFU (ex2.approx) otherwise.
+// On GB300 MUFU retires ex2.approx.f32 at 8 lanes a clock per SM sub-partition (4 cycles per
+// warp instruction, 32 per clock per SM), so a block's 128 exponentials per row take 512
+// cycles of MUFU time against ~1100 cycles of MMA: MUFU is not what bounds the softmax,
+// while the FMA-pipe form costs 7 FMA-pipe lane operations per value (1.75x MUFU's pipe
+// time) and lengthens the softmax's chain. Measured on the 32K causal and the D = 64
+// resonance workloads, 1, 2 and 5 pairs of 16 on the FMA pipe all ran slower than none
+// (e.g. 5 of 16: 1225 vs 1365 and 690 vs 775 TFLOP/s), so the mask is empty.
+constexpr uint32_t kPolyMask = 0x0000u;
+
+__device__ __forceinline__ void exp2_split(float& p0, float& p1, float x0, float x1, int c) {
+  if ((kPolyMask >> (c & 15)) & 1u) {
+    exp2_fma2(p0, p1, x0, x1);
+  } else {
+    p0 = ex2_approx(x0);
+    p1 = ex2_approx(x1);
+  }
+}
+
+
 struct AttnParams {
   float* lse;            // [B, Hq, Sq] fp32 or nullptr
   int B, Hq, Hkv, Sq, Sk;
@@ -599,8 +620,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
           float y0, y1, x0, x1;
           add_f16x2_f32(y0, y1, hp[c], b16);
           fmul2(x0, x1, y0, y1, sl2, sl2);
-          const float p0 = ex2_approx(x0);
-          const float p1 = ex2_approx(x1);
+          float p0, p1;
+          exp2_split(p0, p1, x0, x1, c);
           pk[c] = pack_half2(p0, p1);
           if constexpr (F16PV) {
             hs[c & 3] = hadd2(hs[c & 3], pk[c]);
@@ -616,8 +637,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         for (int c = 0; c < kPairs; ++c) {
           float x0, x1;
           ffma2(x0, x1, sv[2 * c], sv[2 * c + 1], mul, mul, bias, bias);
-          const float p0 = ex2_approx(x0);
-          const float p1 = ex2_approx(x1);
+          float p0, p1;
+          exp2_split(p0, p1, x0, x1, c);
           const int a = (c & 3) * 2;
           fadd2(rs[a], rs[a + 1], rs[a], rs[a + 1], p0, p1);
           pk[c] = pack_half2(p0, p1);

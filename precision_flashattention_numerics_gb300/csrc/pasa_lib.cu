@@ -36,6 +36,24 @@ __global__ void wait_selftest_kernel() {
   }
 }
 
+// Element i: the FMA-pipe exponential the softmax uses for part of its scores (poly) and the
+// MUFU one it uses for the rest (mufu), both of x[i]; pairs go through exp2_fma2 together.
+__global__ void exp2_selftest_kernel(const float* __restrict__ x, float* __restrict__ poly, float* __restrict__ mufu,
+                                     int n) {
+  const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
+  if (i >= n) return;
+  const float x0 = x[i];
+  const float x1 = i + 1 < n ? x[i + 1] : 0.0f;
+  float p0, p1;
+  exp2_fma2(p0, p1, x0, x1);
+  poly[i] = p0;
+  mufu[i] = ex2_approx(x0);
+  if (i + 1 < n) {
+    poly[i + 1] = p1;
+    mufu[i + 1] = ex2_approx(x1);
+  }
+}
+
 }  // namespace pasa
 
 namespace {
@@ -731,6 +749,17 @@ int pasa_selftest_wait_timeout(void* stream) {
   int rc = check_device();
   if (rc != PASA_OK) return rc;
   pasa::wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>();
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? PASA_OK : cuda_fail(e);
+}
+
+int pasa_selftest_exp2(const float* x, float* poly, float* mufu, int n, void* stream) {
+  if (!x || !poly || !mufu) return PASA_ERR_NULLPTR;
+  if (n <= 0) return PASA_ERR_SHAPE;
+  int rc = check_device();
+  if (rc != PASA_OK) return rc;
+  const int pairs = (n + 1) / 2;
+  pasa::exp2_selftest_kernel<<<(pairs + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(x, poly, mufu, n);
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? PASA_OK : cuda_fail(e);
 }

@@ -2,10 +2,11 @@
 // tcgen05 (TMEM alloc, MMA, commit, ld/st, fences) and shared-memory matrix descriptors.
 //
 // Every mbarrier wait in this library is bounded: it polls with try_wait, gives up after
-// kWaitTimeoutNs of %globaltimer time (or as soon as another CTA of the same launch has
-// given up), records a timeout in the device error word and returns false, so a broken
-// pipeline ends the kernel instead of hanging the GPU. The early abort is scoped to one
-// launch: a timeout nobody has read yet does not make later launches give up.
+// kWaitTimeoutNs of %globaltimer time (or as soon as another warp of its CTA has given up),
+// records a timeout in the device error word and returns false, so a broken pipeline ends
+// the kernel instead of hanging the GPU. The abort stays inside the CTA: a timeout, read
+// or not, never makes another CTA or a later launch give up; each waiting CTA of a broken
+// launch reaches its own limit.
 #pragma once
 
 #include <cstdint>
@@ -24,12 +25,9 @@ enum : int {
 
 // Defined here: the library is compiled as a single translation unit that includes this
 // header once. g_device_error and g_device_error_info latch the first timeout until the host
-// reads them (pasa_check_device_error). g_abort_grid holds the grid id (%gridid, a number the
-// driver gives each launch in a context) of the launch that last timed out: the other CTAs of
-// that launch see it and stop waiting, while CTAs of any other launch ignore it.
+// reads them (pasa_check_device_error); no kernel reads them.
 __device__ int g_device_error = 0;
 __device__ unsigned long long g_device_error_info = 0;
-__device__ unsigned long long g_abort_grid = 0;
 
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s per wait
 
@@ -91,38 +89,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-__device__ __forceinline__ unsigned long long grid_id() {
-  unsigned long long g;
-  asm volatile("mov.u64 %0, %%gridid;" : "=l"(g));
-  return g;
-}
-
-// Record a timeout (first one wins) with a caller-supplied site tag, raise the CTA's abort
-// flag and publish this launch's grid id to its other CTAs.
+// Record a timeout (first one wins) with a caller-supplied site tag, and raise the CTA's
+// abort flag.
 __device__ __forceinline__ void record_timeout(volatile int* abort_flag, uint32_t site) {
   *abort_flag = 1;
-  atomicExch(&g_abort_grid, grid_id());
   if (atomicCAS(&g_device_error, kDeviceOk, kDeviceErrTimeout) == kDeviceOk) {
     g_device_error_info = (static_cast<unsigned long long>(blockIdx.x) << 32) | site;
   }
 }
 
-// Bounded wait for phase `parity` of `bar`. Returns false if this CTA, or another CTA of the
-// same launch, has given up.
+// Bounded wait for phase `parity` of `bar`. Returns false if this CTA has given up.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           uint32_t site) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  const unsigned long long gid = grid_id();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (*reinterpret_cast<volatile unsigned long long*>(&g_abort_grid) == gid) {
-      *abort_flag = 1;
-      return false;
-    }
     if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
       record_timeout(abort_flag, site);
       return false;
@@ -441,6 +426,16 @@ __device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1, 
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
+__device__ __forceinline__ void fsub2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "sub.rn.f32x2 rd, ra, rb;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 __device__ __forceinline__ void fmul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
   asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
       "mov.b64 ra, {%2, %3};\n\t"
@@ -500,6 +495,48 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// 2^x for two values on the FMA pipe instead of MUFU (the exponential unit issues 4 lanes a
+// clock per SM sub-partition against the FMA pipe's 32, so moving a share of a softmax's
+// exponentials here shortens the MUFU queue). Cody and Waite's range reduction
+// (W. J. Cody, W. Waite, "Software Manual for the Elementary Functions", 1980) splits
+// x = n + f with n = rint(x) and f in [-1/2, 1/2]; 2^n is an exponent-field add and 2^f a
+// cubic fitted in this library by a minimax (linear-programming) fit of the relative error
+// on [-1/2, 1/2]: max relative error 7.5e-5 in fp32 Horner evaluation, below half an fp16
+// spacing (2^-12), the rounding P gets anyway.
+//   rint: y = x + 1.5 * 2^23 holds rint(x) (round to nearest even) in its low mantissa
+//   bits for |x| < 2^22, so y - 1.5 * 2^23 is rint(x) and (bits(y) << 23) + bits(1.0) is
+//   the fp32 number 2^n, which multiplies the cubic.
+//   Range: x is first raised to -126 (max.NaN keeps NaN), so 2^n >= 2^-126 stays a normal
+//   number: the result for x <= -126 is a value below 2^-125 (0 once rounded to fp16,
+//   nothing in an fp32 sum). NaN gives NaN and +inf gives NaN (through f = inf - inf).
+//   x must be <= 127.
+constexpr float kExp2C0 = 0.999927998f;  // 0x3F7FFB48
+constexpr float kExp2C1 = 0.693260968f;  // 0x3F31798D
+constexpr float kExp2C2 = 0.242611378f;  // 0x3E786F1E
+constexpr float kExp2C3 = 0.0551717766f;  // 0x3D61FBCD
+
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+
+__device__ __forceinline__ void exp2_fma2(float& p0, float& p1, float x0, float x1) {
+  constexpr float kRint = 12582912.0f;   // 1.5 * 2^23
+  x0 = max_nan(x0, -126.0f);
+  x1 = max_nan(x1, -126.0f);
+  float y0, y1, n0, n1, f0, f1, q0, q1;
+  fadd2(y0, y1, x0, x1, kRint, kRint);
+  fsub2(n0, n1, y0, y1, kRint, kRint);
+  fsub2(f0, f1, x0, x1, n0, n1);
+  ffma2(q0, q1, f0, f1, kExp2C3, kExp2C3, kExp2C2, kExp2C2);
+  ffma2(q0, q1, q0, q1, f0, f1, kExp2C1, kExp2C1);
+  ffma2(q0, q1, q0, q1, f0, f1, kExp2C0, kExp2C0);
+  const float s0 = __uint_as_float((__float_as_uint(y0) << 23) + 0x3F800000u);
+  const float s1 = __uint_as_float((__float_as_uint(y1) << 23) + 0x3F800000u);
+  fmul2(p0, p1, q0, q1, s0, s1);
 }
 
 }  // namespace pasa

@@ -5,7 +5,7 @@ device error word and the kernel returns, so the host can read the error and the
 stays usable. pasa_selftest_wait_timeout runs that wait on a barrier nothing arrives on;
 this test checks the status the host reads, the site tag, that the word is cleared, and
 that the next attention call is correct (checked against the fp64 oracle). A timeout ends
-only its own launch: a later launch is correct even while the timeout is still unread.
+only the CTA it happened in: a later launch is correct even while the timeout is still unread.
 """
 import ctypes
 import time
@@ -65,9 +65,10 @@ def test_python_check_raises_the_timeout():
 
 
 def test_unread_timeout_does_not_abort_later_launches():
-    # The error word latches the timeout until it is read, but the abort that lets the other
-    # CTAs of a failed launch stop early is keyed to that launch: the attention call queued
-    # behind an unread timeout must still be correct, and the timeout must still be reported.
+    # The error word latches the timeout until it is read, but no kernel reads it: a wait
+    # gives up only at its own limit or when another warp of its CTA has given up. The
+    # attention call queued behind an unread timeout must still be correct, and the timeout
+    # must still be reported.
     import precision_flashattention_numerics_gb300 as p
 
     lib = p.library()
