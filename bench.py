@@ -41,11 +41,14 @@ DEFAULT_WORKLOAD = "kbias10_t3_b1h28g4_s32768_d128_causal"
 # Each extra (workload, mode) of the default run: its TFLOP/s, fraction of the peak and
 # relRMSE against the fp64 oracle. None = the mode of the headline line.
 ALSO_RUNS = [
-    ("kbias20_b1h28g4_s4096_d128_causal", None),
-    ("resonance_a30_b2h5_s9216_d64", None),
-    ("iid_b4h32g8_s8192_d128_causal", None),
-    ("kbias10_t3_b1h28g4_s32768_d128_causal", 1),
-    ("resonance_a30_b2h5_s9216_d64", 1),
+    ("kbias20_b1h28g4_s4096_d128_causal", None, False),
+    ("resonance_a30_b2h5_s9216_d64", None, False),
+    ("iid_b4h32g8_s8192_d128_causal", None, False),
+    ("kbias10_t3_b1h28g4_s32768_d128_causal", 1, False),
+    ("resonance_a30_b2h5_s9216_d64", 1, False),
+    # the shift fused into the attention kernel (one launch, raw keys) on the same workloads
+    ("kbias10_t3_b1h28g4_s32768_d128_causal", None, True),
+    ("iid_b4h32g8_s8192_d128_causal", None, True),
 ]
 DECODE_WORKLOAD = "kbias10_t3_b8h28g4_q1_s32768_d128_decode"
 MODE_NAMES = {0: "shift_f16acc", 1: "shift_f32acc", 2: "naive_f16acc", 3: "noshift_f32acc", 4: "shift_f16all",
@@ -232,12 +235,16 @@ def rmse_vs_oracle(o, pairs):
             "vs": "fp64 oracle (plain attention) on the same fp16 inputs"}
 
 
-def bench_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int, also: bool = False, mode=None):
+def bench_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int, also: bool = False, mode=None,
+              fused=None):
     import torch
 
     import precision_flashattention_numerics_gb300 as pasa
 
     mode = args.mode if mode is None else mode
+    fused = args.fused if fused is None else fused
+    if fused and (w.D != 128 or mode not in SHIFT_MODES):
+        raise SystemExit("--fused needs D = 128 and a shift mode (0, 1, 4)")
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
@@ -254,13 +261,17 @@ def bench_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int, also
     prep = {}
 
     def prep_keys():
+        if fused:
+            return   # the attention kernel shifts the keys itself
         if shift:
             pasa.kshift(kt, out=ks, means=means)
         elif fp8:
             prep["k8"], prep["means"], prep["kscale"] = pasa.kprep_fp8(kt, mode=mode)
 
     def attention():
-        if fp8:
+        if fused:
+            pasa.attn_fwd_fused(qt, kt, vt, causal=w.causal, mode=mode, out=o, lse=lse)
+        elif fp8:
             pasa.attn_fwd_fp8(qt, prep["k8"], prep["means"], prep["kscale"], vt, causal=w.causal, mode=mode,
                               out=o, lse=lse)
         else:
@@ -300,7 +311,7 @@ def bench_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int, also
     total_ms = t_start.elapsed_time(t_end)
     total_ms = max_over_ranks(total_ms, world)
     attn_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(n)]
-    kshift_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(n)] if (shift or fp8) else [0.0] * n
+    kshift_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(n)] if ((shift or fp8) and not fused) else [0.0] * n
     flops = w.flops()
     finite = bool(torch.isfinite(o).all().item())
     res = {
@@ -515,6 +526,8 @@ def main():
     ap.add_argument("--no-also", action="store_true")
     ap.add_argument("--host-chunks", type=int, default=0,
                     help="pieces of the host-buffer (e2e) call; 0 = the library's automatic count")
+    ap.add_argument("--fused", action="store_true",
+                    help="time pasa_attn_fwd_fused (the shift inside the attention kernel) instead of the pre-pass path")
     ap.add_argument("--decode", action="store_true",
                     help="time only the decode step (refresh the cache's last block + attend) on the decode workload")
     args = ap.parse_args()
@@ -528,6 +541,7 @@ def main():
     config = {
         "workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk, "D": w.D,
         "causal": w.causal, "inputs": w.kind, "mode": MODE_NAMES[args.mode],
+        "path": "fused shift (pasa_attn_fwd_fused)" if args.fused else "shift pre-pass + attention",
         "l2": "inputs larger than L2 (129 MB); no flush between steps",
         "flop_convention": "4*B*Hq*visible_pairs*D",
     }
@@ -575,12 +589,14 @@ def main():
     res = bench_gpu(args, w, rank, world, local_rank)
     also = {}
     if not args.no_also and world == 1:
-        for name, amode in ALSO_RUNS:
+        for name, amode, afused in ALSO_RUNS:
             amode = args.mode if amode is None else amode
-            if name == w.name and amode == args.mode:
+            if name == w.name and amode == args.mode and afused == args.fused:
                 continue
             wa = wl.WORKLOADS[name]
-            ra = bench_gpu(args, wa, rank, world, local_rank, also=True, mode=amode)
+            if afused and (wa.D != 128 or amode not in SHIFT_MODES):
+                continue
+            ra = bench_gpu(args, wa, rank, world, local_rank, also=True, mode=amode, fused=afused)
             aq, ak, av = ra["host"]
             rows = wl.sample_rows(wa, 128)
             import oracle
@@ -588,8 +604,10 @@ def main():
             o_ref, _ = oracle.attention(aq, ak, av, causal=wa.causal, rows=rows)
             apeak, _ = peak_for(amode)
             attn_tf = ra["flops"] / (ra["attn_ms"] * 1e-3) / 1e12
-            also[f"{name}/{MODE_NAMES[amode]}"] = {
-                "workload": name, "mode": MODE_NAMES[amode], "tflops": round(ra["tflops"], 1),
+            also[f"{name}/{MODE_NAMES[amode]}" + ("/fused" if afused else "")] = {
+                "workload": name, "mode": MODE_NAMES[amode],
+                "path": "fused shift (pasa_attn_fwd_fused, one launch)" if afused else "shift pre-pass + attention",
+                "tflops": round(ra["tflops"], 1),
                 "ms_per_step": round(ra["ms_per_step"], 4), "attn_ms": round(ra["attn_ms"], 4),
                 "attn_tflops": round(attn_tf, 1), "attn_frac": round(attn_tf / apeak, 4),
                 "kshift_ms": round(ra["kshift_ms"], 4), "finite": ra["finite"],
@@ -609,7 +627,7 @@ def main():
         "peak_source": peak_note,
     }
     kshift_kernel = None
-    if args.mode in SHIFT_MODES or args.mode in FP8_MODES:
+    if (args.mode in SHIFT_MODES or args.mode in FP8_MODES) and not args.fused:
         import precision_flashattention_numerics_gb300 as pasa
 
         nbk = math.ceil(w.Sk / pasa.block_rows(w.D))
@@ -654,7 +672,8 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3+f16" if args.mode in FP8_MODES else "f16",
             "data": "synthetic", "config": config,
             "roofline": roofline, "kshift": kshift_kernel, "cpu_baseline": cpu, "e2e": res["e2e"],
-            "gpu_launches": args.steps * (2 if (args.mode in SHIFT_MODES or args.mode in FP8_MODES) else 1), "clocks": res["clocks"],
+            "gpu_launches": args.steps * (2 if ((args.mode in SHIFT_MODES or args.mode in FP8_MODES) and not args.fused)
+                                          else 1), "clocks": res["clocks"],
             "finite_output": res["finite"], "rmse": rmse, "also": also,
         }
         print(json.dumps(out))

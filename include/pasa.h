@@ -93,6 +93,29 @@ int pasa_attn_fwd(const void* q, const void* k, const void* v, void* o, float* l
                   int Sq, int Sk, int D, int causal, float scale, int mode, void* stream);
 
 /*
+ * PASA attention forward with the pseudo-average shift fused into the attention kernel
+ * (Abstract of the PASA paper: "online pseudo-average shifting"): one launch, raw keys in,
+ * no workspace. Each CTA reduces every raw key tile in shared memory as it lands (per
+ * channel: the maximum |K|, its fp16 spacing g, the exact sum of rint_even(K / g)), shifts
+ * the tile in place to K' = fp16_rn(K - m) with m = g * rint_even(sum / n), and computes
+ * the fp32 offsets q_i . m_j itself; the rest is the pasa_attn_fwd kernel. K' and m are
+ * those of pasa_kshift bit for bit. The offsets are summed in another order than the
+ * pre-pass path's (on the CUDA cores instead of the tensor core), so o and lse agree with
+ * pasa_attn_fwd to fp32 rounding, not bit for bit.
+ *   - Arguments as in pasa_attn_fwd; D must be 128 and mode 0, 1 or 4, else
+ *     PASA_ERR_UNSUPPORTED.
+ *   - k_shifted_out [B, Hkv, Sk, D] and means_out [B, Hkv, ceil(Sk / 128), D], fp16 device
+ *     buffers, may be NULL; when given, the kernel also writes the K' and m it computed
+ *     there (every CTA of a kv head writes the same values), for checking.
+ *   - Every CTA of a kv head repeats the shift of each key block it reads (ceil(Sq / 128)
+ *     query tiles times Hq / Hkv heads), where pasa_attn_fwd shifts each block once in a
+ *     separate kernel: this entry point trades that work for a launch and a workspace.
+ */
+int pasa_attn_fwd_fused(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                        int Sq, int Sk, int D, int causal, float scale, int mode, void* k_shifted_out,
+                        void* means_out, void* stream);
+
+/*
  * pasa_attn_fwd for callers that cannot allocate device memory. (The paper has no
  * counterpart: this is a library convenience.) Some callers may not call cudaMalloc at
  * all, for instance a process whose GPU memory is reserved up front by a framework or

@@ -18,7 +18,7 @@ import torch
 
 __all__ = [
     "MODE_SHIFT_F16ACC", "MODE_SHIFT_F32ACC", "MODE_NAIVE_F16ACC", "MODE_NOSHIFT_F32ACC", "MODE_SHIFT_F16ALL", "MODE_SHIFT_FP8", "MODE_NAIVE_FP8", "kprep_fp8", "attn_fwd_fp8",
-    "PasaError", "attn_fwd", "attn_fwd_alloc", "attn_fwd_shifted", "attn_fwd_stats", "kshift", "workspace_bytes", "check_device_error", "block_rows",
+    "PasaError", "attn_fwd", "attn_fwd_alloc", "attn_fwd_fused", "attn_fwd_shifted", "attn_fwd_stats", "kshift", "workspace_bytes", "check_device_error", "block_rows",
     "library", "library_path",
 ]
 
@@ -43,6 +43,7 @@ SIGNATURES = {
     "pasa_block_rows": ([_I], _I),
     "pasa_attn_fwd": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P], _I),
     "pasa_attn_fwd_noalloc": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P], _I),
+    "pasa_attn_fwd_fused": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P], _I),
     "pasa_attn_fwd_workspace_bytes": ([_I, _I, _I, _I, _I], _SZ),
     "pasa_attn_fwd_ws": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P], _I),
     "pasa_attn_fwd_stats": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P], _I),
@@ -149,6 +150,35 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, mode: in
     if rc != 0:
         raise PasaError(rc, "pasa_attn_fwd_ws")
     return out, lse
+
+
+def attn_fwd_fused(q, k, v, causal: bool = False, scale: float | None = None, mode: int = MODE_SHIFT_F16ACC,
+                   out=None, lse=None, return_shift: bool = False):
+    """Like attn_fwd, through pasa_attn_fwd_fused: the pseudo-average shift runs inside the
+    attention kernel (one launch, no workspace; D = 128, modes 0, 1 and 4). With
+    return_shift=True it also returns the shifted keys and block means the kernel computed:
+    (o, lse, k_shifted, means)."""
+    lib = library()
+    _check(q, "q"), _check(k, "k"), _check(v, "v")
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
+        raise ValueError("expected q [B,Hq,Sq,D] and k, v [B,Hkv,Sk,D]")
+    B, Hq, Sq, D = q.shape
+    _, Hkv, Sk, _ = k.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Sq), device=q.device, dtype=torch.float32)
+    ks = means = None
+    if return_shift:
+        bn = block_rows(D)
+        ks = torch.empty_like(k)
+        means = torch.empty((B, Hkv, (Sk + bn - 1) // bn, D), device=k.device, dtype=torch.float16)
+    rc = lib.pasa_attn_fwd_fused(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Sk, D,
+                                 int(bool(causal)), float(scale) if scale is not None else 0.0, int(mode),
+                                 _ptr(ks), _ptr(means), _stream())
+    if rc != 0:
+        raise PasaError(rc, "pasa_attn_fwd_fused")
+    return (out, lse, ks, means) if return_shift else (out, lse)
 
 
 def attn_fwd_alloc(q, k, v, causal: bool = False, scale: float | None = None, mode: int = MODE_SHIFT_F16ACC,

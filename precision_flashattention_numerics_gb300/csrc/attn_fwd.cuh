@@ -60,6 +60,8 @@ namespace pasa {
 constexpr int kTileRows = 128;       // query rows per CTA (MMA M)
 constexpr int kChunkBlocks = 16;     // key blocks per offsets MMA (its N)
 constexpr int kAttnThreads = 224;
+constexpr int kAttnThreadsFused = 352;   // + four shift warps (7-10) in the FUSED kernels
+constexpr int kShiftBar = 3;             // named barrier of the shift warps
 constexpr float kRescaleLog2 = 8.0f;
 
 // The softmax's exponentials of a block: pair c (two scores) runs on the FMA pipe
@@ -82,7 +84,6 @@ __device__ __forceinline__ void exp2_split(float& p0, float& p1, float x0, float
   }
 }
 
-
 struct AttnParams {
   float* lse;            // [B, Hq, Sq] fp32 or nullptr
   int B, Hq, Hkv, Sq, Sk;
@@ -103,6 +104,10 @@ struct AttnParams {
   int bps;
   float* part_o;
   float* part_lse;
+  // FUSED kernels, optional (nullptr: not written): the shifted keys [B, Hkv, Sk, D] and the
+  // block means [B, Hkv, nbt, D] the kernel computed, for checking them against the pre-pass
+  __half* kshift_out;
+  __half* means_out;
 };
 
 // TMEM column map (see the header comment).
@@ -118,7 +123,7 @@ struct TmemMap {
   static_assert(D == 64 || D == 128, "head dim");
 };
 
-template <int D, int BN, int KST, int VST, bool FP8 = false>
+template <int D, int BN, int KST, int VST, bool FP8 = false, bool FUSED = false>
 struct AttnSmem {
   static constexpr int kChunks = D / 64;                 // 128-byte swizzle atoms along D (fp16)
   static constexpr int kKB = FP8 ? 1 : 2;                // bytes per key element
@@ -135,7 +140,15 @@ struct AttnSmem {
   alignas(1024) uint8_t q8[FP8 ? kTileRows * D : 16];  // FP8: e4m3 codes of Q (one 128-byte atom per row)
   alignas(1024) uint8_t k[KST][kKTile];
   alignas(1024) uint8_t v[VST][kVTile];
-  alignas(1024) uint8_t m[2][kMTile];
+  alignas(1024) uint8_t m[FUSED ? 1 : 2][FUSED ? 16 : kMTile];
+  // FUSED: offsets ring (one c per query row and K slot), the block's means in fp32, and the
+  // shift warps' exchange of per-channel maxima and integer sums (4 warps x 16 units)
+  float cs[FUSED ? KST : 1][FUSED ? kTileRows : 1];
+  float mf[FUSED ? D : 1];
+  uint32_t red_max[FUSED ? 4 : 1][FUSED ? D / 8 : 1][4];
+  uint32_t red_sum[FUSED ? 4 : 1][FUSED ? D / 8 : 1][8];
+  uint64_t sh_full[FUSED ? KST : 1];   // K'_j shifted in place and c_j written (4 shift warps)
+  uint64_t c_free[FUSED ? KST : 1];    // the softmax has read c_j (4 warps)
   uint64_t q_full;
   uint64_t q8_full;     // FP8: the softmax warps have written the e4m3 Q tile (4 warps)
   uint64_t k_full[KST], k_empty[KST];
@@ -153,6 +166,29 @@ struct AttnSmem {
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Named barrier that also ANDs a predicate over the nthreads participants: every thread
+// leaves with the same answer, so a group can decide together to stop.
+__device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
+// Two fp16 values minus two fp16 values, each difference rounded once to fp16 (round to
+// nearest even, subnormals kept).
+__device__ __forceinline__ uint32_t hsub2_rn(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 
 __device__ __forceinline__ float half_lo_to_float(uint32_t w) {
@@ -200,14 +236,15 @@ __device__ __forceinline__ void tmem_ld_scores_f16(uint32_t taddr, uint32_t* hp)
 }
 
 template <int D, int BN, bool F16ACC, bool SHIFT, bool CAUSAL, int KST, int VST, bool STATS = false,
-          bool F16PV = false, bool FP8 = false>
-__global__ void __launch_bounds__(kAttnThreads, 1)
+          bool F16PV = false, bool FP8 = false, bool FUSED = false>
+__global__ void __launch_bounds__(FUSED ? kAttnThreadsFused : kAttnThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                 const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapO,
                 const __grid_constant__ CUtensorMap mapM, const AttnParams p) {
   static_assert(!F16PV || F16ACC, "fp16 PV accumulation is a variant of the fp16-score mode");
   static_assert(!FP8 || (D == 128 && !F16ACC && !STATS && !F16PV), "FP8 scores: D = 128, fp32 accumulation");
-  using Smem = AttnSmem<D, BN, KST, VST, FP8>;
+  static_assert(!FUSED || (D == 128 && SHIFT && !FP8 && !STATS), "the fused shift: D = 128, shifted fp16 keys");
+  using Smem = AttnSmem<D, BN, KST, VST, FP8, FUSED>;
   static_assert(sizeof(Smem) + 1024 <= 227 * 1024, "shared memory per CTA");
   using TM = TmemMap<D, BN>;
   extern __shared__ uint8_t smem_raw[];
@@ -257,6 +294,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     mbar_init(&s.o_full, 1);
     mbar_init(&s.drain[0], 1);
     mbar_init(&s.drain[1], 1);
+    if constexpr (FUSED) {
+      for (int i = 0; i < KST; ++i) {
+        mbar_init(&s.sh_full[i], 4);
+        mbar_init(&s.c_free[i], 4);
+      }
+    }
     s.abort_flag = 0;
     fence_mbar_init();
   }
@@ -276,7 +319,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
       tma_prefetch_desc(&mapQ);
       tma_prefetch_desc(&mapK);
       tma_prefetch_desc(&mapV);
-      if (SHIFT) tma_prefetch_desc(&mapM);
+      if (SHIFT && !FUSED) tma_prefetch_desc(&mapM);
       const int qz = b * p.Hq + hq;
       const int kz = b * p.Hkv + hk;
       mbar_arrive_expect_tx(&s.q_full, Smem::kQTile);
@@ -287,7 +330,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
       // Issue order K_0, K_1, V_0, K_2, V_1, ...: each K runs one block ahead of V, matching
       // the MMA thread, whose loop step j takes K_j and V_(j-1).
       auto load_k = [&](int j) -> bool {
-        if (SHIFT && (j % kChunkBlocks) == 0) {
+        if (SHIFT && !FUSED && (j % kChunkBlocks) == 0) {
           const int ci = j / kChunkBlocks, slot = ci & 1;
           if (!mbar_wait(&s.m_empty[slot], ((ci >> 1) & 1) ^ 1, abort_flag, 0x101)) return false;
           mbar_arrive_expect_tx(&s.m_full[slot], Smem::kMTile);
@@ -361,13 +404,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         const int ks = j % KST;
         const int ci = j / kChunkBlocks;
         const int sb = j & 1;
-        const bool chunk_start = SHIFT && (j % kChunkBlocks) == 0;
+        const bool chunk_start = SHIFT && !FUSED && (j % kChunkBlocks) == 0;
         uint32_t kd[D / 16];
         const uint32_t k_lo = k_lo0 + ks * kKStride;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) kd[kk] = k_lo + (((kk / 4) * Smem::kKChunk + (kk % 4) * 32) >> 4);
         // (FP8: the first D / 32 of these are the e4m3 K-steps of the single 128-byte atom)
-        if (!mbar_wait(&s.k_full[ks], (j / KST) & 1, abort_flag, 0x202)) break;
+        // FUSED: the shift warps have shifted the raw tile in place (K'_j), else TMA brought K'_j
+        if (!mbar_wait(FUSED ? &s.sh_full[ks] : &s.k_full[ks], (j / KST) & 1, abort_flag, 0x202)) break;
         if (chunk_start && !mbar_wait(&s.m_full[ci & 1], (ci >> 1) & 1, abort_flag, 0x203)) break;
         if (j >= 2 && !mbar_wait(&s.s_free[sb], ((j >> 1) - 1) & 1, abort_flag, 0x206)) break;
         tc_fence_after();
@@ -429,6 +473,162 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
       mma_commit(&s.drain[1]);
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(&s.drain[1], 0) && globaltimer_ns() - t0 < kWaitTimeoutNs) {
+      }
+    }
+    __syncwarp();
+  } else if (FUSED && warp >= 7) {
+    // ------------------------------------------------------------------ shift warps (FUSED)
+    // The pseudo-average shift of each raw K tile, in place in shared memory as it lands,
+    // then the tile's offsets for the 128 query rows. The same reading of the pseudo-average
+    // as kshift_kernel (exact integer sums on the grid of the block maximum, one rounding of
+    // K - m), so K' and m are the pre-pass's bit for bit. Thread st owns channels
+    // 8u .. 8u + 7 (one 16-byte unit) of the tile rows rg, rg + 8, ..., rg + 120; in the
+    // 128-byte swizzle those rows hold the unit at the same position (row mod 8 = rg).
+    if constexpr (FUSED) {
+      const int st = tid - 7 * 32;      // 0..127
+      const int sw = st >> 5;           // shift warp 0..3
+      const int u = st & 15;
+      const int rg = st >> 4;           // 0..7
+      static_assert(D / 8 == 16, "16 units per key row");
+      const uint32_t uoff = (u >> 3) * Smem::kKChunk + ((((u & 7) ^ rg)) << 4);
+      constexpr float kRound = 12582912.0f;      // 1.5 * 2^23
+      constexpr uint32_t kRoundBits = 0x4B400000u;
+      const int kz = b * p.Hkv + hk;
+      bool ok = named_bar_and(kShiftBar, 128, mbar_wait(&s.q_full, 0, abort_flag, 0x360));
+      for (int j = 0; ok && j < nblk; ++j) {
+        const int ks = j % KST;
+        // every decision to stop is taken by all 128 threads together (no one is left at a
+        // named barrier)
+        if (!named_bar_and(kShiftBar, 128, mbar_wait(&s.k_full[ks], (j / KST) & 1, abort_flag, 0x361))) {
+          ok = false;
+          break;
+        }
+        uint8_t* tile = s.k[ks];
+        uint4 x[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = *reinterpret_cast<const uint4*>(tile + (rg + 8 * i) * 128 + uoff);
+        // 1. per-channel max |K| (16-bit lanes); an inf or NaN makes it >= 0x7C00
+        uint32_t mx[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          mx[0] = __vmaxu2(mx[0], x[i].x & 0x7FFF7FFFu);
+          mx[1] = __vmaxu2(mx[1], x[i].y & 0x7FFF7FFFu);
+          mx[2] = __vmaxu2(mx[2], x[i].z & 0x7FFF7FFFu);
+          mx[3] = __vmaxu2(mx[3], x[i].w & 0x7FFF7FFFu);
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) mx[c] = __vmaxu2(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 16));
+        if (lane < 16) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) s.red_max[sw][u][c] = mx[c];
+        }
+        named_bar_sync(kShiftBar, 128);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          mx[c] = __vmaxu2(__vmaxu2(s.red_max[0][u][c], s.red_max[1][u][c]),
+                           __vmaxu2(s.red_max[2][u][c], s.red_max[3][u][c]));
+        // 2. grid step g = fp16 spacing at the maximum; guard: m = 0 from 2^15 up (and inf/NaN)
+        float g[8], inv_g[8];
+        bool guard[8];
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
+          const uint32_t a = (mx[h >> 1] >> (16 * (h & 1))) & 0xFFFFu;
+          const int E = static_cast<int>(a >> 10);
+          const int e = E >= 1 ? E - 25 : -24;
+          g[h] = __int_as_float((e + 127) << 23);
+          inv_g[h] = __int_as_float((127 - e) << 23);
+          guard[h] = E >= 30;
+        }
+        // 3. sums of rint_even(K / g): K / g is exact and below 2^11 where not guarded, so
+        //    fp32(K / g + 1.5 * 2^23) holds the rounded integer in its low bits
+        uint32_t sm[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const __half2* hv = reinterpret_cast<const __half2*>(&x[i]);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const float2 f = __half22float2(hv[c]);
+            sm[2 * c] += __float_as_uint(__fmaf_rn(f.x, inv_g[2 * c], kRound)) - kRoundBits;
+            sm[2 * c + 1] += __float_as_uint(__fmaf_rn(f.y, inv_g[2 * c + 1], kRound)) - kRoundBits;
+          }
+        }
+#pragma unroll
+        for (int h = 0; h < 8; ++h) sm[h] += __shfl_xor_sync(0xffffffffu, sm[h], 16);
+        if (lane < 16) {
+#pragma unroll
+          for (int h = 0; h < 8; ++h) s.red_sum[sw][u][h] = sm[h];
+        }
+        named_bar_sync(kShiftBar, 128);
+        // 4. m = g * rint_even(sum / n) over the n valid rows of the block (0 where guarded)
+        const int n = min(BN, p.Sk - (jb0 + j) * BN);
+        float mv[8];
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
+          const int su = static_cast<int>(s.red_sum[0][u][h] + s.red_sum[1][u][h] + s.red_sum[2][u][h] +
+                                          s.red_sum[3][u][h]);
+          int mu;
+          if (n == BN) {
+            // rint_even(su / 128): floor plus the half-even decision on the remainder
+            const int fl = su >> 7, rm = su & 127;
+            mu = fl + ((rm > 64 || (rm == 64 && (fl & 1))) ? 1 : 0);
+          } else {
+            mu = rne_div(su, n);
+          }
+          mv[h] = guard[h] ? 0.0f : static_cast<float>(mu) * g[h];  // exact
+        }
+        uint32_t m2[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) m2[c] = pack_half2(mv[2 * c], mv[2 * c + 1]);   // exact
+        // 5. K' = fp16_rn(K - m) in place
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          x[i] = make_uint4(hsub2_rn(x[i].x, m2[0]), hsub2_rn(x[i].y, m2[1]), hsub2_rn(x[i].z, m2[2]),
+                            hsub2_rn(x[i].w, m2[3]));
+          *reinterpret_cast<uint4*>(tile + (rg + 8 * i) * 128 + uoff) = x[i];
+        }
+        if (rg == 0) {
+#pragma unroll
+          for (int h = 0; h < 8; ++h) s.mf[8 * u + h] = mv[h];
+        }
+        if (p.kshift_out != nullptr) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int row = rg + 8 * i;
+            if (row < n)
+              *reinterpret_cast<uint4*>(p.kshift_out + (static_cast<size_t>(kz) * p.Sk + (jb0 + j) * BN + row) * D +
+                                        8 * u) = x[i];
+          }
+        }
+        if (p.means_out != nullptr && rg == 0)
+          *reinterpret_cast<uint4*>(p.means_out + (static_cast<size_t>(kz) * p.nbt + jb0 + j) * D + 8 * u) =
+              make_uint4(m2[0], m2[1], m2[2], m2[3]);
+        fence_proxy_async_smem();   // the MMA reads K' through the async proxy
+        // 6. the offsets c = q_st . m_j of query row st (fp32; the products are exact), once
+        //    the softmax has read the last offsets of this ring slot; the barrier also makes
+        //    every thread's means visible
+        const bool cf = j < KST || mbar_wait(&s.c_free[ks], ((j / KST) & 1) ^ 1, abort_flag, 0x362);
+        if (!named_bar_and(kShiftBar, 128, cf)) {
+          ok = false;
+          break;
+        }
+        float ca[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // four independent pair chains
+#pragma unroll
+        for (int v = 0; v < 16; ++v) {
+          const uint4 qv = *reinterpret_cast<const uint4*>(s.q + (v >> 3) * Smem::kQChunk + st * 128 +
+                                                           ((((v & 7) ^ (st & 7))) << 4));
+          const float4 ma = *reinterpret_cast<const float4*>(s.mf + 8 * v);
+          const float4 mb = *reinterpret_cast<const float4*>(s.mf + 8 * v + 4);
+          const __half2* qh = reinterpret_cast<const __half2*>(&qv);
+          const float2 q0f = __half22float2(qh[0]), q1f = __half22float2(qh[1]);
+          const float2 q2f = __half22float2(qh[2]), q3f = __half22float2(qh[3]);
+          ffma2(ca[0], ca[1], q0f.x, q0f.y, ma.x, ma.y, ca[0], ca[1]);
+          ffma2(ca[2], ca[3], q1f.x, q1f.y, ma.z, ma.w, ca[2], ca[3]);
+          ffma2(ca[4], ca[5], q2f.x, q2f.y, mb.x, mb.y, ca[4], ca[5]);
+          ffma2(ca[6], ca[7], q3f.x, q3f.y, mb.z, mb.w, ca[6], ca[7]);
+        }
+        s.cs[ks][st] = ((ca[0] + ca[1]) + (ca[2] + ca[3])) + ((ca[4] + ca[5]) + (ca[6] + ca[7]));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.sh_full[ks]);
       }
     }
     __syncwarp();
@@ -497,6 +697,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         if (j + 1 < nblk) sk_next = __ldg(kscale_row + jb0 + j + 1);
       }
       if (!mbar_wait(&s.s_full[sb], (j >> 1) & 1, abort_flag, 0x300)) { ok = false; break; }
+      // FUSED: the offset of block j comes from the shift warps through shared memory; their
+      // arrival on sh_full (complete before QK(j) could start) orders the write
+      if (FUSED && !mbar_wait(&s.sh_full[j % KST], (j / KST) & 1, abort_flag, 0x301)) { ok = false; break; }
       tc_fence_after();
       // Load the block's scores and offset, wait once, fence the registers, and release the
       // score buffer to the MMA thread before any arithmetic. fp16 scores (F16ACC) are
@@ -512,14 +715,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
 #pragma unroll
         for (int c = 0; c < BN / 16; ++c) tmem_ld_x16(tS + c * 16, reinterpret_cast<uint32_t*>(sv) + c * 16);
       }
-      if (SHIFT) tmem_ld_x1(tmem + lane_base + TM::c((j / kChunkBlocks) & 1) + (j % kChunkBlocks), cw);
+      if (SHIFT && !FUSED) tmem_ld_x1(tmem + lane_base + TM::c((j / kChunkBlocks) & 1) + (j % kChunkBlocks), cw);
+      if constexpr (FUSED) cw = __float_as_uint(s.cs[j % KST][r]);
       tmem_ld_wait();
       if constexpr (F16ACC) reg_fence<kPairs>(hp);
       else reg_fence<BN>(reinterpret_cast<uint32_t*>(sv));
       reg_fence<1>(&cw);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s.s_free[sb]);
+      if (lane == 0) {
+        mbar_arrive(&s.s_free[sb]);
+        if constexpr (FUSED) mbar_arrive(&s.c_free[j % KST]);
+      }
 
       const int cmax = limit - (jb0 + j) * BN;
       const float c_raw = SHIFT ? __uint_as_float(cw) : 0.0f;

@@ -178,6 +178,22 @@ int launch_attn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap&
   return e == cudaSuccess ? PASA_OK : cuda_fail(e);
 }
 
+// The fused-shift kernel (D = 128, modes 0, 1, 4): raw keys in, shift warps in the kernel.
+template <bool F16ACC, bool CAUSAL, bool F16PV>
+int launch_attn_fused(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mo,
+                      const pasa::AttnParams& p, cudaStream_t st) {
+  constexpr int D = 128, BN = 128, KST = 3, VST = 2;
+  using Smem = pasa::AttnSmem<D, BN, KST, VST, false, true>;
+  auto kern = pasa::attn_fwd_kernel<D, BN, F16ACC, true, CAUSAL, KST, VST, false, F16PV, false, true>;
+  const int smem = static_cast<int>(sizeof(Smem)) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const long long ctas = static_cast<long long>(p.n_qblk) * p.Hq * p.B;
+  kern<<<static_cast<unsigned>(ctas), pasa::kAttnThreadsFused, smem, st>>>(mq, mk, mv, mo, mk, p);
+  e = cudaGetLastError();
+  return e == cudaSuccess ? PASA_OK : cuda_fail(e);
+}
+
 template <int D, bool STATS>
 int attn_dispatch(int mode, int causal, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                   const CUtensorMap& mo, const CUtensorMap& mm, const pasa::AttnParams& p, cudaStream_t st) {
@@ -446,6 +462,8 @@ static int attn_launch(const void* q, const void* kk, const void* mm, const void
   p.bps = 0;
   p.part_o = nullptr;
   p.part_lse = nullptr;
+  p.kshift_out = nullptr;
+  p.means_out = nullptr;
   if (block_stats) {
     const cudaError_t e = cudaMemsetAsync(block_stats, 0, static_cast<size_t>(B) * Hq * nb * 2 * sizeof(float), st);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -614,6 +632,8 @@ static int decode_impl(const void* q, const void* k_shifted, const void* means, 
     p.bps = bps;
     p.part_o = part_o;
     p.part_lse = part_lse;
+    p.kshift_out = nullptr;
+    p.means_out = nullptr;
     rc = D == 64 ? attn_dispatch<64, false>(mode, causal, mq, mk, mv, mo, mmeans, p, st)
                  : attn_dispatch<128, false>(mode, causal, mq, mk, mv, mo, mmeans, p, st);
   }
@@ -743,6 +763,52 @@ int pasa_attn_fwd(const void* q, const void* k, const void* v, void* o, float* l
     if (rc == PASA_OK && e != cudaSuccess) rc = cuda_fail(e);
   }
   return rc;
+}
+
+int pasa_attn_fwd_fused(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                        int Sq, int Sk, int D, int causal, float scale, int mode, void* k_shifted_out,
+                        void* means_out, void* stream) {
+  int rc = validate(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, mode);
+  if (rc != PASA_OK) return rc;
+  if (D != 128) return PASA_ERR_UNSUPPORTED;
+  if (mode != PASA_MODE_SHIFT_F16ACC && mode != PASA_MODE_SHIFT_F32ACC && mode != PASA_MODE_SHIFT_F16ALL)
+    return PASA_ERR_UNSUPPORTED;
+  if ((k_shifted_out && !aligned16(k_shifted_out)) || (means_out && !aligned16(means_out))) return PASA_ERR_ALIGN;
+  rc = check_device();
+  if (rc != PASA_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (!(scale > 0.0f) || !std::isfinite(scale)) scale = 1.0f / std::sqrt(static_cast<float>(D));
+  const int bn = pasa::block_rows_for(D);
+  CUtensorMap mq, mk, mv, mo;
+  if ((rc = make_map(&mq, q, D, Sq, static_cast<long long>(B) * Hq, pasa::kTileRows)) != PASA_OK) return rc;
+  if ((rc = make_map(&mk, k, D, Sk, static_cast<long long>(B) * Hkv, bn)) != PASA_OK) return rc;
+  if ((rc = make_map(&mv, v, D, Sk, static_cast<long long>(B) * Hkv, bn)) != PASA_OK) return rc;
+  if ((rc = make_map(&mo, o, D, Sq, static_cast<long long>(B) * Hq, pasa::kTileRows)) != PASA_OK) return rc;
+  pasa::AttnParams p = {};
+  p.lse = lse;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Sq = Sq;
+  p.Sk = Sk;
+  p.n_qblk = (Sq + pasa::kTileRows - 1) / pasa::kTileRows;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.inv_scale_log2 = 1.0f / p.scale_log2;
+  p.nbt = (Sk + bn - 1) / bn;
+  p.sq_mod = Sq;
+  p.kshift_out = static_cast<__half*>(k_shifted_out);
+  p.means_out = static_cast<__half*>(means_out);
+  switch (mode) {
+    case PASA_MODE_SHIFT_F16ACC:
+      return causal ? launch_attn_fused<true, true, false>(mq, mk, mv, mo, p, st)
+                    : launch_attn_fused<true, false, false>(mq, mk, mv, mo, p, st);
+    case PASA_MODE_SHIFT_F32ACC:
+      return causal ? launch_attn_fused<false, true, false>(mq, mk, mv, mo, p, st)
+                    : launch_attn_fused<false, false, false>(mq, mk, mv, mo, p, st);
+    default:
+      return causal ? launch_attn_fused<true, true, true>(mq, mk, mv, mo, p, st)
+                    : launch_attn_fused<true, false, true>(mq, mk, mv, mo, p, st);
+  }
 }
 
 int pasa_selftest_wait_timeout(void* stream) {
