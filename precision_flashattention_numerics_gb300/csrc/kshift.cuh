@@ -330,4 +330,144 @@ kshift_kernel(const __half* __restrict__ k, void* __restrict__ kshift, __half* _
   }
 }
 
+// The fp16 grid-mean shift (kShiftF16, the prefill path) held in registers instead of
+// shared memory: thread (u, rg) owns the 16-byte unit u (channels 8u .. 8u + 7) of the block
+// rows rg, rg + RG, rg + 2 RG, ...; it loads them straight from global memory (a warp reads
+// whole rows, so the loads are coalesced), reduces the per-channel maximum and integer sums
+// with one shuffle level and an exchange across the CTA's warps, and writes K' from the same
+// registers. No staging pass over shared memory, so nothing but HBM bounds it. The reading
+// is kshift_kernel's; K' is one rounding of K - m (sub.rn.f16x2), which is what that
+// kernel's fp32 subtraction and fp16 rounding give (checked bit for bit in the tests).
+constexpr int kShiftRegThreads = 128;
+
+template <int D, int BN>
+__global__ void __launch_bounds__(kShiftRegThreads)
+kshift_reg_kernel(const __half* __restrict__ k, __half* __restrict__ kshift, __half* __restrict__ means, int Sk,
+                  int nb, int j0, int cap, int nb_cap) {
+  constexpr int U = D / 8;                       // 16-byte units per row
+  constexpr int RG = kShiftRegThreads / U;       // row groups
+  constexpr int RPT = BN / RG;                   // rows per thread
+  constexpr int NW = kShiftRegThreads / 32;
+  constexpr int LPR = 32 / U;                    // row groups per warp
+  static_assert(BN % RG == 0 && 32 % U == 0, "layout");
+  __shared__ uint32_t sh_max[NW][U][4];
+  __shared__ uint32_t sh_sum[NW][U][8];
+
+  const int j = j0 + blockIdx.x;
+  const int bh = blockIdx.y;
+  const int tid = threadIdx.x;
+  const int u = tid % U;
+  const int rg = tid / U;
+  const int warp = tid / 32;
+  const int row0 = j * BN;
+  const int n = min(BN, Sk - row0);
+  const uint4* src = reinterpret_cast<const uint4*>(k + (static_cast<size_t>(bh) * cap + row0) * D) + u;
+  uint4* dst = reinterpret_cast<uint4*>(kshift + (static_cast<size_t>(bh) * cap + row0) * D) + u;
+
+  uint4 x[RPT];
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    const int r = rg + i * RG;
+    x[i] = r < n ? __ldg(src + static_cast<size_t>(r) * U) : make_uint4(0, 0, 0, 0);
+  }
+  // 1. per-channel max |K| (16-bit lanes); an inf or NaN makes it >= 0x7C00
+  uint32_t mx[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    mx[0] = __vmaxu2(mx[0], x[i].x & 0x7FFF7FFFu);
+    mx[1] = __vmaxu2(mx[1], x[i].y & 0x7FFF7FFFu);
+    mx[2] = __vmaxu2(mx[2], x[i].z & 0x7FFF7FFFu);
+    mx[3] = __vmaxu2(mx[3], x[i].w & 0x7FFF7FFFu);
+  }
+#pragma unroll
+  for (int off = U; off < 32; off *= 2)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) mx[c] = __vmaxu2(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], off));
+  if ((tid % 32) < U) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) sh_max[warp][u][c] = mx[c];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t m = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) m = __vmaxu2(m, sh_max[w][u][c]);
+    mx[c] = m;
+  }
+  // 2. grid step per channel; guard (m = 0) from 2^15 up and for inf/NaN
+  float g[8], inv_g[8];
+  bool guard[8];
+#pragma unroll
+  for (int h = 0; h < 8; ++h) {
+    const uint32_t a = (mx[h / 2] >> (16 * (h & 1))) & 0xFFFFu;
+    const int E = static_cast<int>(a >> 10);
+    const int e = E >= 1 ? E - 25 : -24;
+    g[h] = __int_as_float((e + 127) << 23);
+    inv_g[h] = __int_as_float((127 - e) << 23);
+    guard[h] = E >= 30;
+  }
+  // 3. exact integer sums of rint_even(K / g) (rows >= n are zeros); see kshift_kernel
+  constexpr float kRound = 12582912.0f;      // 1.5 * 2^23
+  constexpr uint32_t kRoundBits = 0x4B400000u;
+  uint32_t sum[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    const __half2* hv = reinterpret_cast<const __half2*>(&x[i]);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const float2 f = __half22float2(hv[c]);
+      sum[2 * c] += __float_as_uint(__fmaf_rn(f.x, inv_g[2 * c], kRound)) - kRoundBits;
+      sum[2 * c + 1] += __float_as_uint(__fmaf_rn(f.y, inv_g[2 * c + 1], kRound)) - kRoundBits;
+    }
+  }
+#pragma unroll
+  for (int off = U; off < 32; off *= 2)
+#pragma unroll
+    for (int h = 0; h < 8; ++h) sum[h] += __shfl_xor_sync(0xffffffffu, sum[h], off);
+  if ((tid % 32) < U) {
+#pragma unroll
+    for (int h = 0; h < 8; ++h) sh_sum[warp][u][h] = sum[h];
+  }
+  __syncthreads();
+  // 4. m = g * rint_even(sum / n), then K' = fp16_rn(K - m) from the registers
+  uint32_t m2[4];
+  float mf[8];
+#pragma unroll
+  for (int h = 0; h < 8; ++h) {
+    uint32_t su = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) su += sh_sum[w][u][h];
+    const int si = static_cast<int>(su);
+    int mu;
+    if (n == BN && (BN & (BN - 1)) == 0) {
+      constexpr int kShift = BN == 128 ? 7 : (BN == 64 ? 6 : 0);
+      const int fl = si >> kShift, rm = si & (BN - 1);
+      mu = fl + ((2 * rm > BN || (2 * rm == BN && (fl & 1))) ? 1 : 0);
+    } else {
+      mu = rne_div(si, n);
+    }
+    mf[h] = guard[h] ? 0.0f : static_cast<float>(mu) * g[h];   // exact, an fp16 value
+  }
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const __half2 h2 = __floats2half2_rn(mf[2 * c], mf[2 * c + 1]);
+    m2[c] = *reinterpret_cast<const uint32_t*>(&h2);
+  }
+  if (rg == 0) reinterpret_cast<uint4*>(means + (static_cast<size_t>(bh) * nb_cap + j) * D)[u] =
+      make_uint4(m2[0], m2[1], m2[2], m2[3]);
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    const int r = rg + i * RG;
+    if (r < n) {
+      uint4 o;
+      asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(o.x) : "r"(x[i].x), "r"(m2[0]));
+      asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(o.y) : "r"(x[i].y), "r"(m2[1]));
+      asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(o.z) : "r"(x[i].z), "r"(m2[2]));
+      asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(o.w) : "r"(x[i].w), "r"(m2[3]));
+      dst[static_cast<size_t>(r) * U] = o;
+    }
+  }
+}
+
 }  // namespace pasa

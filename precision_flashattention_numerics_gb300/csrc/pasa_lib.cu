@@ -143,6 +143,14 @@ int launch_kshift(const void* k, void* ks, void* means, float* kscale, int B, in
   const int nb = (Sk + BN - 1) / BN;
   if (cap <= 0) cap = Sk;
   dim3 grid(nb - first_block, B * H);
+  if constexpr (OUT == pasa::kShiftF16 && !PLAIN) {
+    // the fp16 grid-mean shift: the register-resident kernel
+    pasa::kshift_reg_kernel<D, BN><<<grid, pasa::kShiftRegThreads, 0, st>>>(
+        static_cast<const __half*>(k), static_cast<__half*>(ks), static_cast<__half*>(means), Sk, nb, first_block,
+        cap, (cap + BN - 1) / BN);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? PASA_OK : cuda_fail(e);
+  }
   pasa::kshift_kernel<D, BN, OUT, PLAIN><<<grid, pasa::kShiftThreads, 0, st>>>(
       static_cast<const __half*>(k), ks, static_cast<__half*>(means), kscale, Sk, nb, first_block, cap,
       (cap + BN - 1) / BN);
