@@ -367,3 +367,33 @@ def test_host_buffer_plan_properties(lib):
         assert nbytes >= problem and nbytes % 256 == 0
 
     check()
+
+
+def call_fused(lib, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, Hq=2, Hkv=1, Sq=64, Sk=64, D=128,
+               causal=0, mode=0, ks_out=None, m_out=None):
+    P = ctypes.c_void_p
+    return lib.pasa_attn_fwd_fused(P(q), P(k), P(v), P(o), P(lse), B, Hq, Hkv, Sq, Sk, D, causal, 0.0, mode,
+                                   P(ks_out) if ks_out is not None else None,
+                                   P(m_out) if m_out is not None else None, None)
+
+
+def test_fused_argument_errors(lib):
+    # the fused-shift entry point: D = 128 and the shifted modes only, checked before any launch
+    assert call_fused(lib, q=0) == -1
+    assert call_fused(lib, v=0) == -1
+    assert call_fused(lib, B=0) == -2
+    assert call_fused(lib, Hq=3, Hkv=2) == -2
+    assert call_fused(lib, D=64) == -3
+    for mode in (2, 3, 5, 6, 7):
+        assert call_fused(lib, mode=mode) == -3, mode
+    assert call_fused(lib, k=FAKE_MIS) == -4
+    assert call_fused(lib, lse=FAKE_MIS) == -4
+    assert call_fused(lib, ks_out=FAKE_MIS) == -4
+    assert call_fused(lib, m_out=FAKE_MIS) == -4
+
+
+def test_exp2_selftest_argument_errors(lib):
+    P = ctypes.c_void_p
+    assert lib.pasa_selftest_exp2(None, P(FAKE), P(FAKE), 16, None) == -1
+    assert lib.pasa_selftest_exp2(P(FAKE), P(FAKE), None, 16, None) == -1
+    assert lib.pasa_selftest_exp2(P(FAKE), P(FAKE), P(FAKE), 0, None) == -2
