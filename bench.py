@@ -448,6 +448,12 @@ def bench_decode(args, w: wl.Workload, local_rank: int, sampler=None):
     }
 
 
+def _json_num(x):
+    """A float for the JSON line; an overflowed accumulator (inf) is reported as "inf"."""
+    x = float(x)
+    return x if math.isfinite(x) else ("inf" if x > 0 else "nan" if x != x else "-inf")
+
+
 def bench_stats(args, w: wl.Workload, local_rank: int):
     """The overflow diagnostic (pasa_attn_fwd_stats with per-key-block maxima): one step is the
     shift, the zeroing of the block maxima and the diagnostic variant of the attention kernel,
@@ -474,9 +480,18 @@ def bench_stats(args, w: wl.Workload, local_rank: int):
     torch.cuda.synchronize()
     pasa.check_device_error()
     ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    # score magnitudes of the last call, over all query rows: what the score accumulator held
+    # (S' with the shift, S without) and the recovered raw scores |S' + q.m|, against 65504
+    _, _, st, _ = pasa.attn_fwd_stats(qt, kt, vt, causal=w.causal, mode=mode, block_stats=True)
+    pasa.check_device_error()
+    acc, rec = st[..., 0], st[..., 1]
     return {"workload": w.name, "mode": MODE_NAMES[mode], "ms_per_step": round(ms, 4),
             "tflops": round(w.flops() / (ms * 1e-3) / 1e12, 1), "steps": n,
-            "step": "kshift + zeroing of the block maxima + diagnostic attention kernel"}
+            "step": "kshift + zeroing of the block maxima + diagnostic attention kernel",
+            "max_abs_accumulated_score": _json_num(acc.max().item()),
+            "max_abs_raw_score": _json_num(rec.max().item()),
+            "rows_over_fp16_max": int((acc > 65504.0).sum().item()),
+            "fp16_max": 65504.0}
 
 
 def decode_main(args, rank: int, world: int, local_rank: int):
