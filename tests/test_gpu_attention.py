@@ -352,3 +352,62 @@ def test_pasa_attn_fwd_c_abi_against_oracle(case, mode):
     # and the same bytes as the workspace entry point the other tests use
     o_ws, lse_ws = pasa().attn_fwd(qt, kt, vt, causal=causal, mode=mode)
     assert torch.equal(o, o_ws) and torch.equal(lse, lse_ws)
+
+
+# ---------------------------------------------------------------------------------------
+# seeded random sweep: shapes, ragged lengths, GQA ratios, masks, modes and both key paths
+# (pre-pass and fused shift), each against the oracle with the gates used above
+# ---------------------------------------------------------------------------------------
+def _sweep_cases(n=32, seed=2024):
+    rng = np.random.default_rng(seed)
+    out = []
+    for t in range(n):
+        D = int(rng.choice([64, 128]))
+        Hkv = int(rng.integers(1, 4))
+        g = int(rng.choice([1, 2, 4, 7]))
+        Sq = int(rng.integers(1, 700))
+        Sk = int(max(1, Sq + rng.integers(-300, 400)))
+        causal = bool(rng.integers(0, 2))
+        kind = str(rng.choice(["iid", "kbias", "kbias_t3"]))
+        mode = int(rng.choice([0, 1, 2, 3, 4]))
+        fused = D == 128 and mode in (0, 1, 4) and bool(rng.integers(0, 2))
+        out.append((int(rng.integers(1, 3)), Hkv * g, Hkv, Sq, Sk, D, causal, kind, mode, fused, 700 + t))
+    return out
+
+
+SWEEP = _sweep_cases()
+
+
+@pytest.mark.parametrize("case", SWEEP, ids=[f"{c[5]}d-{c[1]}/{c[2]}h-{c[3]}x{c[4]}-{'c' if c[6] else 'n'}-{c[7]}-m{c[8]}"
+                                             f"{'-fused' if c[9] else ''}" for c in SWEEP])
+def test_random_sweep_against_oracle(case):
+    B, Hq, Hkv, Sq, Sk, D, causal, kind, mode, fused, seed = case
+    params = {"iid": {}, "kbias": {"bias_std": 20.0}, "kbias_t3": {"bias_std": 10.0, "t_dof": 3, "t_scale": 4.0}}[kind]
+    q, k, v = small_case(B, Hq, Hkv, Sq, Sk, D, kind, seed, **params)
+    p = pasa()
+    qt, kt, vt = to_dev(q, k, v)
+    if fused:
+        o, lse = p.attn_fwd_fused(qt, kt, vt, causal=causal, mode=mode)
+    else:
+        o, lse = p.attn_fwd(qt, kt, vt, causal=causal, mode=mode)
+    p.check_device_error()
+    o_ref, lse_ref = oracle.attention(q, k, v, causal=causal)
+    og = o.double().cpu().numpy()
+    lg = lse.double().cpu().numpy()
+    assert np.isfinite(og).all()
+    fin = np.isfinite(lse_ref)
+    assert np.all(np.isneginf(lg[~fin])) and np.all(og.reshape(-1, D)[~fin.reshape(-1)] == 0.0)
+    if not fin.any():
+        return
+    rmse, rmax = rel_errors(og.reshape(-1, D)[fin.reshape(-1)], o_ref.reshape(-1, D)[fin.reshape(-1)])
+    if mode == 4:
+        bound = (5e-2 if kind != "iid" else 1e-2) * np.abs(o_ref).max() + f16all_bound(Sk) * float(
+            np.abs(v.astype(np.float64)).max())
+        assert np.abs(og - o_ref).max() <= bound
+    elif mode == 2 and kind != "iid":
+        assert rmse <= 5e-2 and rmax <= 2e-1, (rmse, rmax)
+    elif kind != "iid":
+        assert rmse <= 5e-3 and rmax <= 5e-2, (rmse, rmax)
+    else:
+        assert rmse <= 2e-3 and rmax <= 1e-2, (rmse, rmax)
+    assert np.max(np.abs(lg[fin] - lse_ref[fin])) <= lse_tolerance(q, k, causal, mode, D)
