@@ -19,8 +19,12 @@
 //
 // TMEM (512 columns) holds two score buffers S_0, S_1 (BN columns each), the output
 // accumulator O (D columns), the probabilities P (BN/2 columns, two fp16 per column) and two
-// buffers of offsets C (16 columns each: q_i . m_j for 16 consecutive key blocks), all
-// disjoint. Key block j uses S_(j mod 2), so the score MMA of block j+1 is issued while the
+// buffers of offsets C (16 columns each: q_i . m_j for 16 consecutive key blocks) and, in the
+// columns left, the Q tile (at D = 128 the 32 columns left hold its first 64 channels), all
+// disjoint. The score and offsets
+// MMAs take those K-steps with A in TMEM (a tcgen05 MMA with M = 128, N <= 128 runs at ~67
+// cycles with A in TMEM against ~86 with both operands in shared memory) and the rest with
+// both operands in shared memory. Key block j uses S_(j mod 2), so the score MMA of block j+1 is issued while the
 // softmax still works on block j-1 and S_(j+1) is ready before the softmax reaches it: once
 // running, the softmax never waits for scores and the tensor pipe always has the next
 // block's work queued. The softmax releases an S buffer (s_free) as soon as it has loaded
@@ -117,7 +121,11 @@ struct TmemMap {
   static constexpr int o = 2 * BN;
   static constexpr int p = 2 * BN + D;
   __host__ __device__ static constexpr int c(int b) { return 2 * BN + D + BN / 2 + b * kChunkBlocks; }
-  static constexpr int total = 2 * BN + D + BN / 2 + 2 * kChunkBlocks;
+  // The first kQtSteps K-steps of the Q tile as the A operand (8 columns per K-step of 16):
+  // as many as the 512 columns leave room for.
+  static constexpr int q = 2 * BN + D + BN / 2 + 2 * kChunkBlocks;
+  static constexpr int kQtSteps = (512 - q) / 8 < D / 16 ? (512 - q) / 8 : D / 16;
+  static constexpr int total = q + 8 * kQtSteps;
   static_assert(total <= 512, "TMEM budget");
   static_assert(BN % 32 == 0 && BN <= 256, "key block");
   static_assert(D == 64 || D == 128, "head dim");
@@ -400,6 +408,16 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
       constexpr uint32_t id_s8 = idesc_e4m3(kTileRows, BN);
       const uint32_t q8_lo = sdesc_lo(smem_u32(s.q8), 16);
       bool ok = mbar_wait(FP8 ? &s.q8_full : &s.q_full, 0, abort_flag, 0x201);
+      const uint32_t tQ = tmem + TM::q;
+      constexpr int kQt = FP8 ? 0 : TM::kQtSteps;   // FP8 keeps the fp16 Q (offsets) in shared memory
+      if (kQt > 0 && ok && nblk > 0) {
+        // Q's first K-steps into TMEM once. Only with key blocks: without them the epilogue
+        // rewrites the Q buffer as soon as Q has landed, and no MMA completion would cover
+        // this copy.
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kQt; ++kk) tmem_cp_128x256b(tQ + kk * 8, qd[kk], hi_kmaj);
+      }
       for (int j = 0; ok && j < nblk; ++j) {
         const int ks = j % KST;
         const int ci = j / kChunkBlocks;
@@ -421,7 +439,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off_m = ((kk / 4) * Smem::kMChunk + (kk % 4) * 32) >> 4;
-            mma_ss_w(tC, qd[kk], hi_kmaj, m_lo + off_m, hi_kmaj, id_c, kk > 0 ? 1u : 0u);
+            if (kk < kQt) mma_ts_w(tC, tQ + kk * 8, m_lo + off_m, hi_kmaj, id_c, kk > 0 ? 1u : 0u);
+            else mma_ss_w(tC, qd[kk], hi_kmaj, m_lo + off_m, hi_kmaj, id_c, kk > 0 ? 1u : 0u);
           }
         }
         const uint32_t tS = tmem + TM::s(sb);
@@ -431,7 +450,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             mma_ss_f8_w(tS, q8_lo + ((kk * 32) >> 4), hi_kmaj, kd[kk], hi_kmaj, id_s8, kk > 0 ? 1u : 0u);
         } else {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) mma_ss_w(tS, qd[kk], hi_kmaj, kd[kk], hi_kmaj, id_s, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            if (kk < kQt) mma_ts_w(tS, tQ + kk * 8, kd[kk], hi_kmaj, id_s, kk > 0 ? 1u : 0u);
+            else mma_ss_w(tS, qd[kk], hi_kmaj, kd[kk], hi_kmaj, id_s, kk > 0 ? 1u : 0u);
+          }
         }
         mma_commit(&s.s_full[sb]);
         mma_commit(&s.k_empty[ks]);

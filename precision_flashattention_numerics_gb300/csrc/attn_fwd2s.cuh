@@ -16,8 +16,10 @@
 //
 // Warp roles (352 threads): warps 0-7 softmax + epilogue (two sets), warp 8 TMA producer
 // (Q once, K' one block ahead of V, 16-block means chunks), warp 9 TMEM owner and the score /
-// offsets MMAs, warp 10 the PV MMAs. TMEM as attn_fwd_kernel: two score buffers S_0, S_1,
-// O, P and two offsets buffers. Every wait is bounded (ptx.cuh).
+// offsets MMAs, warp 10 the PV MMAs. TMEM: two score buffers S_0, S_1, O, P, two offsets
+// buffers and the Q tile (D / 2 columns). The score and offsets MMAs read Q from TMEM: a
+// tcgen05 MMA with A in TMEM runs at ~67 cycles per M = 128, N <= 128 step against ~86 with
+// both operands in shared memory. Every wait is bounded (ptx.cuh).
 //
 // Used for D = 64 prefill in modes 0-3 (pasa_lib.cu); the diagnostic, fp16-PV, FP8 and
 // split-key (decode) work stays on attn_fwd_kernel.
@@ -49,7 +51,8 @@ struct TmemMap {
   static constexpr int o = 2 * BN;
   static constexpr int p = 2 * BN + D;
   __host__ __device__ static constexpr int c(int b) { return 2 * BN + D + BN / 2 + b * kChunkBlocks; }
-  static constexpr int total = 2 * BN + D + BN / 2 + 2 * kChunkBlocks;
+  static constexpr int q = 2 * BN + D + BN / 2 + 2 * kChunkBlocks;   // Q as the A operand
+  static constexpr int total = q + D / 2;
   static_assert(total <= 512, "TMEM budget");
   static_assert(BN % 32 == 0 && BN <= 256, "key block");
   static_assert(D == 64 || D == 128, "head dim");
@@ -290,7 +293,15 @@ attn_fwd_2set_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_cons
       uint32_t qd[D / 16];
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) qd[kk] = q_lo + (((kk / 4) * Smem::kQChunk + (kk % 4) * 32) >> 4);
+      const uint32_t tQ = tmem + TM::q;
       bool ok = mbar_wait(&s.q_full, 0, abort_flag, 0x201);
+      if (ok && nblk > 0) {
+        // Q into TMEM once. Only with key blocks: without them the epilogue rewrites the Q
+        // buffer as soon as Q has landed, and no MMA completion would cover this copy.
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) tmem_cp_128x256b(tQ + kk * 8, qd[kk], hi_kmaj);
+      }
       for (int j = 0; ok && j < nblk; ++j) {
         const int ks = j % KST;
         const int ci = j / kChunkBlocks;
@@ -301,6 +312,7 @@ attn_fwd_2set_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_cons
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) kd[kk] = k_lo + (((kk / 4) * Smem::kKChunk + (kk % 4) * 32) >> 4);
         if (!mbar_wait(&s.k_full[ks], (j / KST) & 1, abort_flag, 0x202)) break;
+        if (!mbar_wait(&s.v_full[j % VST], (j / VST) & 1, abort_flag, 0x207)) break;
         if (chunk_start && !mbar_wait(&s.m_full[ci & 1], (ci >> 1) & 1, abort_flag, 0x203)) break;
         if (j >= 2 && !mbar_wait(&s.s_free[sb], ((j >> 1) - 1) & 1, abort_flag, 0x206)) break;
         tc_fence_after();
@@ -310,12 +322,12 @@ attn_fwd_2set_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_cons
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off_m = ((kk / 4) * Smem::kMChunk + (kk % 4) * 32) >> 4;
-            mma_ss_w(tC, qd[kk], hi_kmaj, m_lo + off_m, hi_kmaj, id_c, kk > 0 ? 1u : 0u);
+            mma_ts_w(tC, tQ + kk * 8, m_lo + off_m, hi_kmaj, id_c, kk > 0 ? 1u : 0u);
           }
         }
         const uint32_t tS = tmem + TM::s(sb);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) mma_ss_w(tS, qd[kk], hi_kmaj, kd[kk], hi_kmaj, id_s, kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < D / 16; ++kk) mma_ts_w(tS, tQ + kk * 8, kd[kk], hi_kmaj, id_s, kk > 0 ? 1u : 0u);
         mma_commit(&s.s_full[sb]);
         mma_commit(&s.k_empty[ks]);
         if (chunk_start) mma_commit(&s.m_empty[ci & 1]);
@@ -329,7 +341,10 @@ attn_fwd_2set_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_cons
     __syncwarp();
   } else if (warp == 10) {
     // ------------------------------------------------------------------ PV issuer
-    // PV(j) once the softmax has written P of block j and V_j has landed.
+    // PV(j) once the softmax has written P of block j. V_j has landed by then: the QK thread
+    // waited for it before issuing QK(j), and the softmax loads S_j (after QK(j) completes)
+    // before it writes P of block j. Waiting here as well cost ~1% (one more barrier poll
+    // on the path from the P store to the PV MMAs).
     if (lane == 0) {
       constexpr uint32_t id_o = idesc_f16(kTileRows, D, true, true);
       constexpr uint32_t hi_v = sdesc_hi_sw128(1024);
@@ -343,7 +358,6 @@ attn_fwd_2set_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_cons
         const uint32_t v_lo = v_lo0 + vs * kVStride;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) vd[kk] = v_lo + kk * (2048 >> 4);
-        if (!mbar_wait(&s.v_full[vs], (j / VST) & 1, abort_flag, 0x204)) break;
         if (!mbar_wait(&s.p_full, j & 1, abort_flag, 0x205)) break;
         tc_fence_after();
         const uint32_t acc0 = j > 0 ? 1u : 0u;

@@ -348,7 +348,6 @@ kshift_reg_kernel(const __half* __restrict__ k, __half* __restrict__ kshift, __h
   constexpr int RG = kShiftRegThreads / U;       // row groups
   constexpr int RPT = BN / RG;                   // rows per thread
   constexpr int NW = kShiftRegThreads / 32;
-  constexpr int LPR = 32 / U;                    // row groups per warp
   static_assert(BN % RG == 0 && 32 % U == 0, "layout");
   __shared__ uint32_t sh_max[NW][U][4];
   __shared__ uint32_t sh_sum[NW][U][8];

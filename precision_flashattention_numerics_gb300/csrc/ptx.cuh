@@ -334,6 +334,20 @@ __device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint3
       : "memory");
 }
 
+// Copy a 128-row x 32-byte tile from shared memory (given by the same descriptor words as an
+// MMA operand) into 128 TMEM lanes x 8 columns: row r -> lane r, bytes 4c..4c+3 of the row ->
+// column c, i.e. the layout of an fp16 A operand of a TS MMA for one K-step of 16. A later
+// tcgen05.mma issued by the same thread reads it without a wait (the two are executed in
+// issue order, PTX ISA: tcgen05 pipelined instruction pairs).
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint32_t s_lo, uint32_t s_hi) {
+  asm volatile(
+      "{\n\t.reg .b64 sd;\n\t"
+      "mov.b64 sd, {%1, %2};\n\t"
+      "tcgen05.cp.cta_group::1.128x256b [%0], sd;\n\t}" ::"r"(taddr),
+      "r"(s_lo), "r"(s_hi)
+      : "memory");
+}
+
 // kind::f8f6f4 with both operands in shared memory (e4m3 A and B with the descriptor of
 // idesc_e4m3; K = 32 elements per instruction).
 __device__ __forceinline__ void mma_ss_f8_w(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
