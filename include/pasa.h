@@ -173,14 +173,25 @@ int pasa_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, 
  * problem of n (batch, kv head) units with one kv head, or query rows [r0, r1) of one unit
  * with the keys they see, and every query tile meets the same key blocks and
  * pseudo-averages as in one call: the results are bit-identical to pasa_attn_fwd on the
- * same inputs. The three side streams are non-blocking streams the library creates once
- * per device and keeps. Errors: as pasa_attn_fwd (shapes and mode), PASA_ERR_WORKSPACE
- * when the buffer is too small, PASA_ERR_ALIGN when it is not 256-byte aligned; a failure
- * after enqueueing began still orders `stream` after all work already queued.
+ * same inputs. The three side streams are non-blocking streams the library creates on
+ * first use per device and keeps until pasa_release_host_streams. Errors: as
+ * pasa_attn_fwd (shapes and mode), PASA_ERR_WORKSPACE when the buffer is too small,
+ * PASA_ERR_ALIGN when it is not 256-byte aligned; a failure after enqueueing began still
+ * orders `stream` after all work already queued.
  */
 int pasa_attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                        int Sq, int Sk, int D, int causal, float scale, int mode, int chunks, void* device_buffer,
                        size_t device_buffer_bytes, void* stream);
+
+/* Destroys the three side streams pasa_attn_fwd_host created on the current device, after
+ * synchronizing each, so that the library holds no CUDA object of its own there; the next
+ * pasa_attn_fwd_host call on the device creates them again. The library has no counterpart
+ * in the paper: this is resource management of the host-buffer entry point. Call it only
+ * while no other host thread is inside pasa_attn_fwd_host on the same device (their calls
+ * would enqueue on a stream being destroyed). Returns PASA_OK (also when there was nothing
+ * to release) or PASA_ERR_CUDA (pasa_last_cuda_error gives the cudaError_t); the handles
+ * are dropped either way. */
+int pasa_release_host_streams(void);
 
 /* The pieces pasa_attn_fwd_host runs for these arguments, in order: writes min(count,
  * max_pieces) records of six ints (u0, n, r0, r1, k0, k1) to `pieces` (host memory) and

@@ -61,6 +61,7 @@ SIGNATURES = {
     "pasa_attn_fwd_host": ([_P, _P, _P, _P, _P] + [_I] * 7 + [_F, _I, _I, _P, _SZ, _P], _I),
     "pasa_attn_fwd_host_device_bytes": ([_I] * 9, _SZ),
     "pasa_attn_fwd_host_plan": ([_I] * 9 + [_P, _I], _I),
+    "pasa_release_host_streams": ([], _I),
     "pasa_check_device_error": ([_P, ctypes.POINTER(ctypes.c_ulonglong)], _I),
     "pasa_selftest_wait_timeout": ([_P], _I),
     "pasa_selftest_exp2": ([_P, _P, _P, _I, _P], _I),
@@ -249,6 +250,14 @@ def attn_fwd_host(q, k, v, causal: bool = False, scale: float | None = None, mod
     if sync:
         torch.cuda.current_stream().synchronize()
     return out, lse
+
+
+def release_host_streams() -> None:
+    """pasa_release_host_streams: destroy the side streams attn_fwd_host created on the
+    current device (recreated by the next attn_fwd_host call)."""
+    rc = library().pasa_release_host_streams()
+    if rc != 0:
+        raise PasaError(rc, "pasa_release_host_streams")
 
 
 def attn_fwd_stats(q, k, v, causal: bool = False, scale: float | None = None, mode: int = MODE_SHIFT_F16ACC,

@@ -1098,6 +1098,24 @@ cudaError_t copy_rows(void* dst, size_t dpitch, const void* src, size_t spitch, 
 
 }  // namespace
 
+extern "C" int pasa_release_host_streams(void) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return PASA_OK;   // none were ever created there
+  std::lock_guard<std::mutex> lock(g_side_mutex);
+  cudaError_t first = cudaSuccess;
+  for (int j = 0; j < 3; ++j) {
+    cudaStream_t& st = g_side_streams[dev][j];
+    if (st == nullptr) continue;
+    e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess) e = cudaStreamDestroy(st);
+    if (e != cudaSuccess && first == cudaSuccess) first = e;
+    st = nullptr;   // a failed destroy leaves the handle to the runtime; never reuse it
+  }
+  return first == cudaSuccess ? PASA_OK : cuda_fail(first);
+}
+
 extern "C" size_t pasa_attn_fwd_host_device_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal,
                                                    int mode, int chunks) {
   if (chunks < 0 || validate_shape(B, Hq, Hkv, Sq, Sk, D, mode) != PASA_OK) return 0;

@@ -164,6 +164,26 @@ def test_host_calls_queue_in_order_on_one_buffer():
         assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
 
 
+def test_release_host_streams_then_call_again():
+    """pasa_release_host_streams drops the side streams (after their work is done); the
+    next host call creates them again and still agrees bit for bit. Releasing twice, or
+    before any host call, is a no-op."""
+    p = pasa()
+    B, Hq, Hkv, Sq, Sk, D = 2, 6, 3, 400, 400, 128
+    q, k, v = make(B, Hq, Hkv, Sq, Sk, D, "kbias", 734, bias_std=20.0)
+    o_ref, lse_ref = device_result(q, k, v, True, 0)
+    qh, kh, vh = host_tensors(q, k, v)
+    o1, l1 = p.attn_fwd_host(qh, kh, vh, causal=True, mode=0, chunks=3, sync=False)
+    p.release_host_streams()   # waits for the side streams' share of the call above
+    torch.cuda.current_stream().synchronize()
+    assert torch.equal(o1, o_ref) and torch.equal(l1, lse_ref)
+    p.release_host_streams()
+    o2, l2 = p.attn_fwd_host(qh, kh, vh, causal=True, mode=0, chunks=3)
+    assert torch.equal(o2, o_ref) and torch.equal(l2, lse_ref)
+    p.release_host_streams()
+    p.check_device_error()
+
+
 def test_host_against_oracle():
     p = pasa()
     B, Hq, Hkv, Sq, Sk, D = 2, 4, 2, 333, 333, 128
