@@ -158,8 +158,10 @@ int pasa_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, 
  *             Sk >= Sq with Sk - Sq a multiple of 128).
  *   device_buffer, device_buffer_bytes
  *             device memory of at least pasa_attn_fwd_host_device_bytes(...) bytes, 256-byte
- *             aligned: it stages the whole problem (q, k, v, o, lse) and two shift
- *             workspaces, one per compute stream. Its contents on entry do not matter.
+ *             aligned: it stages the whole problem (q, k, v, o, lse), the prepared
+ *             keys of each unit cut into query-row pieces (each piece prepares only the
+ *             key blocks it newly sees) and two shift workspaces for the other pieces,
+ *             one per compute stream. Its contents on entry do not matter.
  *             NULL: the call takes it from the stream-ordered allocator on `stream` and
  *             frees it there.
  *   stream    the stream the kernels run on. The call only enqueues: o and lse hold the

@@ -159,12 +159,16 @@ int launch_kshift(const void* k, void* ks, void* means, float* kscale, int B, in
 }
 
 // fp16 K' for the fp16 modes; e4m3 codes (of K', or of K in the naive FP8 mode) otherwise.
+// The key preparation of `mode` (fp16 shift, or e4m3 codes and scales) for key blocks
+// [first_block, ceil(Sk / BN)) of heads holding cap (>= Sk) rows each.
 int kshift_dispatch(const void* k, void* ks, void* means, float* kscale, int B, int H, int Sk, int D, int mode,
-                    cudaStream_t st) {
-  if (mode == PASA_MODE_SHIFT_FP8) return launch_kshift<128, pasa::kShiftFp8>(k, ks, means, kscale, B, H, Sk, st);
-  if (mode == PASA_MODE_NAIVE_FP8) return launch_kshift<128, pasa::kRawFp8>(k, ks, means, kscale, B, H, Sk, st);
-  return D == 64 ? launch_kshift<64, pasa::kShiftF16>(k, ks, means, nullptr, B, H, Sk, st)
-                 : launch_kshift<128, pasa::kShiftF16>(k, ks, means, nullptr, B, H, Sk, st);
+                    cudaStream_t st, int first_block = 0, int cap = 0) {
+  if (mode == PASA_MODE_SHIFT_FP8)
+    return launch_kshift<128, pasa::kShiftFp8>(k, ks, means, kscale, B, H, Sk, st, first_block, cap);
+  if (mode == PASA_MODE_NAIVE_FP8)
+    return launch_kshift<128, pasa::kRawFp8>(k, ks, means, kscale, B, H, Sk, st, first_block, cap);
+  return D == 64 ? launch_kshift<64, pasa::kShiftF16>(k, ks, means, nullptr, B, H, Sk, st, first_block, cap)
+                 : launch_kshift<128, pasa::kShiftF16>(k, ks, means, nullptr, B, H, Sk, st, first_block, cap);
 }
 
 template <int D, bool F16ACC, bool SHIFT, bool CAUSAL, bool STATS, bool F16PV = false, bool FP8 = false>
@@ -954,12 +958,14 @@ struct HostPiece {
   int u0 = 0, n = 0;    // units [u0, u0 + n)
   int r0 = 0, r1 = 0;   // query rows [r0, r1) of each unit
   int k0 = 0, k1 = 0;   // keys this piece copies in; it attends keys [0, k1)
+  bool rowcut = false;  // one of the query-row pieces of a unit
   size_t q_off = 0, kv_off = 0, o_off = 0, lse_off = 0;  // slots in the device buffer
+  size_t prep_off = 0;  // rowcut with a key preparation: the unit's prepared keys (all Sk rows)
 };
 
 struct HostPlan {
   std::vector<HostPiece> pieces;
-  int max_units = 0;  // units in the largest piece
+  int max_units = 0;  // units in the largest piece that is not a row piece
   size_t ws_off = 0, ws_bytes = 0, total = 0;
 };
 
@@ -1020,7 +1026,7 @@ HostPlan host_plan(int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, in
         int kprev = 0;
         for (size_t i = 0; i + 1 < cuts.size(); ++i) {
           HostPiece pc;
-          pc.u0 = u, pc.n = 1, pc.r0 = cuts[i], pc.r1 = cuts[i + 1];
+          pc.u0 = u, pc.n = 1, pc.r0 = cuts[i], pc.r1 = cuts[i + 1], pc.rowcut = true;
           pc.k1 = causal ? pc.r1 + (Sk - Sq) : Sk;
           pc.k0 = kprev;
           kprev = pc.k1;
@@ -1039,9 +1045,14 @@ HostPlan host_plan(int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, in
     }
   }
   // slots: q and o [n, g, rows, D], lse [n, g, rows], and the keys/values [n, Sk, D] of a
-  // unit once (row pieces after the first of a unit reuse it); each 256-byte aligned
+  // unit once (row pieces after the first of a unit reuse it), with, for a unit cut into
+  // row pieces, its prepared keys (shifted keys and means, or e4m3 codes and scales, for
+  // all Sk rows): each row piece prepares only the key blocks it newly sees, the blocks
+  // before them being final once written (a block's preparation reads that block only);
+  // each slot 256-byte aligned
   const size_t row_bytes = static_cast<size_t>(D) * 2;
-  size_t off = 0, kv_last = 0;
+  const size_t prep_bytes = align_up(pasa_attn_fwd_workspace_bytes(1, 1, Sk, D, mode), 256);
+  size_t off = 0, kv_last = 0, prep_last = 0;
   int kv_unit = -1;
   for (HostPiece& pc : hp.pieces) {
     const size_t nrows = static_cast<size_t>(pc.n) * g * (pc.r1 - pc.r0);
@@ -1050,16 +1061,22 @@ HostPlan host_plan(int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, in
     pc.lse_off = off; off += align_up(nrows * 4, 256);
     if (pc.n == 1 && pc.k0 > 0 && kv_unit == pc.u0) {
       pc.kv_off = kv_last;
+      pc.prep_off = prep_last;
     } else {
       pc.kv_off = kv_last = off;
       kv_unit = pc.n == 1 ? pc.u0 : -1;
       off += 2 * align_up(static_cast<size_t>(pc.n) * Sk * row_bytes, 256);
+      if (pc.rowcut && prep_bytes > 0) {
+        pc.prep_off = prep_last = off;
+        off += prep_bytes;
+      }
     }
-    if (pc.n > hp.max_units) hp.max_units = pc.n;
+    if (!pc.rowcut && pc.n > hp.max_units) hp.max_units = pc.n;
   }
-  // one shift workspace per compute stream (pieces alternate between two)
+  // one shift workspace per compute stream (pieces alternate between two), for the pieces of
+  // whole units
   hp.ws_off = off;
-  hp.ws_bytes = align_up(pasa_attn_fwd_workspace_bytes(hp.max_units, 1, Sk, D, mode), 256);
+  hp.ws_bytes = hp.max_units > 0 ? align_up(pasa_attn_fwd_workspace_bytes(hp.max_units, 1, Sk, D, mode), 256) : 0;
   hp.total = off + (hp.pieces.size() > 1 ? 2 : 1) * hp.ws_bytes;
   return hp;
 }
@@ -1159,9 +1176,10 @@ extern "C" int pasa_attn_fwd_host(const void* q, const void* k, const void* v, v
   cudaStream_t s_run[2] = {st, side[2]};  // piece i computes on s_run[i % 2]
 
   // events: [0] start on st, [1] h2d stream done, [2] d2h stream done, [3] second compute
-  // stream done, [4 + i] piece i's inputs landed, [4 + np + i] piece i's kernels finished
+  // stream done, [4 + i] piece i's inputs landed, [4 + np + i] piece i's kernels finished,
+  // [4 + 2 np + i] a row piece's key blocks, and those of its unit's earlier pieces, prepared
   const int np = static_cast<int>(hp.pieces.size());
-  std::vector<cudaEvent_t> ev(4 + 2 * static_cast<size_t>(np), nullptr);
+  std::vector<cudaEvent_t> ev(4 + 3 * static_cast<size_t>(np), nullptr);
   cudaError_t e = cudaSuccess;
   size_t made = 0;
   for (; made < ev.size(); ++made) {
@@ -1216,17 +1234,36 @@ extern "C" int pasa_attn_fwd_host(const void* q, const void* k, const void* v, v
                    w, static_cast<size_t>(pc.n) * g, cudaMemcpyHostToDevice, s_in));
     step(cudaEventRecord(ev[4 + i], s_in));
   }
+  const bool prep = shift_mode(mode) || fp8_mode(mode);
+  const WorkspaceLayout pl = workspace_layout(1, 1, Sk, D, mode);   // a row-cut unit's prepared keys
+  const int bn = pasa::block_rows_for(D);
   for (int i = 0; i < np && e == cudaSuccess; ++i) {
     const HostPiece& pc = hp.pieces[i];
     const size_t kv_bytes = align_up(static_cast<size_t>(pc.n) * kv_unit, 256);
     const int rows = pc.r1 - pc.r0;
     cudaStream_t run = s_run[i & 1];
     if (!step(cudaStreamWaitEvent(run, ev[4 + i], 0))) break;
-    const int krc = pasa_attn_fwd_ws(buf + pc.q_off, buf + pc.kv_off, buf + pc.kv_off + kv_bytes, buf + pc.o_off,
-                                     lse ? reinterpret_cast<float*>(buf + pc.lse_off) : nullptr, pc.n, g, 1, rows,
-                                     pc.k1, D, causal, scale, mode,
-                                     hp.ws_bytes ? buf + hp.ws_off + (i & 1) * hp.ws_bytes : nullptr, hp.ws_bytes,
-                                     run);
+    int krc = PASA_OK;
+    if (pc.rowcut && prep) {
+      // prepare this piece's new key blocks [k0, k1) into the unit's slot, then wait until
+      // the unit's earlier pieces have prepared theirs (on either compute stream)
+      uint8_t* pb = buf + pc.prep_off;
+      float* kscale = fp8_mode(mode) ? reinterpret_cast<float*>(pb + pl.kscale_off) : nullptr;
+      if (pc.k1 > pc.k0) krc = kshift_dispatch(buf + pc.kv_off, pb + pl.kshift_off, pb + pl.means_off, kscale, 1, 1,
+                                               pc.k1, D, mode, run, pc.k0 / bn, Sk);
+      if (krc == PASA_OK && i > 0 && hp.pieces[i - 1].rowcut && hp.pieces[i - 1].u0 == pc.u0)
+        step(cudaStreamWaitEvent(run, ev[4 + 2 * np + i - 1], 0));
+      step(cudaEventRecord(ev[4 + 2 * np + i], run));
+      if (krc == PASA_OK && e == cudaSuccess)
+        krc = attn_launch(buf + pc.q_off, pb + pl.kshift_off, pb + pl.means_off, buf + pc.kv_off + kv_bytes,
+                          buf + pc.o_off, lse ? reinterpret_cast<float*>(buf + pc.lse_off) : nullptr, 1, g, 1, rows,
+                          pc.k1, D, causal, scale, mode, run, nullptr, nullptr, kscale);
+    } else {
+      krc = pasa_attn_fwd_ws(buf + pc.q_off, buf + pc.kv_off, buf + pc.kv_off + kv_bytes, buf + pc.o_off,
+                             lse ? reinterpret_cast<float*>(buf + pc.lse_off) : nullptr, pc.n, g, 1, rows, pc.k1, D,
+                             causal, scale, mode, hp.ws_bytes ? buf + hp.ws_off + (i & 1) * hp.ws_bytes : nullptr,
+                             hp.ws_bytes, run);
+    }
     if (krc != PASA_OK) {
       rc = krc;
       break;
