@@ -349,21 +349,25 @@ def bench_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int, also
     torch.cuda.synchronize()
     n_e2e = n
     barrier(world)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(n_e2e):
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e + 1)]
+    marks[0].record(stream)
+    for i in range(n_e2e):
         e2e_step()
-    e1.record(stream)
+        marks[i + 1].record(stream)
     torch.cuda.synchronize()
     pasa.check_device_error()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    e2e_ms = max_over_ranks(marks[0].elapsed_time(marks[-1]), world)
+    step_ms = [marks[i].elapsed_time(marks[i + 1]) for i in range(n_e2e)]
     res["e2e"] = {
         "value": flops * n_e2e * world / (e2e_ms * 1e-3) / 1e12,
         "unit": "TFLOP/s",
         "h2d_bytes_per_step": int(q.nbytes + k.nbytes + v.nbytes),
         "d2h_bytes_per_step": int(oh.numel() * 2 + lh.numel() * 4),
         "ms_per_step": e2e_ms / n_e2e,
+        # value and ms_per_step are over all timed steps; single steps of this path now and
+        # then stall for several ms (host copy path), which these two make visible
+        "median_step_ms": statistics.median(step_ms),
+        "max_step_ms": max(step_ms),
     }
     return res
 
