@@ -373,9 +373,11 @@ def bench_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int, also
 
 
 def bench_decode(args, w: wl.Workload, local_rank: int, sampler=None):
-    """One decode step: refresh the shifted cache's last block (where the new key row lands:
-    pasa_kshift_blocks) and attend (pasa_attn_fwd_decode: decode kernel + split merge).
-    The cache is shifted once before timing, as a prefill would leave it."""
+    """One decode step: refresh the shifted cache's last block (where the new key row lands)
+    and attend (decode kernel + split merge). The fp16 shifted cache takes both in one call,
+    pasa_attn_fwd_decode_step, whose decode kernel overlaps the refresh; the e4m3 cache
+    calls pasa_kprep_fp8_blocks, then pasa_attn_fwd_decode_fp8. attn_ms times the attend
+    call alone. The cache is shifted once before timing, as a prefill would leave it."""
     import torch
 
     import precision_flashattention_numerics_gb300 as pasa
@@ -412,30 +414,45 @@ def bench_decode(args, w: wl.Workload, local_rank: int, sampler=None):
         else:
             pasa.attn_fwd_decode(qt, ks, means, vt, causal=w.causal, mode=mode, out=o, lse=lse, workspace=ws)
 
+    combined = shift and not fp8   # one call: pasa_attn_fwd_decode_step (the decode kernel overlaps the refresh)
+
+    def step():
+        if combined:
+            pasa.attn_fwd_decode_step(qt, kt, ks, means, vt, last, causal=w.causal, mode=mode, out=o, lse=lse,
+                                      workspace=ws)
+        else:
+            refresh()
+            attend()
+
     for _ in range(max(3, args.warmup)):
-        refresh()
-        attend()
+        step()
     torch.cuda.synchronize()
     pasa.check_device_error()
     n = args.steps if args.decode else max(args.steps, 20)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
     if sampler:
         sampler.__enter__()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
+    marks[0].record(stream)
     for i in range(n):
-        ev[i][0].record(stream)
-        refresh()
-        ev[i][1].record(stream)
-        attend()
-        ev[i][2].record(stream)
+        step()
+        marks[i + 1].record(stream)
     torch.cuda.synchronize()
     wall_ms = (time.perf_counter() - t0) * 1e3 / n
     if sampler:
         sampler.__exit__(None, None, None)
     pasa.check_device_error()
-    step_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][2]) for i in range(n))
-    attn_ms = statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for i in range(n))
+    step_ms = marks[0].elapsed_time(marks[-1]) / n
+    # the attend call alone (events around each call), for the kernel's roofline
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    for i in range(n):
+        ev[i][0].record(stream)
+        attend()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    pasa.check_device_error()
+    attn_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(n))
     nb = -(-w.Sk // bn)
     # algorithmic bytes of the attention: the cache (K' or K: fp16, or e4m3 codes and block
     # scales; V fp16), the block means, q, o, lse
@@ -449,6 +466,7 @@ def bench_decode(args, w: wl.Workload, local_rank: int, sampler=None):
         "attn_bytes": moved, "attn_gbs": round(gbs, 1), "finite": bool(torch.isfinite(o).all().item()),
         "launches_per_step": (1 if (shift or fp8) else 0) + (2 if nbytes else 1),
         "merge": "combine_splits_kernel" if nbytes else "in the decode kernel (thread-block cluster)",
+        "step_call": "pasa_attn_fwd_decode_step" if combined else "refresh, then attend",
     }
 
 

@@ -380,6 +380,29 @@ int pasa_attn_fwd_decode(const void* q, const void* k_shifted, const void* means
                          int splits, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * One decode step on a shifted fp16 key cache: the refresh of pasa_kshift_blocks(k,
+ * k_shifted, means, B, Hkv, Sk, Sk_cap, D, first_block) followed by pasa_attn_fwd_decode on
+ * the refreshed cache, in one call (same citation as pasa_kshift_blocks; the library's
+ * pairing of the two has no counterpart in the paper). Results are bit-identical to the two
+ * calls in sequence. The difference is scheduling: the decode kernel is launched with
+ * programmatic dependence on the refresh, starts while the refresh still runs, and waits
+ * for it (griddepcontrol.wait) only before it reads key blocks first_block and later (their
+ * K', means and scales), which every split reaches last, so the refresh is hidden. The
+ * decode kernels that do not take this schedule (more than 32 packed rows, or D = 64) run
+ * after the refresh in stream order.
+ *   k          the raw fp16 key cache [B, Hkv, Sk_cap, D] the refresh reads
+ *   k_shifted, means   the shifted cache and its block means, rewritten from first_block on
+ *   other arguments as pasa_attn_fwd_decode; modes 2 and 3 (no shifted cache) only run
+ *   the decode, and the FP8 modes are PASA_ERR_UNSUPPORTED (pasa_kprep_fp8_blocks and
+ *   pasa_attn_fwd_decode_fp8 cover them). Errors: as the two calls; all arguments are
+ *   checked before anything is enqueued.
+ */
+int pasa_attn_fwd_decode_step(const void* q, const void* k, void* k_shifted, void* means, const void* v, void* o,
+                              float* lse, int B, int Hq, int Hkv, int Sq, int Sk, int Sk_cap, int D, int causal,
+                              float scale, int mode, int first_block, int splits, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/*
  * Decode on an FP8 key cache (modes 5 and 6; the FP8 score modes of pasa_attn_fwd_fp8 on
  * the decode work layout of pasa_attn_fwd_decode). The cache holds e4m3 codes k8 [B, Hkv,
  * Sk_cap, D] uint8 with one fp32 scale per 128-key block, kscale [B, Hkv,

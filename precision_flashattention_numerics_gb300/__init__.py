@@ -55,6 +55,7 @@ SIGNATURES = {
     "pasa_kshift_blocks": ([_P, _P, _P, _I, _I, _I, _I, _I, _I, _P], _I),
     "pasa_attn_fwd_decode_workspace_bytes": ([_I, _I, _I, _I, _I, _I, _I], _SZ),
     "pasa_attn_fwd_decode": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P], _I),
+    "pasa_attn_fwd_decode_step": ([_P, _P, _P, _P, _P, _P, _P] + [_I] * 8 + [_F, _I, _I, _I, _P, _SZ, _P], _I),
     "pasa_attn_fwd_decode_fp8": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P],
                                  _I),
     "pasa_kprep_fp8_blocks": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P], _I),
@@ -408,6 +409,34 @@ def attn_fwd_decode(q, k_shifted, means, v, causal: bool = False, scale: float |
                                   _ptr(workspace) if nbytes else None, nbytes, _stream())
     if rc != 0:
         raise PasaError(rc, "pasa_attn_fwd_decode")
+    return out, lse
+
+
+def attn_fwd_decode_step(q, k, k_shifted, means, v, first_block: int, causal: bool = False,
+                         scale: float | None = None, mode: int = MODE_SHIFT_F16ACC, splits: int = 0, out=None,
+                         lse=None, workspace=None, length: int | None = None):
+    """pasa_attn_fwd_decode_step: refresh key blocks first_block.. of the shifted cache
+    (k_shifted, means) from the raw cache k, then decode on it, in one call (the decode kernel
+    overlaps the refresh). Arguments as :func:`attn_fwd_decode` plus the raw cache k
+    [B,Hkv,cap,D] and first_block. Returns (o, lse)."""
+    lib = library()
+    _check(q, "q"), _check(k, "k"), _check(k_shifted, "k_shifted"), _check(v, "v")
+    if means is not None:
+        _check(means, "means")
+    B, Hq, Sq, D = q.shape
+    _, Hkv, cap, _ = k_shifted.shape
+    Sk = cap if length is None else int(length)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, Hq, Sq), device=q.device, dtype=torch.float32) if lse is None else lse
+    nbytes = lib.pasa_attn_fwd_decode_workspace_bytes(B, Hq, Hkv, Sq, Sk, D, int(splits))
+    if nbytes and (workspace is None or workspace.numel() * workspace.element_size() < nbytes):
+        workspace = torch.empty(nbytes, device=q.device, dtype=torch.uint8)
+    rc = lib.pasa_attn_fwd_decode_step(_ptr(q), _ptr(k), _ptr(k_shifted), _ptr(means) if means is not None else None,
+                                       _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Sk, cap, D, int(bool(causal)),
+                                       float(scale) if scale is not None else 0.0, int(mode), int(first_block),
+                                       int(splits), _ptr(workspace) if nbytes else None, nbytes, _stream())
+    if rc != 0:
+        raise PasaError(rc, "pasa_attn_fwd_decode_step")
     return out, lse
 
 

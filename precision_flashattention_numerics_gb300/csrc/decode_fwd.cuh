@@ -69,6 +69,11 @@ struct DecodeParams {
                       // merge their partial results through distributed shared memory
   const float* kscale;  // FP8: [planes][kstride] fp32 e4m3 scale of each key block
   int kstride;
+  // The first key block (global index) that the kernel queued ahead of this launch rewrites
+  // (a cache refresh, with this launch's programmatic dependence on it): its keys, means and
+  // scales, and those of every later block, are read only after griddep_wait(). INT_MAX:
+  // nothing to wait for.
+  int dep_block;
 };
 
 template <int NQ, int KST, int VST, bool FP8 = false, int G = 1>
@@ -207,9 +212,17 @@ decode_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
 #pragma unroll
       for (int c = 0; c < 2; ++c) tma_load_3d(s.q + c * Smem::kQChunk, &mapQ, &s.q_full, c * 64, 0, plane);
       int k_issued = 0, v_issued = 0, m_issued = 0;
+      bool dep_done = false;
+      auto dep_wait = [&](int first_global_block) {   // before reading a refreshed block
+        if (!dep_done && first_global_block >= p.dep_block) {
+          griddep_wait();
+          dep_done = true;
+        }
+      };
       auto load_k = [&](int j) -> bool {
         if (SHIFT && (j % kChunkBlocks) == 0) {
           const int ci = j / kChunkBlocks, slot = ci & 1;
+          dep_wait(jb0 + j + kChunkBlocks - 1);   // the chunk's last block
           if (!mbar_wait(&s.m_empty[slot], ((ci >> 1) & 1) ^ 1, abort_flag, 0x501)) return false;
           mbar_arrive_expect_tx(&s.m_full[slot], Smem::kMTile);
 #pragma unroll
@@ -218,6 +231,7 @@ decode_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
           m_issued = ci + 1;
         }
         const int ks = j % KST;
+        dep_wait(jb0 + j);
         if (!mbar_wait(&s.k_empty[ks], ((j / KST) & 1) ^ 1, abort_flag, 0x502)) return false;
         mbar_arrive_expect_tx(&s.k_full[ks], Smem::kKTile);
 #pragma unroll
@@ -405,7 +419,15 @@ decode_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
 
     // FP8: block scales, loaded one block ahead so the load is off the score path
     const float* kscale_row = FP8 ? p.kscale + static_cast<size_t>(plane) * p.kstride : nullptr;
-    float sk_next = (FP8 && g < nblk) ? __ldg(kscale_row + jb0 + g) : 1.0f;
+    bool dep_done = false;   // FP8: the block scales of refreshed blocks after griddep_wait()
+    auto scale_of = [&](int global_block) {
+      if (!dep_done && global_block >= p.dep_block) {
+        griddep_wait();
+        dep_done = true;
+      }
+      return __ldg(kscale_row + global_block);
+    };
+    float sk_next = (FP8 && g < nblk) ? scale_of(jb0 + g) : 1.0f;
     for (int j = g; j < nblk; j += G) {
       const int i = j / G;   // the group's local block index
       const int sb = i & 1;
@@ -413,7 +435,7 @@ decode_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
       float sk = 1.0f;
       if constexpr (FP8) {
         sk = sk_next;
-        if (j + G < nblk) sk_next = __ldg(kscale_row + jg + G);
+        if (j + G < nblk) sk_next = scale_of(jg + G);
       }
       if (SHIFT && (j % kChunkBlocks) == g) {   // the group's first block of a chunk
         // offsets of the chunk's 16 blocks: thread t takes block t % 16 and the query rows

@@ -95,7 +95,9 @@ kshift_kernel(const __half* __restrict__ k, void* __restrict__ kshift, __half* _
   __shared__ uint32_t sh_amax[NW];
 
   // blocks [j0, nb) of the Sk valid rows; planes are cap rows (means: nb_cap blocks) apart.
-  // j0 > 0 refreshes the tail of a key cache after an append.
+  // j0 > 0 refreshes the tail of a key cache after an append. A decode launch queued behind
+  // a refresh may start now: it reads the refreshed blocks only after griddep_wait().
+  griddep_launch_dependents();
   const int j = j0 + blockIdx.x;
   const int bh = blockIdx.y;
   const int tid = threadIdx.x;
@@ -352,6 +354,7 @@ kshift_reg_kernel(const __half* __restrict__ k, __half* __restrict__ kshift, __h
   __shared__ uint32_t sh_max[NW][U][4];
   __shared__ uint32_t sh_sum[NW][U][8];
 
+  griddep_launch_dependents();   // as in kshift_kernel: a queued decode launch may start
   const int j = j0 + blockIdx.x;
   const int bh = blockIdx.y;
   const int tid = threadIdx.x;

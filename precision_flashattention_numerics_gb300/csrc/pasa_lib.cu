@@ -1,6 +1,7 @@
 // libpasa.so: the C ABI declared in include/pasa.h. Host-side argument validation, TMA
 // descriptor encoding, workspace layout and kernel dispatch. Compiled as one translation
 // unit for sm_103a.
+#include <climits>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -293,9 +294,11 @@ int twoset_dispatch(int mode, int causal, const CUtensorMap& mq, const CUtensorM
 }
 
 // The swapped-operand decode kernel (D = 128, at most 32 packed query rows per kv head).
+// pdl: launch with programmatic stream serialization, so the kernel may start while the
+// refresh queued ahead of it still runs (it waits for it before reading p.dep_block on).
 template <int NQ, bool F16ACC, bool SHIFT, bool F16PV, bool FP8 = false>
 int launch_decode(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mm,
-                         const pasa::DecodeParams& p, long long planes, int splits, cudaStream_t st) {
+                         const pasa::DecodeParams& p, long long planes, int splits, cudaStream_t st, bool pdl) {
   // e4m3 keys at 16 columns: two softmax warpgroups (even and odd key blocks) and rings of
   // 4 K + 3 V; fp16 keys: one group with 3 K' + 3 V (16 columns) or 3 + 2 (32 columns).
   // (Measured on the 8 x 32K-key cache: two groups lift the e4m3 cache by 7%, while the fp16
@@ -311,15 +314,24 @@ int launch_decode(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMa
   cfg.blockDim = dim3(pasa::dec_threads(G));
   cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
+  unsigned na = 0;
   if (p.cluster) {
     // the splits of a kv head as one cluster (at most 8: the portable cluster size)
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = static_cast<unsigned>(splits);
-    attr[0].val.clusterDim.z = 1;
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 1;
+    attr[na].val.clusterDim.y = static_cast<unsigned>(splits);
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  if (na > 0) {
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = na;
   }
   e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mm, p);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -330,17 +342,20 @@ int launch_decode(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMa
 template <int NQ>
 int decode_dispatch(int mode, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                            const CUtensorMap& mm, const pasa::DecodeParams& p, long long planes, int splits,
-                           cudaStream_t st) {
+                           cudaStream_t st, bool pdl) {
+#define PASA_DEC_CASE(MODE, ...) \
+  case MODE: return launch_decode<NQ, __VA_ARGS__>(mq, mk, mv, mm, p, planes, splits, st, pdl);
   switch (mode) {
-    case PASA_MODE_SHIFT_F16ACC: return launch_decode<NQ, true, true, false>(mq, mk, mv, mm, p, planes, splits, st);
-    case PASA_MODE_SHIFT_F32ACC: return launch_decode<NQ, false, true, false>(mq, mk, mv, mm, p, planes, splits, st);
-    case PASA_MODE_NAIVE_F16ACC: return launch_decode<NQ, true, false, false>(mq, mk, mv, mm, p, planes, splits, st);
-    case PASA_MODE_NOSHIFT_F32ACC: return launch_decode<NQ, false, false, false>(mq, mk, mv, mm, p, planes, splits, st);
-    case PASA_MODE_SHIFT_F16ALL: return launch_decode<NQ, true, true, true>(mq, mk, mv, mm, p, planes, splits, st);
-    case PASA_MODE_SHIFT_FP8: return launch_decode<NQ, false, true, false, true>(mq, mk, mv, mm, p, planes, splits, st);
-    case PASA_MODE_NAIVE_FP8: return launch_decode<NQ, false, false, false, true>(mq, mk, mv, mm, p, planes, splits, st);
+    PASA_DEC_CASE(PASA_MODE_SHIFT_F16ACC, true, true, false)
+    PASA_DEC_CASE(PASA_MODE_SHIFT_F32ACC, false, true, false)
+    PASA_DEC_CASE(PASA_MODE_NAIVE_F16ACC, true, false, false)
+    PASA_DEC_CASE(PASA_MODE_NOSHIFT_F32ACC, false, false, false)
+    PASA_DEC_CASE(PASA_MODE_SHIFT_F16ALL, true, true, true)
+    PASA_DEC_CASE(PASA_MODE_SHIFT_FP8, false, true, false, true)
+    PASA_DEC_CASE(PASA_MODE_NAIVE_FP8, false, false, false, true)
     default: return PASA_ERR_UNSUPPORTED;
   }
+#undef PASA_DEC_CASE
 }
 
 }  // namespace
@@ -548,10 +563,13 @@ size_t pasa_attn_fwd_decode_workspace_bytes(int B, int Hq, int Hkv, int Sq, int 
 }
 
 // Decode on a key cache: fp16 keys (K' or K) for modes 0-4, e4m3 codes with block scales
-// `kscale` for modes 5 and 6.
+// `kscale` for modes 5 and 6. dep_block < nb: the kernel queued just ahead on the stream
+// rewrites key blocks [dep_block, nb) (a refresh); the swapped-operand decode kernel then
+// starts while it runs and waits for it only before reading those blocks.
 static int decode_impl(const void* q, const void* k_shifted, const void* means, const float* kscale, const void* v,
                        void* o, float* lse, int B, int Hq, int Hkv, int Sq, int Sk, int Sk_cap, int D, int causal,
-                       float scale, int mode, int splits, void* workspace, size_t workspace_bytes, void* stream) {
+                       float scale, int mode, int splits, void* workspace, size_t workspace_bytes, void* stream,
+                       int dep_block = INT_MAX) {
   int rc = validate(q, k_shifted, v, o, lse, B, Hq, Hkv, Sq, Sk, D, mode);
   if (rc != PASA_OK) return rc;
   if (Sk_cap < Sk) return PASA_ERR_SHAPE;
@@ -620,8 +638,10 @@ static int decode_impl(const void* q, const void* k_shifted, const void* means, 
     dp.cluster = cluster ? 1 : 0;
     dp.kscale = kscale;
     dp.kstride = (Sk_cap + bn - 1) / bn;
-    rc = nq == 16 ? decode_dispatch<16>(mode, mq, mk, mv, mmeans, dp, planes, sp, st)
-                  : decode_dispatch<32>(mode, mq, mk, mv, mmeans, dp, planes, sp, st);
+    dp.dep_block = dep_block;
+    const bool pdl = dep_block < nb;
+    rc = nq == 16 ? decode_dispatch<16>(mode, mq, mk, mv, mmeans, dp, planes, sp, st, pdl)
+                  : decode_dispatch<32>(mode, mq, mk, mv, mmeans, dp, planes, sp, st, pdl);
   } else {
     // query rows on the MMA's M side: the attention kernel on the packed [g * Sq] rows
     if ((rc = make_map(&mq, q, D, rows, planes, pasa::kTileRows)) != PASA_OK) return rc;
@@ -667,6 +687,40 @@ int pasa_attn_fwd_decode(const void* q, const void* k_shifted, const void* means
   if (fp8_mode(mode)) return PASA_ERR_UNSUPPORTED;   // e4m3 caches: pasa_attn_fwd_decode_fp8
   return decode_impl(q, k_shifted, means, nullptr, v, o, lse, B, Hq, Hkv, Sq, Sk, Sk_cap, D, causal, scale, mode,
                      splits, workspace, workspace_bytes, stream);
+}
+
+int pasa_attn_fwd_decode_step(const void* q, const void* k, void* k_shifted, void* means, const void* v, void* o,
+                              float* lse, int B, int Hq, int Hkv, int Sq, int Sk, int Sk_cap, int D, int causal,
+                              float scale, int mode, int first_block, int splits, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  if (fp8_mode(mode)) return PASA_ERR_UNSUPPORTED;   // e4m3 caches: pasa_kprep_fp8_blocks + _decode_fp8
+  if (!shift_mode(mode)) {
+    // raw-key modes keep no shifted copy: nothing to refresh
+    return decode_impl(q, k_shifted, means, nullptr, v, o, lse, B, Hq, Hkv, Sq, Sk, Sk_cap, D, causal, scale, mode,
+                       splits, workspace, workspace_bytes, stream);
+  }
+  // argument checks of both calls before anything is enqueued
+  if (!k) return PASA_ERR_NULLPTR;
+  if (!aligned16(k)) return PASA_ERR_ALIGN;
+  int rc = validate(q, k_shifted, v, o, lse, B, Hq, Hkv, Sq, Sk, D, mode);
+  if (rc != PASA_OK) return rc;
+  if (!means) return PASA_ERR_NULLPTR;
+  if (!aligned16(means)) return PASA_ERR_ALIGN;
+  if (Sk_cap < Sk || splits < 0) return Sk_cap < Sk ? PASA_ERR_SHAPE : PASA_ERR_UNSUPPORTED;
+  const int nb = (Sk + pasa::block_rows_for(D) - 1) / pasa::block_rows_for(D);
+  if (first_block < 0 || first_block >= nb || static_cast<long long>(B) * Hkv > 65535) return PASA_ERR_SHAPE;
+  if (static_cast<long long>(Hq / Hkv) * Sq > pasa::kTileRows) return PASA_ERR_UNSUPPORTED;
+  int sp = 1;
+  const int bps = decode_split(B, Hkv, Sk, D, splits, &sp);
+  if (bps > 0 && !decode_cluster_merge(D, static_cast<long long>(Hq / Hkv) * Sq, sp)) {
+    if (!workspace || workspace_bytes < pasa_attn_fwd_decode_workspace_bytes(B, Hq, Hkv, Sq, Sk, D, splits))
+      return PASA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PASA_ERR_ALIGN;
+  }
+  rc = pasa_kshift_blocks(k, k_shifted, means, B, Hkv, Sk, Sk_cap, D, first_block, stream);
+  if (rc != PASA_OK) return rc;
+  return decode_impl(q, k_shifted, means, nullptr, v, o, lse, B, Hq, Hkv, Sq, Sk, Sk_cap, D, causal, scale, mode,
+                     splits, workspace, workspace_bytes, stream, first_block);
 }
 
 int pasa_attn_fwd_decode_fp8(const void* q, const void* k8, const void* means, const float* kscale, const void* v,

@@ -115,6 +115,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// Programmatic dependent launch (PTX griddepcontrol). A kernel launched with programmatic
+// stream serialization may start before the kernel ahead of it on the stream has finished:
+// griddep_wait() returns once that kernel has completed and its writes are visible (at once
+// when the launch has no such predecessor), and griddep_launch_dependents() lets a kernel
+// queued behind this one start early (no effect when there is none).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------------------
 // TMA (tiled tensor copies). No multicast anywhere in this library.
 // ---------------------------------------------------------------------------------------

@@ -184,6 +184,31 @@ def test_decode_entry_points_check_arguments(lib):
     assert kb(P(FAKE), P(FAKE_MIS), P(FAKE), 1, 1, 300, 300, 128, 0, None) == -4
 
 
+def test_decode_step_checks_arguments(lib):
+    """pasa_attn_fwd_decode_step checks the arguments of both of its calls before it enqueues
+    anything (nothing here reaches a device)."""
+    P = ctypes.c_void_p
+
+    # pasa_attn_fwd_decode_step(q, k, k_shifted, means, v, o, lse, B, Hq, Hkv, Sq, Sk, Sk_cap, D, causal,
+    #                           scale, mode, first_block, splits, workspace, workspace_bytes, stream)
+    def step(k=FAKE, means=FAKE, Sk=5000, cap=5000, D=128, mode=0, first=39, splits=0, ws=None, ws_bytes=0):
+        return lib.pasa_attn_fwd_decode_step(P(FAKE), P(k) if k else None, P(FAKE), P(means) if means else None,
+                                             P(FAKE), P(FAKE), P(FAKE), 1, 8, 1, 1, Sk, cap, D, 1, 0.0, mode, first,
+                                             splits, P(ws) if ws else None, ws_bytes, None)
+
+    assert step(k=0) == -1                     # the refresh reads the raw cache
+    assert step(k=FAKE_MIS) == -4
+    assert step(means=0) == -1 and step(means=FAKE_MIS) == -4
+    assert step(mode=5) == -3 and step(mode=6) == -3   # e4m3 caches: kprep_fp8_blocks + decode_fp8
+    assert step(first=40) == -2 and step(first=-1) == -2   # 5000 keys: blocks 0..39
+    assert step(cap=4999) == -2
+    assert step(D=96) == -3
+    assert step(splits=-1) == -3
+    need = lib.pasa_attn_fwd_decode_workspace_bytes(1, 8, 1, 1, 5000, 128, 10)
+    assert step(splits=10, ws=FAKE, ws_bytes=need - 1) == -7
+    assert step(splits=10, ws=FAKE + 16, ws_bytes=need) == -4
+
+
 def test_decode_workspace_bytes(lib):
     # split choice: `splits` if given, else at most one CTA per SM (152) over the B * Hkv
     # kv heads and at least eight key blocks per split; blocks spread evenly; no workspace

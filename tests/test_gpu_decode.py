@@ -247,3 +247,76 @@ def test_full_size_decode():
             continue   # as in the prefill full-size tests: reported only on biased heavy-tailed keys
         assert rmse <= 5e-3, (mode, rmse, rmax)
         assert np.abs(lse.double().cpu().numpy() - lse_ref).max() <= lse_tolerance(q, k, True, mode, D)
+
+
+STEP_CASES = [
+    # (B, Hq, Hkv, Sq, Sk, cap, D, splits): the swapped-operand kernel with the in-cluster
+    # merge, one split, the workspace merge (> 8 splits), 32 packed rows, and the attention
+    # kernel on packed rows (D = 64; 48 rows)
+    (2, 28, 4, 1, 5000, 5120, 128, 0),
+    (1, 8, 2, 2, 1100, 1280, 128, 1),
+    (1, 4, 1, 1, 9000, 9216, 128, 12),
+    (2, 16, 2, 4, 3000, 3072, 128, 0),
+    (1, 8, 2, 1, 2000, 2048, 64, 0),
+    (1, 24, 2, 4, 700, 768, 128, 0),
+]
+
+
+@pytest.mark.parametrize("mode", [0, 1, 4, 2])
+@pytest.mark.parametrize("case", range(len(STEP_CASES)))
+def test_decode_step_equals_refresh_then_decode(case, mode):
+    """pasa_attn_fwd_decode_step after an append (the last block rewritten in the raw cache)
+    gives the shifted cache, the means, O and the LSE of pasa_kshift_blocks followed by
+    pasa_attn_fwd_decode, bit for bit; its decode kernel overlaps the refresh and waits for
+    it only before the refreshed blocks."""
+    p = pasa()
+    B, Hq, Hkv, Sq, Sk, cap, D, splits = STEP_CASES[case]
+    q, k, v = inputs(B, Hq, Hkv, Sq, cap, D, "kbias_t3", 300 + case, bias_std=10.0, t_dof=3, t_scale=4.0)
+    qt, kt, vt = to_dev(q, k, v)
+    nbc = -(-cap // BN)
+    first = (Sk - Sq) // BN   # the block the Sq appended rows start in
+    caches = []
+    for _ in range(2):
+        ks = torch.zeros_like(kt)
+        m = torch.zeros((B, Hkv, nbc, D), device="cuda", dtype=torch.float16)
+        p.kshift_blocks(kt, ks, m, 0, length=Sk - Sq)   # the cache before the append
+        caches.append((ks, m))
+    (ka, ma), (kb, mb) = caches
+    shift = mode in (0, 1, 4)
+    if shift:
+        p.kshift_blocks(kt, ka, ma, first, length=Sk)
+    o_a, l_a = p.attn_fwd_decode(qt, ka if shift else kt, ma if shift else None, vt, causal=True, mode=mode,
+                                 splits=splits, length=Sk)
+    o_b, l_b = p.attn_fwd_decode_step(qt, kt, kb if shift else kt, mb if shift else None, vt, first, causal=True,
+                                      mode=mode, splits=splits, length=Sk)
+    torch.cuda.synchronize()
+    p.check_device_error()
+    assert torch.equal(o_a, o_b) and torch.equal(l_a, l_b)
+    if shift:
+        assert torch.equal(ka, kb) and torch.equal(ma, mb)
+
+
+def test_decode_step_loop_against_the_oracle():
+    """Decode steps through pasa_attn_fwd_decode_step, each appending one key/value row per
+    head: checked against the fp64 oracle at every step."""
+    p = pasa()
+    B, Hq, Hkv, D, S0, steps, cap = 2, 28, 4, 128, 4090, 8, 4224
+    q, k, v = inputs(B, Hq, Hkv, steps, S0 + steps, D, "kbias", 124, bias_std=20.0)
+    (kt, vt) = to_dev(k, v)
+    kc = torch.zeros((B, Hkv, cap, D), device="cuda", dtype=torch.float16)
+    vc = torch.zeros_like(kc)
+    ksc = torch.zeros_like(kc)
+    mc = torch.zeros((B, Hkv, cap // BN, D), device="cuda", dtype=torch.float16)
+    kc[:, :, :S0], vc[:, :, :S0] = kt[:, :, :S0], vt[:, :, :S0]
+    p.kshift_blocks(kc, ksc, mc, 0, length=S0)
+    for t in range(steps):
+        Sk = S0 + t + 1
+        kc[:, :, Sk - 1], vc[:, :, Sk - 1] = kt[:, :, Sk - 1], vt[:, :, Sk - 1]
+        qs = np.ascontiguousarray(q[:, :, t:t + 1])
+        (qt,) = to_dev(qs)
+        o, lse = p.attn_fwd_decode_step(qt, kc, ksc, mc, vc, (Sk - 1) // BN, causal=True, mode=0, length=Sk)
+        p.check_device_error()
+        o_ref, lse_ref = oracle.attention(qs, k[:, :, :Sk], v[:, :, :Sk], causal=True)
+        rmse, rmax = rel_errors(o.double().cpu().numpy(), o_ref)
+        assert rmse <= 5e-3 and rmax <= 5e-2, (t, rmse, rmax)
+        assert np.abs(lse.double().cpu().numpy() - lse_ref).max() <= lse_tolerance(qs, k[:, :, :Sk], True, 0, D)
