@@ -65,9 +65,9 @@ TRAFFIC_MODE = 0
 TRAFFIC_BYTES = 692542208 + 199207936
 TRAFFIC_KERNEL_SHA = "00961d8215c83675"
 # The same for one decode-kernel launch on the decode workload (an ncu capture at full
-# size: 539.11 MB read + 3.17 MB written).
-DECODE_TRAFFIC_BYTES = 539113472 + 3172608
-DECODE_TRAFFIC_SHA = "ca888b56aee96d33"
+# size: 539.11 MB read + 2.97 MB written).
+DECODE_TRAFFIC_BYTES = 539112960 + 2970368
+DECODE_TRAFFIC_SHA = "0ff35ca3bb268cac"
 
 
 def _source_sha(name):
