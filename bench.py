@@ -373,11 +373,11 @@ def bench_gpu(args, w: wl.Workload, rank: int, world: int, local_rank: int, also
 
 
 def bench_decode(args, w: wl.Workload, local_rank: int, sampler=None):
-    """One decode step: refresh the shifted cache's last block (where the new key row lands)
-    and attend (decode kernel + split merge). The fp16 shifted cache takes both in one call,
-    pasa_attn_fwd_decode_step, whose decode kernel overlaps the refresh; the e4m3 cache
-    calls pasa_kprep_fp8_blocks, then pasa_attn_fwd_decode_fp8. attn_ms times the attend
-    call alone. The cache is shifted once before timing, as a prefill would leave it."""
+    """One decode step: refresh the cache's last block (where the new key row lands) and
+    attend (decode kernel + split merge), in one call (pasa_attn_fwd_decode_step, or
+    _step_fp8 for the e4m3 cache), whose decode kernel overlaps the refresh. attn_ms times
+    the attend call alone. The cache is prepared once before timing, as a prefill would
+    leave it."""
     import torch
 
     import precision_flashattention_numerics_gb300 as pasa
@@ -401,12 +401,6 @@ def bench_decode(args, w: wl.Workload, local_rank: int, sampler=None):
     last = (w.Sk - 1) // bn
     stream = torch.cuda.current_stream()
 
-    def refresh():
-        if fp8:
-            pasa.kprep_fp8_blocks(kt, ks, means, kscale, last, mode=mode)
-        elif shift:
-            pasa.kshift_blocks(kt, ks, means, last)
-
     def attend():
         if fp8:
             pasa.attn_fwd_decode_fp8(qt, ks, means, kscale, vt, causal=w.causal, mode=mode, out=o, lse=lse,
@@ -414,15 +408,14 @@ def bench_decode(args, w: wl.Workload, local_rank: int, sampler=None):
         else:
             pasa.attn_fwd_decode(qt, ks, means, vt, causal=w.causal, mode=mode, out=o, lse=lse, workspace=ws)
 
-    combined = shift and not fp8   # one call: pasa_attn_fwd_decode_step (the decode kernel overlaps the refresh)
-
     def step():
-        if combined:
+        # one call: refresh and decode, the decode kernel overlapping the refresh
+        if fp8:
+            pasa.attn_fwd_decode_step_fp8(qt, kt, ks, means, kscale, vt, last, causal=w.causal, mode=mode, out=o,
+                                          lse=lse, workspace=ws)
+        else:
             pasa.attn_fwd_decode_step(qt, kt, ks, means, vt, last, causal=w.causal, mode=mode, out=o, lse=lse,
                                       workspace=ws)
-        else:
-            refresh()
-            attend()
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -466,7 +459,7 @@ def bench_decode(args, w: wl.Workload, local_rank: int, sampler=None):
         "attn_bytes": moved, "attn_gbs": round(gbs, 1), "finite": bool(torch.isfinite(o).all().item()),
         "launches_per_step": (1 if (shift or fp8) else 0) + (2 if nbytes else 1),
         "merge": "combine_splits_kernel" if nbytes else "in the decode kernel (thread-block cluster)",
-        "step_call": "pasa_attn_fwd_decode_step" if combined else "refresh, then attend",
+        "step_call": "pasa_attn_fwd_decode_step_fp8" if fp8 else "pasa_attn_fwd_decode_step",
     }
 
 

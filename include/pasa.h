@@ -393,8 +393,8 @@ int pasa_attn_fwd_decode(const void* q, const void* k_shifted, const void* means
  *   k          the raw fp16 key cache [B, Hkv, Sk_cap, D] the refresh reads
  *   k_shifted, means   the shifted cache and its block means, rewritten from first_block on
  *   other arguments as pasa_attn_fwd_decode; modes 2 and 3 (no shifted cache) only run
- *   the decode, and the FP8 modes are PASA_ERR_UNSUPPORTED (pasa_kprep_fp8_blocks and
- *   pasa_attn_fwd_decode_fp8 cover them). Errors: as the two calls; all arguments are
+ *   the decode, and the FP8 modes are PASA_ERR_UNSUPPORTED (pasa_attn_fwd_decode_step_fp8
+ *   covers them). Errors: as the two calls; all arguments are
  *   checked before anything is enqueued.
  */
 int pasa_attn_fwd_decode_step(const void* q, const void* k, void* k_shifted, void* means, const void* v, void* o,
@@ -417,6 +417,18 @@ int pasa_attn_fwd_decode_step(const void* q, const void* k, void* k_shifted, voi
 int pasa_attn_fwd_decode_fp8(const void* q, const void* k8, const void* means, const float* kscale, const void* v,
                              void* o, float* lse, int B, int Hq, int Hkv, int Sq, int Sk, int Sk_cap, int D, int causal,
                              float scale, int mode, int splits, void* workspace, size_t workspace_bytes, void* stream);
+
+/* One decode step on an e4m3 key cache: pasa_kprep_fp8_blocks(k, k8, means, kscale, B, Hkv,
+ * Sk, Sk_cap, D, mode, first_block) followed by pasa_attn_fwd_decode_fp8 on the refreshed
+ * cache, in one call, with the schedule of pasa_attn_fwd_decode_step (the decode kernel
+ * overlaps the refresh and waits for it only before the refreshed blocks, their codes,
+ * means and scales). Bit-identical to the two calls. Modes 5 and 6 only (other modes:
+ * PASA_ERR_UNSUPPORTED); D = 128 with at most 32 packed rows, as pasa_attn_fwd_decode_fp8.
+ * Errors: as the two calls, all checked before anything is enqueued. */
+int pasa_attn_fwd_decode_step_fp8(const void* q, const void* k, void* k8, void* means, float* kscale, const void* v,
+                                  void* o, float* lse, int B, int Hq, int Hkv, int Sq, int Sk, int Sk_cap, int D,
+                                  int causal, float scale, int mode, int first_block, int splits, void* workspace,
+                                  size_t workspace_bytes, void* stream);
 
 /*
  * pasa_kprep_fp8 for key blocks [first_block, ceil(Sk / 128)) of a cache of Sk valid keys in

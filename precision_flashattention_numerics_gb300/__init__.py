@@ -56,6 +56,7 @@ SIGNATURES = {
     "pasa_attn_fwd_decode_workspace_bytes": ([_I, _I, _I, _I, _I, _I, _I], _SZ),
     "pasa_attn_fwd_decode": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P], _I),
     "pasa_attn_fwd_decode_step": ([_P, _P, _P, _P, _P, _P, _P] + [_I] * 8 + [_F, _I, _I, _I, _P, _SZ, _P], _I),
+    "pasa_attn_fwd_decode_step_fp8": ([_P] * 8 + [_I] * 8 + [_F, _I, _I, _I, _P, _SZ, _P], _I),
     "pasa_attn_fwd_decode_fp8": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P],
                                  _I),
     "pasa_kprep_fp8_blocks": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P], _I),
@@ -437,6 +438,31 @@ def attn_fwd_decode_step(q, k, k_shifted, means, v, first_block: int, causal: bo
                                        int(splits), _ptr(workspace) if nbytes else None, nbytes, _stream())
     if rc != 0:
         raise PasaError(rc, "pasa_attn_fwd_decode_step")
+    return out, lse
+
+
+def attn_fwd_decode_step_fp8(q, k, k8, means, kscale, v, first_block: int, causal: bool = False,
+                             scale: float | None = None, mode: int = MODE_SHIFT_FP8, splits: int = 0, out=None,
+                             lse=None, workspace=None, length: int | None = None):
+    """pasa_attn_fwd_decode_step_fp8: refresh key blocks first_block.. of the e4m3 cache (k8,
+    means, kscale) from the raw cache k, then decode on it, in one call. Returns (o, lse)."""
+    lib = library()
+    _check(q, "q"), _check(k, "k"), _check(v, "v")
+    B, Hq, Sq, D = q.shape
+    _, Hkv, cap, _ = k8.shape
+    Sk = cap if length is None else int(length)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, Hq, Sq), device=q.device, dtype=torch.float32) if lse is None else lse
+    nbytes = lib.pasa_attn_fwd_decode_workspace_bytes(B, Hq, Hkv, Sq, Sk, D, int(splits))
+    if nbytes and (workspace is None or workspace.numel() * workspace.element_size() < nbytes):
+        workspace = torch.empty(nbytes, device=q.device, dtype=torch.uint8)
+    rc = lib.pasa_attn_fwd_decode_step_fp8(_ptr(q), _ptr(k), _ptr(k8), _ptr(means) if means is not None else None,
+                                           _ptr(kscale), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Sk, cap, D,
+                                           int(bool(causal)), float(scale) if scale is not None else 0.0, int(mode),
+                                           int(first_block), int(splits), _ptr(workspace) if nbytes else None, nbytes,
+                                           _stream())
+    if rc != 0:
+        raise PasaError(rc, "pasa_attn_fwd_decode_step_fp8")
     return out, lse
 
 

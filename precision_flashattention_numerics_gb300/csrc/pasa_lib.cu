@@ -723,6 +723,33 @@ int pasa_attn_fwd_decode_step(const void* q, const void* k, void* k_shifted, voi
                      splits, workspace, workspace_bytes, stream, first_block);
 }
 
+int pasa_attn_fwd_decode_step_fp8(const void* q, const void* k, void* k8, void* means, float* kscale, const void* v,
+                                  void* o, float* lse, int B, int Hq, int Hkv, int Sq, int Sk, int Sk_cap, int D,
+                                  int causal, float scale, int mode, int first_block, int splits, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  if (!fp8_mode(mode)) return PASA_ERR_UNSUPPORTED;   // fp16 caches: pasa_attn_fwd_decode_step
+  // argument checks of both calls before anything is enqueued
+  if (!k || !kscale || (mode == PASA_MODE_SHIFT_FP8 && !means)) return PASA_ERR_NULLPTR;
+  if (!aligned16(k) || !aligned16(kscale) || (means && !aligned16(means))) return PASA_ERR_ALIGN;
+  int rc = validate(q, k8, v, o, lse, B, Hq, Hkv, Sq, Sk, D, mode);
+  if (rc != PASA_OK) return rc;
+  if (D != 128 || static_cast<long long>(Hq / Hkv) * Sq > 32) return PASA_ERR_UNSUPPORTED;
+  if (Sk_cap < Sk || splits < 0) return Sk_cap < Sk ? PASA_ERR_SHAPE : PASA_ERR_UNSUPPORTED;
+  const int nb = (Sk + 127) / 128;
+  if (first_block < 0 || first_block >= nb || static_cast<long long>(B) * Hkv > 65535) return PASA_ERR_SHAPE;
+  int sp = 1;
+  const int bps = decode_split(B, Hkv, Sk, D, splits, &sp);
+  if (bps > 0 && !decode_cluster_merge(D, static_cast<long long>(Hq / Hkv) * Sq, sp)) {
+    if (!workspace || workspace_bytes < pasa_attn_fwd_decode_workspace_bytes(B, Hq, Hkv, Sq, Sk, D, splits))
+      return PASA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PASA_ERR_ALIGN;
+  }
+  rc = pasa_kprep_fp8_blocks(k, k8, means, kscale, B, Hkv, Sk, Sk_cap, D, mode, first_block, stream);
+  if (rc != PASA_OK) return rc;
+  return decode_impl(q, k8, means, kscale, v, o, lse, B, Hq, Hkv, Sq, Sk, Sk_cap, D, causal, scale, mode, splits,
+                     workspace, workspace_bytes, stream, first_block);
+}
+
 int pasa_attn_fwd_decode_fp8(const void* q, const void* k8, const void* means, const float* kscale, const void* v,
                              void* o, float* lse, int B, int Hq, int Hkv, int Sq, int Sk, int Sk_cap, int D, int causal,
                              float scale, int mode, int splits, void* workspace, size_t workspace_bytes, void* stream) {

@@ -209,6 +209,25 @@ def test_decode_step_checks_arguments(lib):
     assert step(splits=10, ws=FAKE + 16, ws_bytes=need) == -4
 
 
+def test_decode_step_fp8_checks_arguments(lib):
+    P = ctypes.c_void_p
+
+    # pasa_attn_fwd_decode_step_fp8(q, k, k8, means, kscale, v, o, lse, B, Hq, Hkv, Sq, Sk, Sk_cap, D,
+    #                               causal, scale, mode, first_block, splits, workspace, workspace_bytes, stream)
+    def step(k=FAKE, means=FAKE, kscale=FAKE, Sq=1, Sk=5000, D=128, mode=5, first=39):
+        return lib.pasa_attn_fwd_decode_step_fp8(P(FAKE), P(k) if k else None, P(FAKE), P(means) if means else None,
+                                                 P(kscale) if kscale else None, P(FAKE), P(FAKE), P(FAKE), 1, 8, 1,
+                                                 Sq, Sk, Sk, D, 1, 0.0, mode, first, 0, None, 0, None)
+
+    assert step(mode=0) == -3 and step(mode=3) == -3   # fp16 caches: pasa_attn_fwd_decode_step
+    assert step(k=0) == -1 and step(kscale=0) == -1
+    assert step(means=0) == -1                          # mode 5 keeps block means
+    assert step(k=FAKE_MIS) == -4 and step(kscale=FAKE_MIS) == -4
+    assert step(D=64) == -3
+    assert step(Sq=5) == -3                             # 40 packed rows: beyond the decode kernel
+    assert step(first=40) == -2 and step(first=-1) == -2
+
+
 def test_decode_workspace_bytes(lib):
     # split choice: `splits` if given, else at most one CTA per SM (152) over the B * Hkv
     # kv heads and at least eight key blocks per split; blocks spread evenly; no workspace

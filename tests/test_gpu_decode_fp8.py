@@ -151,3 +151,43 @@ def test_shift_makes_fp8_decode_usable_on_biased_keys():
         err[mode] = rel_errors(o.double().cpu().numpy(), o_ref)[0]
     print(f"\ndecode relRMSE vs plain attention: FP8 PASA {err[5]:.3e}, FP8 naive {err[6]:.3e}")
     assert err[5] < err[6] / 3, err
+
+
+STEP_CASES = [
+    # (B, Hq, Hkv, Sq, Sk, cap, splits): cluster merge, one split, the workspace merge, 32 rows
+    (2, 28, 4, 1, 5000, 5120, 0),
+    (1, 8, 2, 2, 1100, 1280, 1),
+    (1, 4, 1, 1, 9000, 9216, 12),
+    (2, 16, 2, 4, 3000, 3072, 0),
+]
+
+
+@pytest.mark.parametrize("mode", [5, 6])
+@pytest.mark.parametrize("case", range(len(STEP_CASES)))
+def test_decode_step_fp8_equals_refresh_then_decode(case, mode):
+    """pasa_attn_fwd_decode_step_fp8 after an append gives the codes, block scales, means, O
+    and LSE of pasa_kprep_fp8_blocks followed by pasa_attn_fwd_decode_fp8, bit for bit."""
+    p = pasa()
+    B, Hq, Hkv, Sq, Sk, cap, splits = STEP_CASES[case]
+    q, k, v = inputs(B, Hq, Hkv, Sq, cap, "kbias_t3", 400 + case, bias_std=10.0, t_dof=3, t_scale=4.0)
+    qt, kt, vt = to_dev(q, k, v)
+    nbc = -(-cap // BN)
+    first = (Sk - Sq) // BN
+    caches = []
+    for _ in range(2):
+        k8 = torch.zeros((B, Hkv, cap, 128), device="cuda", dtype=torch.uint8)
+        ks = torch.zeros((B, Hkv, nbc), device="cuda", dtype=torch.float32)
+        mc = torch.zeros((B, Hkv, nbc, 128), device="cuda", dtype=torch.float16) if mode == 5 else None
+        p.kprep_fp8_blocks(kt, k8, mc, ks, 0, mode=mode, length=Sk - Sq)   # before the append
+        caches.append((k8, mc, ks))
+    (k8a, ma, sa), (k8b, mb, sb) = caches
+    p.kprep_fp8_blocks(kt, k8a, ma, sa, first, mode=mode, length=Sk)
+    o_a, l_a = p.attn_fwd_decode_fp8(qt, k8a, ma, sa, vt, causal=True, mode=mode, splits=splits, length=Sk)
+    o_b, l_b = p.attn_fwd_decode_step_fp8(qt, kt, k8b, mb, sb, vt, first, causal=True, mode=mode, splits=splits,
+                                          length=Sk)
+    torch.cuda.synchronize()
+    p.check_device_error()
+    assert torch.equal(o_a, o_b) and torch.equal(l_a, l_b)
+    assert torch.equal(k8a, k8b) and torch.equal(sa, sb)
+    if mode == 5:
+        assert torch.equal(ma, mb)
