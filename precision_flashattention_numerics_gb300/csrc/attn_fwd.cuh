@@ -366,6 +366,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         v_issued = j + 1;
         return true;
       };
+      // The keys and means may come from the shift kernel queued just ahead of this launch
+      // (launched with programmatic dependence on it): wait for it before the first load of
+      // either. Q is not written by it and is already on its way.
+      griddep_wait();
       bool pok = nblk == 0 || load_k(0);
       for (int j = 0; pok && j < nblk; ++j) {
         if (j + 1 < nblk && !load_k(j + 1)) break;
@@ -677,6 +681,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     const float* kscale_row = FP8 ? p.kscale + static_cast<size_t>(b * p.Hkv + hk) * p.nbt : nullptr;
     float sk_next = 1.0f;
     if constexpr (FP8) {
+      griddep_wait();   // the block scales come from the key preparation queued just ahead
       if (nblk > 0) sk_next = __ldg(kscale_row + jb0);
       if (!mbar_wait(&s.q_full, 0, abort_flag, 0x340)) ok = false;
       uint4 qrow[D / 8];

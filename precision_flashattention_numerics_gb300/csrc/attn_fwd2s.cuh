@@ -255,6 +255,10 @@ attn_fwd_2set_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_cons
         v_issued = j + 1;
         return true;
       };
+      // The keys and means may come from the shift kernel queued just ahead of this launch
+      // (launched with programmatic dependence on it): wait for it before the first load of
+      // either. Q is not written by it and is already on its way.
+      griddep_wait();
       bool pok = nblk == 0 || load_k(0);
       for (int j = 0; pok && j < nblk; ++j) {
         if (j + 1 < nblk && !load_k(j + 1)) break;

@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <utility>
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -172,9 +173,30 @@ int kshift_dispatch(const void* k, void* ks, void* means, float* kscale, int B, 
                  : launch_kshift<128, pasa::kShiftF16>(k, ks, means, nullptr, B, H, Sk, st, first_block, cap);
 }
 
+// Launch `kern` on `st`; with pdl, by programmatic stream serialization: the kernel may start
+// while the kernel queued just ahead of it (the key preparation of the same call) still
+// runs, and waits for it with griddep_wait() before reading what it writes.
+template <typename... Params, typename... Args>
+cudaError_t launch_kernel(void (*kern)(Params...), dim3 grid, dim3 block, int smem, cudaStream_t st, bool pdl,
+                          Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  if (pdl) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 template <int D, bool F16ACC, bool SHIFT, bool CAUSAL, bool STATS, bool F16PV = false, bool FP8 = false>
 int launch_attn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mo,
-                const CUtensorMap& mm, const pasa::AttnParams& p, cudaStream_t st) {
+                const CUtensorMap& mm, const pasa::AttnParams& p, cudaStream_t st, bool pdl = false) {
   constexpr int BN = pasa::block_rows_for(D);
   // ring slots: D = 128 fp16 keys: 3 K + 2 V (201 KB of shared memory); e4m3 keys: 4 + 3
   constexpr int KST = D == 128 ? (FP8 ? 4 : 3) : 4;
@@ -186,8 +208,9 @@ int launch_attn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap&
   if (e != cudaSuccess) return cuda_fail(e);
   const long long ctas = static_cast<long long>(p.n_qblk) * p.Hq * p.B;
   const unsigned splits = p.bps > 0 ? static_cast<unsigned>((p.nbt + p.bps - 1) / p.bps) : 1u;
-  kern<<<dim3(static_cast<unsigned>(ctas), splits), pasa::kAttnThreads, smem, st>>>(mq, mk, mv, mo, mm, p);
-  e = cudaGetLastError();
+  e = launch_kernel(kern, dim3(static_cast<unsigned>(ctas), splits), dim3(pasa::kAttnThreads), smem, st, pdl, mq, mk, mv,
+                    mo, mm, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? PASA_OK : cuda_fail(e);
 }
 
@@ -209,27 +232,28 @@ int launch_attn_fused(const CUtensorMap& mq, const CUtensorMap& mk, const CUtens
 
 template <int D, bool STATS>
 int attn_dispatch(int mode, int causal, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                  const CUtensorMap& mo, const CUtensorMap& mm, const pasa::AttnParams& p, cudaStream_t st) {
+                  const CUtensorMap& mo, const CUtensorMap& mm, const pasa::AttnParams& p, cudaStream_t st,
+                  bool pdl = false) {
 #define PASA_CASE(MODE, F16, SH)                                                        \
   case MODE:                                                                            \
-    return causal ? launch_attn<D, F16, SH, true, STATS>(mq, mk, mv, mo, mm, p, st)     \
-                  : launch_attn<D, F16, SH, false, STATS>(mq, mk, mv, mo, mm, p, st);
+    return causal ? launch_attn<D, F16, SH, true, STATS>(mq, mk, mv, mo, mm, p, st, pdl)     \
+                  : launch_attn<D, F16, SH, false, STATS>(mq, mk, mv, mo, mm, p, st, pdl);
   switch (mode) {
     PASA_CASE(PASA_MODE_SHIFT_F16ACC, true, true)
     PASA_CASE(PASA_MODE_SHIFT_F32ACC, false, true)
     PASA_CASE(PASA_MODE_NAIVE_F16ACC, true, false)
     PASA_CASE(PASA_MODE_NOSHIFT_F32ACC, false, false)
     case PASA_MODE_SHIFT_F16ALL:
-      return causal ? launch_attn<D, true, true, true, STATS, true>(mq, mk, mv, mo, mm, p, st)
-                    : launch_attn<D, true, true, false, STATS, true>(mq, mk, mv, mo, mm, p, st);
+      return causal ? launch_attn<D, true, true, true, STATS, true>(mq, mk, mv, mo, mm, p, st, pdl)
+                    : launch_attn<D, true, true, false, STATS, true>(mq, mk, mv, mo, mm, p, st, pdl);
     case PASA_MODE_SHIFT_FP8:
     case PASA_MODE_NAIVE_FP8:
       if constexpr (D == 128 && !STATS) {
         if (mode == PASA_MODE_SHIFT_FP8)
-          return causal ? launch_attn<D, false, true, true, false, false, true>(mq, mk, mv, mo, mm, p, st)
-                        : launch_attn<D, false, true, false, false, false, true>(mq, mk, mv, mo, mm, p, st);
-        return causal ? launch_attn<D, false, false, true, false, false, true>(mq, mk, mv, mo, mm, p, st)
-                      : launch_attn<D, false, false, false, false, false, true>(mq, mk, mv, mo, mm, p, st);
+          return causal ? launch_attn<D, false, true, true, false, false, true>(mq, mk, mv, mo, mm, p, st, pdl)
+                        : launch_attn<D, false, true, false, false, false, true>(mq, mk, mv, mo, mm, p, st, pdl);
+        return causal ? launch_attn<D, false, false, true, false, false, true>(mq, mk, mv, mo, mm, p, st, pdl)
+                      : launch_attn<D, false, false, false, false, false, true>(mq, mk, mv, mo, mm, p, st, pdl);
       }
       return PASA_ERR_UNSUPPORTED;
     default:
@@ -264,24 +288,26 @@ int validate(const void* q, const void* k, const void* v, const void* o, const f
 // D = 64 prefill, modes 0-3: two softmax warp sets on alternate key blocks.
 template <bool F16ACC, bool SHIFT, bool CAUSAL>
 int launch_2set(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mo,
-                const CUtensorMap& mm, const pasa::AttnParams& p, cudaStream_t st) {
+                const CUtensorMap& mm, const pasa::AttnParams& p, cudaStream_t st, bool pdl = false) {
   constexpr int KST = 4, VST = 4;
   auto kern = pasa::twoset::attn_fwd_2set_kernel<64, 128, F16ACC, SHIFT, CAUSAL, KST, VST, false>;
   const int smem = static_cast<int>(sizeof(pasa::twoset::AttnSmem<64, 128, KST, VST>)) + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e);
   const long long ctas = static_cast<long long>(p.n_qblk) * p.Hq * p.B;
-  kern<<<static_cast<unsigned>(ctas), pasa::twoset::kAttnThreads, smem, st>>>(mq, mk, mv, mo, mm, p);
-  e = cudaGetLastError();
+  e = launch_kernel(kern, dim3(static_cast<unsigned>(ctas)), dim3(pasa::twoset::kAttnThreads), smem, st, pdl, mq, mk,
+                    mv, mo, mm, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? PASA_OK : cuda_fail(e);
 }
 
 int twoset_dispatch(int mode, int causal, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                    const CUtensorMap& mo, const CUtensorMap& mm, const pasa::AttnParams& p, cudaStream_t st) {
+                    const CUtensorMap& mo, const CUtensorMap& mm, const pasa::AttnParams& p, cudaStream_t st,
+                    bool pdl = false) {
 #define PASA_2S_CASE(MODE, F16, SH)                                                   \
   case MODE:                                                                          \
-    return causal ? launch_2set<F16, SH, true>(mq, mk, mv, mo, mm, p, st)             \
-                  : launch_2set<F16, SH, false>(mq, mk, mv, mo, mm, p, st);
+    return causal ? launch_2set<F16, SH, true>(mq, mk, mv, mo, mm, p, st, pdl)        \
+                  : launch_2set<F16, SH, false>(mq, mk, mv, mo, mm, p, st, pdl);
   switch (mode) {
     PASA_2S_CASE(PASA_MODE_SHIFT_F16ACC, true, true)
     PASA_2S_CASE(PASA_MODE_SHIFT_F32ACC, false, true)
@@ -451,9 +477,12 @@ int pasa_kshift_blocks(const void* k, void* k_shifted, void* means, int B, int H
 }
 
 // Launch the attention kernel on (possibly shifted) keys `kk` and block means `mm`.
+// pdl: the key preparation of the same call was launched just before on `st` (see
+// launch_kernel); never with the diagnostic outputs, whose zeroing sits in between.
 static int attn_launch(const void* q, const void* kk, const void* mm, const void* v, void* o, float* lse, int B,
                        int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale, int mode, cudaStream_t st,
-                       float* stats = nullptr, float* block_stats = nullptr, const float* kscale = nullptr) {
+                       float* stats = nullptr, float* block_stats = nullptr, const float* kscale = nullptr,
+                       bool pdl = false) {
   const bool shift = shift_mode(mode);
   if (!(scale > 0.0f) || !std::isfinite(scale)) scale = 1.0f / std::sqrt(static_cast<float>(D));
   const int bn = pasa::block_rows_for(D);
@@ -499,9 +528,9 @@ static int attn_launch(const void* q, const void* kk, const void* mm, const void
     return D == 64 ? attn_dispatch<64, true>(mode, causal, mq, mk, mv, mo, mmeans, p, st)
                    : attn_dispatch<128, true>(mode, causal, mq, mk, mv, mo, mmeans, p, st);
   if (D == 64 && mode <= PASA_MODE_NOSHIFT_F32ACC)
-    return twoset_dispatch(mode, causal, mq, mk, mv, mo, mmeans, p, st);
-  return D == 64 ? attn_dispatch<64, false>(mode, causal, mq, mk, mv, mo, mmeans, p, st)
-                 : attn_dispatch<128, false>(mode, causal, mq, mk, mv, mo, mmeans, p, st);
+    return twoset_dispatch(mode, causal, mq, mk, mv, mo, mmeans, p, st, pdl);
+  return D == 64 ? attn_dispatch<64, false>(mode, causal, mq, mk, mv, mo, mmeans, p, st, pdl)
+                 : attn_dispatch<128, false>(mode, causal, mq, mk, mv, mo, mmeans, p, st, pdl);
 }
 
 int pasa_attn_fwd_shifted(const void* q, const void* k_shifted, const void* means, const void* v, void* o,
@@ -803,7 +832,8 @@ int pasa_attn_fwd_ws(const void* q, const void* k, const void* v, void* o, float
     kk = ks;
     mm = means;
   }
-  return attn_launch(q, kk, mm, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, mode, st, nullptr, nullptr, kscale);
+  return attn_launch(q, kk, mm, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, mode, st, nullptr, nullptr, kscale,
+                     prep);
 }
 
 int pasa_attn_fwd_stats(const void* q, const void* k, const void* v, void* o, float* lse, float* stats,

@@ -411,3 +411,30 @@ def test_random_sweep_against_oracle(case):
     else:
         assert rmse <= 2e-3 and rmax <= 1e-2, (rmse, rmax)
     assert np.max(np.abs(lg[fin] - lse_ref[fin])) <= lse_tolerance(q, k, causal, mode, D)
+
+
+@pytest.mark.parametrize("D,mode", [(128, 0), (128, 1), (128, 4), (128, 5), (64, 0), (64, 1)])
+def test_back_to_back_calls_share_a_workspace(D, mode):
+    """pasa_attn_fwd_ws launches the key preparation and then the attention kernel, which may
+    start before the preparation ends and waits for it (griddepcontrol) before reading the
+    prepared keys. Three calls on different inputs, queued without a host synchronisation
+    on one workspace, must each equal the preparation and the attention run as separate
+    calls on their own buffers, bit for bit: no call may read another's prepared keys."""
+    p = pasa()
+    B, Hq, Hkv, S = 1, 8, 2, 1500
+    ins = [to_dev(*wl.make_inputs(wl.Workload("ws", B, Hq, Hkv, S, S, D, True, "kbias", 900 + i,
+                                              (("bias_std", 10.0),)))) for i in range(3)]
+    ws = torch.empty(p.library().pasa_attn_fwd_workspace_bytes(B, Hkv, S, D, mode), device="cuda",
+                     dtype=torch.uint8)
+    outs = [p.attn_fwd(q, k, v, causal=True, mode=mode, workspace=ws) for (q, k, v) in ins]
+    torch.cuda.synchronize()
+    p.check_device_error()
+    for (q, k, v), (o, lse) in zip(ins, outs):
+        if mode == 5:
+            k8, means, kscale = p.kprep_fp8(k, mode=mode)
+            o_ref, lse_ref = p.attn_fwd_fp8(q, k8, means, kscale, v, causal=True, mode=mode)
+        else:
+            ks, means = p.kshift(k)
+            o_ref, lse_ref = p.attn_fwd_shifted(q, ks, means, v, causal=True, mode=mode)
+        torch.cuda.synchronize()
+        assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
