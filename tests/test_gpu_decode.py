@@ -320,3 +320,33 @@ def test_decode_step_loop_against_the_oracle():
         rmse, rmax = rel_errors(o.double().cpu().numpy(), o_ref)
         assert rmse <= 5e-3 and rmax <= 5e-2, (t, rmse, rmax)
         assert np.abs(lse.double().cpu().numpy() - lse_ref).max() <= lse_tolerance(qs, k[:, :, :Sk], True, 0, D)
+
+
+def test_decode_step_and_one_call_prefill_on_a_side_stream():
+    """The calls that launch a kernel with programmatic dependence on the key preparation
+    (the decode step; the one-call prefill) give the same results on a non-default stream
+    as the separate calls on the default one, with work queued on that stream around them."""
+    p = pasa()
+    B, Hq, Hkv, Sq, Sk, cap, D = 2, 28, 4, 1, 3000, 3072, 128
+    q, k, v = inputs(B, Hq, Hkv, Sq, cap, D, "kbias", 77, bias_std=20.0)
+    qt, kt, vt = to_dev(q, k, v)
+    first = (Sk - 1) // BN
+    ka, ma = torch.zeros_like(kt), torch.zeros((B, Hkv, cap // BN, D), device="cuda", dtype=torch.float16)
+    p.kshift_blocks(kt, ka, ma, 0, length=Sk)
+    o_a, l_a = p.attn_fwd_decode(qt, ka, ma, vt, causal=True, mode=0, length=Sk)
+    qp, kp, vp = to_dev(*inputs(1, 8, 2, 700, 700, D, "kbias", 78, bias_std=10.0))
+    ks, means = p.kshift(kp)
+    o_pa, l_pa = p.attn_fwd_shifted(qp, ks, means, vp, causal=True, mode=0)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        kb, mb = torch.zeros_like(kt), torch.zeros_like(ma)
+        p.kshift_blocks(kt, kb, mb, 0, length=Sk - 1)
+        o_b, l_b = p.attn_fwd_decode_step(qt, kt, kb, mb, vt, first, causal=True, mode=0, length=Sk)
+        o_pb, l_pb = p.attn_fwd(qp, kp, vp, causal=True, mode=0)
+        o_b2 = o_b.clone()   # stream-ordered after the step
+    side.synchronize()
+    p.check_device_error()
+    assert torch.equal(o_a, o_b) and torch.equal(l_a, l_b) and torch.equal(o_b2, o_a)
+    assert torch.equal(ka, kb) and torch.equal(ma, mb)
+    assert torch.equal(o_pa, o_pb) and torch.equal(l_pa, l_pb)
