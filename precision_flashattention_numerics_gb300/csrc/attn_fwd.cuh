@@ -891,9 +891,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
       // overlap it.
       if (j >= 1 && !mbar_wait(&s.p_free, (j - 1) & 1, abort_flag, 0x320)) { ok = false; break; }
       tc_fence_after();
+      // P first: its stores do not depend on the rescale, and their latency overlaps it
+#pragma unroll
+      for (int c = 0; c < BN / 16; ++c) tmem_st_x8(tP + c * 8, pk + c * 8);
       if (rescale) {
-        uint32_t w[16];
         if constexpr (F16PV) {
+          uint32_t w[16];
           const uint32_t a2 = pack_half2(alpha, alpha);
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
@@ -905,19 +908,27 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             tmem_st_x16_unpack16(tO + c * 32, w);
           }
         } else {
+          // 64 columns per load round: one wait per 64 (a heavy-tailed workload rescales
+          // in about a fifth of its warp-blocks, inside the softmax's chain)
 #pragma unroll
-          for (int c = 0; c < D / 16; ++c) {
-            tmem_ld_x16(tO + c * 16, w);
+          for (int b0 = 0; b0 < D; b0 += 64) {
+            uint32_t w[64];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld_x16(tO + b0 + c * 16, w + c * 16);
             tmem_ld_wait();
-            reg_fence<16>(w);
+            reg_fence<64>(w);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(__uint_as_float(w[e]) * alpha);
-            tmem_st_x16(tO + c * 16, w);
+            for (int e = 0; e < 64; e += 2) {
+              float a, b;
+              fmul2(a, b, __uint_as_float(w[e]), __uint_as_float(w[e + 1]), alpha, alpha);
+              w[e] = __float_as_uint(a);
+              w[e + 1] = __float_as_uint(b);
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_st_x16(tO + b0 + c * 16, w + c * 16);
           }
         }
       }
-#pragma unroll
-      for (int c = 0; c < BN / 16; ++c) tmem_st_x8(tP + c * 8, pk + c * 8);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
