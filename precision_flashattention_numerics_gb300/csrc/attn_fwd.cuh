@@ -891,9 +891,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
       // overlap it.
       if (j >= 1 && !mbar_wait(&s.p_free, (j - 1) & 1, abort_flag, 0x320)) { ok = false; break; }
       tc_fence_after();
-      // P first: its stores do not depend on the rescale, and their latency overlaps it
+      // P first: its stores do not depend on the rescale, and their latency overlaps it (not
+      // in the fused kernel, where that order makes the 168-register code spill)
+      if constexpr (!FUSED) {
 #pragma unroll
-      for (int c = 0; c < BN / 16; ++c) tmem_st_x8(tP + c * 8, pk + c * 8);
+        for (int c = 0; c < BN / 16; ++c) tmem_st_x8(tP + c * 8, pk + c * 8);
+      }
       if (rescale) {
         if constexpr (F16PV) {
           uint32_t w[16];
@@ -908,26 +911,32 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             tmem_st_x16_unpack16(tO + c * 32, w);
           }
         } else {
-          // 64 columns per load round: one wait per 64 (a heavy-tailed workload rescales
-          // in about a fifth of its warp-blocks, inside the softmax's chain)
+          // kRc columns per load round, one wait each (a heavy-tailed workload rescales in
+          // about a fifth of its warp-blocks, inside the softmax's chain); the fused kernel,
+          // at 168 registers, keeps rounds of 16
+          constexpr int kRc = FUSED ? 16 : 64;
 #pragma unroll
-          for (int b0 = 0; b0 < D; b0 += 64) {
-            uint32_t w[64];
+          for (int b0 = 0; b0 < D; b0 += kRc) {
+            uint32_t w[kRc];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld_x16(tO + b0 + c * 16, w + c * 16);
+            for (int c = 0; c < kRc / 16; ++c) tmem_ld_x16(tO + b0 + c * 16, w + c * 16);
             tmem_ld_wait();
-            reg_fence<64>(w);
+            reg_fence<kRc>(w);
 #pragma unroll
-            for (int e = 0; e < 64; e += 2) {
+            for (int e = 0; e < kRc; e += 2) {
               float a, b;
               fmul2(a, b, __uint_as_float(w[e]), __uint_as_float(w[e + 1]), alpha, alpha);
               w[e] = __float_as_uint(a);
               w[e + 1] = __float_as_uint(b);
             }
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_st_x16(tO + b0 + c * 16, w + c * 16);
+            for (int c = 0; c < kRc / 16; ++c) tmem_st_x16(tO + b0 + c * 16, w + c * 16);
           }
         }
+      }
+      if constexpr (FUSED) {
+#pragma unroll
+        for (int c = 0; c < BN / 16; ++c) tmem_st_x8(tP + c * 8, pk + c * 8);
       }
       tmem_st_wait();
       tc_fence_before();
