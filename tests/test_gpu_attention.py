@@ -3,7 +3,7 @@
 "Online Pseudo-average Shifting Attention (PASA) for Robust Low-precision LLM Inference"
 (arXiv 2503.01873), Abstract: PASA is mathematically equivalent to plain attention, keeps
 fp16 scores from overflowing (65504) under large sequence-dimension bias and Q/K
-resonance, and is judged by RMSE against high-precision attention. Tolerances (output
+resonance, and is evaluated by RMSE against high-precision attention. Tolerances (output
 scale): relRMSE <= 2e-3 and relMax <= 1e-2 on unbiased data; no inf/NaN and relRMSE <= 5e-3
 on biased and resonance data, except where the scores are accumulated in fp16 at
 magnitudes where that cannot hold (resonance keys: shifted scores near 1e4, fp16 spacing
