@@ -750,10 +750,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
       reg_fence<1>(&cw);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&s.s_free[sb]);
-        if constexpr (FUSED) mbar_arrive(&s.c_free[j % KST]);
-      }
+      mbar_arrive_if(&s.s_free[sb], lane == 0);
+      if constexpr (FUSED) mbar_arrive_if(&s.c_free[j % KST], lane == 0);
 
       const int cmax = limit - (jb0 + j) * BN;
       const float c_raw = SHIFT ? __uint_as_float(cw) : 0.0f;
@@ -826,21 +824,20 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
       }
       const float bm = (mx == -INFINITY) ? -INFINITY : (FP8 ? fmaf(mx, fsc, c_raw) : mx + c_raw) * sl2;
       const float m_new = fmaxf(m_run, bm);
-      // Lazy rescale decision; the O rescale itself waits for PV(j-1) further down.
-      float alpha = 1.0f;
-      bool rescale = false;
-      if (j == 0) {
-        m_run = m_new;
+      // Lazy rescale decision, with selects instead of branches; the O rescale itself waits
+      // for PV(j-1) further down. Block 0 takes its max as the running max and leaves l and O.
+      const bool need = m_new > m_run + kRescaleLog2;
+      const bool later = j > 0;
+      const float alpha_n = ex2_approx(m_run - m_new);
+      const float alpha = need ? alpha_n : 1.0f;
+      if constexpr (F16PV) {
+        const float l_s = __half2float(__hmul(__float2half_rn(l_run), __float2half_rn(alpha_n)));
+        l_run = (need && later) ? l_s : l_run;
       } else {
-        const bool need = m_new > m_run + kRescaleLog2;
-        rescale = __any_sync(0xffffffffu, need);
-        if (need) {
-          alpha = ex2_approx(m_run - m_new);
-          if constexpr (F16PV) l_run = __half2float(__hmul(__float2half_rn(l_run), __float2half_rn(alpha)));
-          else l_run *= alpha;
-          m_run = m_new;
-        }
+        l_run = (need && later) ? l_run * alpha_n : l_run;
       }
+      m_run = (need || !later) ? m_new : m_run;
+      const bool rescale = __any_sync(0xffffffffu, need) && later;
       // p = exp2((S' + c) * scale*log2e - m): MUFU ex2 per element, packed fp32 arithmetic per
       // pair, row sums in four independent pair accumulators.
       float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -941,7 +938,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s.p_full);
+      mbar_arrive_if(&s.p_full, lane == 0);
     }
 
     // epilogue: O / l -> fp16 -> swizzled staging (the Q buffer) -> TMA store

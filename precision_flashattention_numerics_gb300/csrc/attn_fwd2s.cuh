@@ -423,7 +423,7 @@ attn_fwd_2set_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_cons
       reg_fence<1>(&cw);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s.s_free[set]);
+      mbar_arrive_if(&s.s_free[set], lane == 0);
 
       const int cmax = limit - j * BN;
       const float c_raw = SHIFT ? __uint_as_float(cw) : 0.0f;
@@ -486,7 +486,7 @@ attn_fwd_2set_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_cons
       const float alpha = need ? ex2_approx(m_prev - m_new) : 1.0f;
       s.xm[set][r] = m_cur;
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s.mxf[quad][set]);
+      mbar_arrive_if(&s.mxf[quad][set], lane == 0);
 
       // p = exp2((S' + c) * scale*log2e - m): MUFU ex2 per element, packed fp32 arithmetic per
       // pair, row sums in four independent pair accumulators.
@@ -544,7 +544,7 @@ attn_fwd_2set_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_cons
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s.p_full);
+      mbar_arrive_if(&s.p_full, lane == 0);
     }
 
     // epilogue: combine the two sets' row sums, O / l -> fp16 -> swizzled staging (the Q
